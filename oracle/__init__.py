@@ -1,0 +1,38 @@
+"""CPU oracle for prefill context-parallel causal attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` use it.  It shares no code, table or
+helper with the CUDA library in ``context_causal_attention_cp_gb300/``.
+
+Everything here is plain Python + NumPy in float64, written to be checked by
+eye against the source pages:
+
+* "Prefill Context Parallelism" (SGLang documentation), sections
+  "Zigzag strategy", "Interleave strategy" and "Attention backend
+  integration" -- the shard layouts and the per-block causal metadata.
+* "什么是 Context Parallelism" (zhifeiding blog), section 2 (the zigzag
+  load-balance figure), section 2.1 (restore index after the all-gather),
+  section 3.1 / 3.3 (partial outputs O_j with their log-sum-exp L_j) and
+  section 3.6 (the LSE merge, a generalisation of FlashAttention's online
+  softmax).
+
+Modules:
+    plan       -- zigzag / interleave shard plans, restore index, tile-load counts
+    attention  -- dense causal attention (per query row) and per-KV-window partials
+    merge      -- the log-sum-exp merge of partial results
+    pipeline   -- plan -> per-shard partial -> [merge] -> restore, end to end
+
+Readings where the pages are silent:
+    R1 remainder tokens of a zigzag split go one each to blocks 0..rem-1;
+    R2 a rank's rows are ordered request by request, early block first;
+    R3 the query at position P sees key positions 0..P of its own request
+       (bottom-right aligned when a cached prefix exists);
+    R4 LSE is the natural log of sum(exp(scale * q.k));
+    R5 query head h reads KV head h // (Hq // Hkv);
+    R6 an empty partial has O = 0 and L = -inf, the identity of the merge.
+The remainder placement (R1) and rank-local order (R2) are fixed by these
+readings only: "parity unpinned" by the pages beyond their even-split examples.
+"""
+
+from . import plan, attention, merge, pipeline  # noqa: F401
