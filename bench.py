@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark: causal prefill context-parallel attention on one GB300.
+
+Default workload: one 32768-token prompt, Llama-3-8B-shaped attention (32
+query / 8 KV heads, head dim 128), CP = 8 zigzag (16 blocks of 2048), bf16
+N(0,1) synthetic inputs.  One step is the whole hot path on the device:
+shard plan -> gather of each shard's query rows -> causal attention of all 8
+shards against the gathered KV in one launch -> restore of O and LSE to
+causal order.  ``value`` is causal attention TFLOP/s over the step
+(2*Hq*(d+dv) flops per visible (query, key) pair), L2 flushed between steps.
+
+The line also carries the LSE-merge GB/s of the 131072-token partial-KV
+decomposition (16 KV blocks of 8192, 136 visible fp32 partials merged and
+scattered to causal order), the restore GB/s, the attention kernel's
+roofline, clocks under load, an end-to-end figure through the public API with
+host buffers, and the CPU oracle timed on a bounded sample of the same
+workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal CP-prefill attention TFLOPS & % of GB300 bf16 peak; LSE-merge GB/s"
+UNIT = "TFLOP/s"
+WORKLOAD = "llama8b_32k"
+MERGE_WORKLOAD = "partialkv_128k"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:  # noqa: BLE001 - the recipe's fallback
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+def visible_pairs(new_lens, prefix_lens):
+    # every new token at position P sees P + 1 keys
+    return sum(n * p + n * (n + 1) // 2 for n, p in zip(new_lens, prefix_lens))
+
+
+def attention_flops(w):
+    return 2.0 * w.Hq * (w.d + w.dv) * visible_pairs(w.new_lens, w.prefix_lens)
+
+
+def config_of(w, extra=None):
+    cfg = {"workload": f"{w.name}: {w.description}", "new_lens": w.new_lens,
+           "prefix_lens": w.prefix_lens, "heads_q": w.Hq, "heads_kv": w.Hkv, "d": w.d,
+           "dv": w.dv, "cp_size": w.cp_size, "strategy": w.strategies[0],
+           "l2": "flushed between steps (256 MiB write outside the step's events)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------- oracle leg --
+def oracle_sample_rate(w, inputs, budget_s, seed=0):
+    """Time the CPU oracle on seeded query rows of the workload for ~budget_s.
+
+    Returns (flops per second, rows, seconds, threads)."""
+    import numpy as np
+    import torch
+    from oracle import attention as oatt
+
+    threads = len(os.sched_getaffinity(0))
+    torch.set_num_threads(threads)
+    k64 = inputs["k"].float().numpy().astype(np.float64)
+    v64 = (k64[:, :, : w.dv] if w.v_is_k_prefix else
+           inputs["v"].float().numpy().astype(np.float64))
+    pos, kv0 = oatt.token_tables(w.new_lens, w.prefix_lens)
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(w.total_new, generator=g).tolist()
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    while done < len(order):
+        i = order[done]
+        q = inputs["q"][i: i + 1].float().numpy().astype(np.float64)
+        oatt.attention_rows(q, k64, v64, pos[i: i + 1], kv0[i: i + 1], w.scale)
+        flops += 2.0 * w.Hq * (w.d + w.dv) * (int(pos[i]) + 1)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt, done, dt, threads
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload]
+    inputs = W.make_inputs(w)
+    rates, rows_total, secs = [], 0, 0.0
+    threads = len(os.sched_getaffinity(0))
+    for s in range(args.warmup + args.steps):
+        rate, rows, dt, threads = oracle_sample_rate(w, inputs, args.ref_step_seconds, seed=s)
+        if s >= args.warmup:
+            rates.append(rate)
+            rows_total += rows
+            secs += dt
+    value = sum(rates) / len(rates) / 1e12
+    ms = attention_flops(w) / (value * 1e12) * 1e3
+    sample = (f"{rows_total} random query rows x all {w.Hq} heads of the workload over "
+              f"{args.steps} steps of ~{args.ref_step_seconds:.0f} s; rate extrapolated to "
+              f"the full workload")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm --
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    strategy = w.strategies[0]
+    inputs = W.make_inputs(w)
+    q = inputs["q"].to(dev)
+    k = inputs["k"].to(dev)
+    v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].to(dev)
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    status = cpa.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, device=dev)
+    ws = {"q_cat": torch.empty_like(q),
+          "o_cat": torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev),
+          "lse_cat": torch.empty((N, Hq), dtype=torch.float32, device=dev),
+          "o": torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev),
+          "lse": torch.empty((N, Hq), dtype=torch.float32, device=dev)}
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        cpa.cp_shard_plan(plan, status=status, stream=stream)
+        qc = cpa.cp_restore(q, plan.gather_idx[:N], out=ws["q_cat"], status=status,
+                            stream=stream)
+        if ev:
+            ev[1].record(stream)
+        cpa.cp_attn_partial(plan.segs, qc, k, v, w.scale, num_segs=plan.total_segs,
+                            tiles=plan.tiles, num_tiles=plan.total_tiles, out=ws["o_cat"],
+                            lse=ws["lse_cat"], status=status, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        cpa.cp_restore(ws["o_cat"], plan.restore_idx[:N], out=ws["o"], status=status,
+                       stream=stream)
+        cpa.cp_restore(ws["lse_cat"], plan.restore_idx[:N], out=ws["lse"], status=status,
+                       stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    launches_per_step = 3 + 1 + 1 + 2   # plan (3 kernels), gather, attention, 2 restores
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, "warmup")
+
+    evs = [[E() for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    cpa.check_status(status, "timed steps")
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    rest_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = attention_flops(w)
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    pk = peaks()
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = flops / (attn_avg_ms * 1e-3) / 1e12
+    restore_bytes = 2 * (N * Hq * dv * 2) + 2 * (N * Hq * 4)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_of(w, {"parallelism": f"replicas{world}"}),
+            "wall_ms_per_step": t_wall * 1e3 / args.steps,
+            "breakdown_ms": {"plan_and_q_gather": sum(prep_ms) / len(prep_ms),
+                             "attention": attn_avg_ms,
+                             "restore_o_lse": sum(rest_ms) / len(rest_ms)},
+            "roofline": {"kernel": "attn_fwd_kernel (tcgen05, 2 heads x 128 rows per CTA)",
+                         "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                         "traffic": None,
+                         "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
+            "restore": {"gbs": restore_bytes / (sum(rest_ms) / len(rest_ms) * 1e-3) / 1e9,
+                        "bytes_per_step": restore_bytes},
+            "clocks": clk.summary(),
+            "gpu_launches": launches_per_step * args.steps}
+    line["restore"]["frac_of_hbm"] = line["restore"]["gbs"] / pk["hbm_gbs"]
+
+    if not args.skip_merge:
+        line["merge"] = bench_merge(args, dev, stream, pk)
+        line["gpu_launches"] += line["merge"].pop("launches")
+    if not args.skip_e2e:
+        line["e2e"] = bench_e2e(args, w, inputs, dev, stream)
+    del q, k, v, ws, flush
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.skip_cpu:
+        rate, rows, dt, threads = oracle_sample_rate(w, inputs, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"{rows} random query rows x all {w.Hq} heads of the "
+                                          f"workload in {dt:.1f} s, fp64 NumPy; rate "
+                                          f"extrapolated to the full workload"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_merge(args, dev, stream, pk):
+    """LSE merge of the 128K partial-KV decomposition (136 fp32 partials)."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    w = W.WORKLOADS[MERGE_WORKLOAD]
+    N, Hq, dv, B = w.total_new, w.Hq, w.dv, w.kv_block
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev)
+    segs = cpa.segments_host(plan)
+    layout, slot_rows = cpa.api.partial_kv_layout(segs, B)
+    g = torch.Generator(device=dev).manual_seed(5)
+    parts_o = torch.randn((slot_rows, Hq, dv), device=dev, generator=g)
+    parts_l = torch.randn((slot_rows, Hq), device=dev, generator=g) * 3 + 10
+    out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    status = cpa.new_status(dev)
+
+    def merge_all():
+        for si, s in enumerate(segs):
+            base, nb = layout[si]
+            ql = s["q_len"]
+            cpa.cp_lse_merge(parts_o[base: base + nb * ql].view(nb, ql, Hq, dv),
+                             parts_l[base: base + nb * ql].view(nb, ql, Hq),
+                             dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql], out=out,
+                             lse_out=lse, num_out_rows=N, status=status, stream=stream)
+
+    for _ in range(3):
+        merge_all()
+    reps = max(3, args.steps // 2)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        merge_all()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    cpa.check_status(status, "merge")
+    read = slot_rows * Hq * (dv + 1) * 4
+    written = N * Hq * (dv * 2 + 4)
+    ms = sorted(times)[len(times) // 2]
+    gbs = (read + written) / (ms * 1e-3) / 1e9
+    del parts_o, parts_l
+    return {"workload": f"{w.name}: {w.description}", "kernel": "lse_merge_kernel",
+            "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"],
+            "bytes_read": read, "bytes_written": written, "parts": slot_rows // (N // 16),
+            "launches": len(segs) * (reps + 3),
+            "note": "partials exceed L2 (18 GB), so every read comes from HBM"}
+
+
+def bench_e2e(args, w, inputs, dev, stream):
+    """Same step through the public API with pinned host inputs and outputs."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+
+    hq = inputs["q"].pin_memory()
+    hk = inputs["k"].pin_memory()
+    hv = None if w.v_is_k_prefix else inputs["v"].pin_memory()
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    ho = torch.empty((N, Hq, dv), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((N, Hq), dtype=torch.float32).pin_memory()
+    q = torch.empty_like(hq, device=dev)
+    k = torch.empty_like(hk, device=dev)
+    v = None if hv is None else torch.empty_like(hv, device=dev)
+    status = cpa.new_status(dev)
+    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], device=dev)
+
+    def one():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        vv = k[:, :, : w.dv] if v is None else v.copy_(hv, non_blocking=True)
+        cpa.cp_shard_plan(plan, status=status, stream=stream)
+        o, lse = cpa.cp_prefill_attention(q, k, vv, plan, w.scale, status=status, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(reps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, "e2e")
+    ms = e0.elapsed_time(e1) / reps
+    h2d = hq.numel() * 2 + hk.numel() * 2 + (0 if hv is None else hv.numel() * 2)
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    return {"value": attention_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "path": "cp_prefill_attention via the C ABI, pinned host q/k/v in, O and LSE out"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-merge", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,23 @@
-"""GB300-native prefill context-parallel causal attention (zigzag / interleave + LSE merge)."""
+"""GB300-native prefill context-parallel causal attention (zigzag / interleave + LSE merge).
+
+The compute path is the C-ABI library ``libcpattn.so`` (CUDA, sm_103a); this
+package holds its thin Python binding (``api``), the in-tree build script and
+the seeded synthetic workloads.  The library is loaded on first use and its
+absence raises: there is no CPU fallback.
+"""
+
+from .api import (  # noqa: F401
+    ShardPlan,
+    alloc_plan,
+    check_status,
+    cp_attn_partial,
+    cp_lse_merge,
+    cp_partial_kv_attention,
+    cp_prefill_attention,
+    cp_restore,
+    cp_shard_plan,
+    cp_shard_plan_sizes,
+    make_plan,
+    new_status,
+    segments_host,
+)

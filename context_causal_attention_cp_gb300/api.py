@@ -1,0 +1,282 @@
+"""Python binding of the C ABI (argument marshalling only).
+
+Every function here converts torch tensors to raw pointers and sizes and calls
+the same-named entry point of ``libcpattn.so``; all device work runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.
+
+Layouts (see include/cpattn.h):
+    q      bf16 [rows, Hq, d]          (cat rows: shard rows in rank order)
+    k, v   bf16 [kv_rows, Hkv, d|dv]   (last dim contiguous; v may view k)
+    o      bf16 or fp32 [rows, Hq, dv]; lse fp32 [rows, Hq] (natural log)
+"""
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import ctypes
+import torch
+
+from . import _lib as L
+
+SEGMENT_FIELDS = ("q_row0", "q_len", "q_pos0", "q_pos_step", "kv_row0", "kv_len", "tok0", "req")
+STRATEGIES = {"zigzag": L.ZIGZAG, "interleave": L.INTERLEAVE}
+
+
+def _strategy(s):
+    if isinstance(s, str):
+        return STRATEGIES[s]
+    return int(s)
+
+
+def _stream(stream):
+    return ctypes.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _i32_array(xs):
+    xs = [int(x) for x in xs]
+    return (ctypes.c_int32 * max(1, len(xs)))(*xs), len(xs)
+
+
+def new_status(device="cuda"):
+    """A zeroed device status word (int32[1])."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status, where="device"):
+    """Synchronise on the status word and raise if a kernel reported an error."""
+    code = int(status.item())
+    if code != L.OK:
+        raise L.CpAttnError(code, where)
+
+
+# --------------------------------------------------------------------- plan --
+def cp_shard_plan_sizes(new_lens: Sequence[int], prefix_lens: Sequence[int], cp_size: int,
+                        strategy):
+    lib = L.load()
+    nl, n = _i32_array(new_lens)
+    pl, n2 = _i32_array(prefix_lens)
+    if n != n2:
+        raise ValueError("new_lens and prefix_lens differ in length")
+    rows = (ctypes.c_int32 * cp_size)()
+    segs = (ctypes.c_int32 * cp_size)()
+    tiles = (ctypes.c_int32 * cp_size)()
+    L.check(lib.cp_shard_plan_sizes(nl, pl, n, cp_size, _strategy(strategy), rows, segs, tiles),
+            "cp_shard_plan_sizes")
+    return list(rows), list(segs), list(tiles)
+
+
+@dataclass
+class ShardPlan:
+    cp_size: int
+    strategy: int
+    rows_per_rank: List[int]
+    segs_per_rank: List[int]
+    tiles_per_rank: List[int]
+    segs: torch.Tensor          # int32 [S, 8] (cp_segment_t)
+    seg_offsets: torch.Tensor   # int32 [C+1]
+    row_offsets: torch.Tensor   # int32 [C+1]
+    gather_idx: torch.Tensor    # int32 [N]
+    positions: torch.Tensor     # int32 [N]
+    restore_idx: torch.Tensor   # int32 [N]
+    tiles: torch.Tensor         # int32 [T, 2]
+    new_lens_dev: torch.Tensor
+    prefix_lens_dev: torch.Tensor
+    num_reqs: int
+
+    @property
+    def total_rows(self):
+        return sum(self.rows_per_rank)
+
+    @property
+    def total_segs(self):
+        return sum(self.segs_per_rank)
+
+    @property
+    def total_tiles(self):
+        return sum(self.tiles_per_rank)
+
+
+def alloc_plan(new_lens, prefix_lens, cp_size, strategy, device="cuda") -> ShardPlan:
+    """Host size pass plus device buffers for a plan (nothing launched)."""
+    rows, segs, tiles = cp_shard_plan_sizes(new_lens, prefix_lens, cp_size, strategy)
+    N, S, T = sum(rows), sum(segs), sum(tiles)
+    i32 = dict(dtype=torch.int32, device=device)
+    return ShardPlan(
+        cp_size=cp_size, strategy=_strategy(strategy), rows_per_rank=rows, segs_per_rank=segs,
+        tiles_per_rank=tiles, segs=torch.empty((max(S, 1), 8), **i32),
+        seg_offsets=torch.empty(cp_size + 1, **i32), row_offsets=torch.empty(cp_size + 1, **i32),
+        gather_idx=torch.empty(max(N, 1), **i32), positions=torch.empty(max(N, 1), **i32),
+        restore_idx=torch.empty(max(N, 1), **i32), tiles=torch.empty((max(T, 1), 2), **i32),
+        new_lens_dev=torch.tensor([int(x) for x in new_lens] or [0], **i32),
+        prefix_lens_dev=torch.tensor([int(x) for x in prefix_lens] or [0], **i32),
+        num_reqs=len(new_lens))
+
+
+def cp_shard_plan(plan: ShardPlan, status=None, stream=None) -> ShardPlan:
+    """Fill ``plan``'s device buffers (kernel launches on ``stream``)."""
+    lib = L.load()
+    L.check(lib.cp_shard_plan(
+        _p(plan.new_lens_dev), _p(plan.prefix_lens_dev), plan.num_reqs, plan.cp_size, plan.strategy,
+        plan.total_rows, plan.total_segs, plan.total_tiles, _p(plan.segs), _p(plan.seg_offsets),
+        _p(plan.row_offsets), _p(plan.gather_idx), _p(plan.positions), _p(plan.restore_idx),
+        _p(plan.tiles), _p(status), _stream(stream)), "cp_shard_plan")
+    return plan
+
+
+def make_plan(new_lens, prefix_lens, cp_size, strategy, device="cuda", status=None,
+              stream=None) -> ShardPlan:
+    return cp_shard_plan(alloc_plan(new_lens, prefix_lens, cp_size, strategy, device), status,
+                         stream)
+
+
+# ---------------------------------------------------------------- attention --
+def cp_attn_partial(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tiles=None,
+                    kv_lo=0, kv_hi=-1, out=None, lse=None, out_fp32=False, out_row_base=0,
+                    num_out_rows=None, status=None, stream=None):
+    """Partial causal attention of every segment row (see cp_attn_partial in cpattn.h)."""
+    lib = L.load()
+    rows, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    if k.shape[1] != Hkv or k.shape[0] != v.shape[0]:
+        raise ValueError("k and v disagree on rows or heads")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k and v must be bfloat16")
+    if not q.is_contiguous() or k.stride(2) != 1 or v.stride(2) != 1:
+        raise ValueError("q must be contiguous; k and v need a contiguous last dim")
+    n_out = rows if num_out_rows is None else num_out_rows
+    if out is None:
+        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((n_out, Hq), dtype=torch.float32, device=q.device)
+    ns = segs.shape[0] if num_segs is None else num_segs
+    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
+    L.check(lib.cp_attn_partial(
+        _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
+        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
+        int(kv_hi), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse), int(out_row_base),
+        out.shape[0], _p(status), _stream(stream)), "cp_attn_partial")
+    return out, lse
+
+
+# -------------------------------------------------------------------- merge --
+def cp_lse_merge(o_parts, lse_parts, *, dst_rows=None, out=None, lse_out=None, out_fp32=True,
+                 num_out_rows=None, status=None, stream=None):
+    """LSE merge over axis 0 of o_parts [n, rows, Hq, dv] / lse_parts [n, rows, Hq]."""
+    lib = L.load()
+    n, rows, Hq, dv = o_parts.shape
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise TypeError("partials must be float32")
+    if o_parts[0].stride() != (Hq * dv, dv, 1) or lse_parts[0].stride() != (Hq, 1):
+        raise ValueError("each partial must be contiguous")
+    n_out = (rows if dst_rows is None else rows) if num_out_rows is None else num_out_rows
+    if out is None:
+        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=o_parts.device)
+    L.check(lib.cp_lse_merge(
+        _p(o_parts), _p(lse_parts), n, o_parts.stride(0), lse_parts.stride(0), rows, Hq, dv,
+        _p(dst_rows), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0],
+        _p(status), _stream(stream)), "cp_lse_merge")
+    return out, lse_out
+
+
+# ------------------------------------------------------------------ restore --
+def cp_restore(src, idx, *, out=None, status=None, stream=None):
+    """out[i] = src[idx[i]] (rows along dim 0)."""
+    lib = L.load()
+    rows = idx.shape[0]
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] > 0 else 0
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    if out is None:
+        out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    L.check(lib.cp_restore(_p(src), src.shape[0], _p(idx), rows, row_bytes, _p(out), _p(status),
+                           _stream(stream)), "cp_restore")
+    return out
+
+
+# --------------------------------------------------------------- pipelines --
+def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream=None,
+                         q_is_cat=False, workspace=None):
+    """Full-KV prefill CP on one GPU: shard rows -> attention -> restore.
+
+    q: bf16 [N, Hq, d] in original (flat) order, or already in cat order when
+    ``q_is_cat``.  Returns (O [N, Hq, dv] bf16, LSE [N, Hq] fp32) in original order.
+    """
+    N, Hq, _ = q.shape
+    dv = v.shape[2]
+    ws = workspace or {}
+    q_cat = q if q_is_cat else cp_restore(q, plan.gather_idx[:N], out=ws.get("q_cat"),
+                                          status=status, stream=stream)
+    o_cat, lse_cat = cp_attn_partial(plan.segs, q_cat, k, v, scale, num_segs=plan.total_segs,
+                                     tiles=plan.tiles, num_tiles=plan.total_tiles,
+                                     out=ws.get("o_cat"), lse=ws.get("lse_cat"),
+                                     status=status, stream=stream)
+    o = cp_restore(o_cat, plan.restore_idx[:N], out=ws.get("o"), status=status, stream=stream)
+    lse = cp_restore(lse_cat, plan.restore_idx[:N], out=ws.get("lse"), status=status,
+                     stream=stream)
+    return o, lse
+
+
+def segments_host(plan: ShardPlan):
+    """Copy the plan's segment table to the host (list of dicts)."""
+    s = plan.segs[: plan.total_segs].cpu().tolist()
+    return [dict(zip(SEGMENT_FIELDS, row)) for row in s]
+
+
+def partial_kv_layout(segs_host, kv_block):
+    """Visible KV blocks per segment and the offset of its partial slots."""
+    out, slot = [], 0
+    for s in segs_host:
+        last_pos = s["q_pos0"] + (s["q_len"] - 1) * s["q_pos_step"]
+        nb = last_pos // kv_block + 1
+        out.append((slot, nb))
+        slot += nb * s["q_len"]
+    return out, slot
+
+
+def cp_partial_kv_attention(q_cat, k, v, plan: ShardPlan, scale, kv_block, *, segs_host=None,
+                            parts_o=None, parts_lse=None, out=None, lse_out=None, status=None,
+                            stream=None):
+    """Partial-KV (ring-style) CP on one GPU.
+
+    Every segment's rows meet the KV one block of ``kv_block`` keys at a time
+    (fp32 partial O_j and L_j per visible block), then the partials are
+    LSE-merged and scattered straight to original token order.
+    Returns (O [N, Hq, dv] bf16, LSE [N, Hq]).
+    """
+    N, Hq, _ = q_cat.shape
+    dv = v.shape[2]
+    segs_host = segs_host or segments_host(plan)
+    layout, total_slot_rows = partial_kv_layout(segs_host, kv_block)
+    dev = q_cat.device
+    if parts_o is None:
+        parts_o = torch.empty((total_slot_rows, Hq, dv), dtype=torch.float32, device=dev)
+    if parts_lse is None:
+        parts_lse = torch.empty((total_slot_rows, Hq), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    for si, s in enumerate(segs_host):
+        base, nb = layout[si]
+        ql = s["q_len"]
+        for j in range(nb):
+            o_j = parts_o[base + j * ql: base + (j + 1) * ql]
+            l_j = parts_lse[base + j * ql: base + (j + 1) * ql]
+            cp_attn_partial(plan.segs[si: si + 1], q_cat, k, v, scale, kv_lo=j * kv_block,
+                            kv_hi=(j + 1) * kv_block, out=o_j, lse=l_j,
+                            out_row_base=s["q_row0"], num_out_rows=ql, status=status,
+                            stream=stream)
+    for si, s in enumerate(segs_host):
+        base, nb = layout[si]
+        ql = s["q_len"]
+        o_parts = parts_o[base: base + nb * ql].view(nb, ql, Hq, dv)
+        l_parts = parts_lse[base: base + nb * ql].view(nb, ql, Hq)
+        cp_lse_merge(o_parts, l_parts, dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql],
+                     out=out, lse_out=lse_out, num_out_rows=N, status=status, stream=stream)
+    return out, lse_out

@@ -1,0 +1,576 @@
+// Shard partial attention for prefill context parallelism on sm_103a.
+//
+// Computes, for every query row of every segment and every query head, the
+// causal attention output O and its log-sum-exp L against the gathered KV
+// (blog "什么是 Context Parallelism", §3.1/§3.3: each rank's queries against a
+// KV block give a partial O_j with L_j; SGLang docs, "Prefill Context
+// Parallelism", §Attention backend integration: the early and late zigzag
+// blocks run with their own query and KV lengths, including any cached
+// prefix).  One launch covers every segment of every shard.
+//
+// Design (one CTA = one 128-row query tile of one segment, for NQ query
+// heads that share one KV head):
+//   warp 4*NQ      TMA producer: Q tiles once, then K and V tiles of 128 keys
+//                  through KST / VST-stage rings (128-byte swizzled boxes).
+//   warp 4*NQ+1    MMA issuer (one thread): S_s = Q_s K^T into TMEM
+//                  (tcgen05.mma, both operands from shared memory) and
+//                  O_s += P_s V with P_s read from TMEM.  For NQ = 2 the two
+//                  tiles ping-pong: while tile 0's softmax runs, the tensor
+//                  core works on tile 1 and vice versa.
+//   warps 0..4NQ-1 softmax, one warpgroup per query tile, one thread per row:
+//                  tcgen05.ld of the S row, causal/window mask only on tiles
+//                  that cross the diagonal or the window edge, online softmax
+//                  in base 2, O rescale in TMEM when the row max grows, P
+//                  written back to TMEM as bf16 (aliasing the S columns), and
+//                  the epilogue (O / l, L = ln(sum)) straight to global memory.
+// Every mbarrier wait is bounded; a wait that runs out sets
+// CPATTN_ERR_TIMEOUT, the CTA drains its own in-flight work and frees TMEM.
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "../../include/cpattn.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int BM = CPATTN_TILE_ROWS;  // query rows per tile (MMA M)
+constexpr int BN = 128;               // keys per KV tile (MMA N of Q K^T)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct AttnParams {
+  const cp_segment_t* segs;
+  const int32_t* tiles;
+  int num_segs, num_tiles;
+  int Hq, g, n_hgroups;
+  float scale_log2;
+  int kv_lo, kv_hi;
+  void* o;
+  int o_f32;
+  float* lse;
+  int out_row_base, num_out_rows, num_q_rows, num_kv_rows;
+  int32_t* status;
+  unsigned long long timeout_ns;
+};
+
+template <int D, int DV, int NQ, int KST, int VST>
+struct Cfg {
+  static constexpr int kThreads = NQ * 128 + 64;
+  static constexpr int kProducerWarp = NQ * 4;
+  static constexpr int kMmaWarp = NQ * 4 + 1;
+  static constexpr int kQTileBytes = BM * D * 2;
+  static constexpr int kKTileBytes = BN * D * 2;
+  static constexpr int kVTileBytes = BN * DV * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + NQ * kQTileBytes;
+  static constexpr int kVOff = kKOff + KST * kKTileBytes;
+  static constexpr int kBarOff = kVOff + VST * kVTileBytes;
+  static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 3 * NQ + 1;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + align slack
+  static constexpr int kTmemNeed = NQ * (BN + DV);
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256 : 512;
+  static_assert(kTmemNeed <= 512, "TMEM budget");
+  static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= 256, "head dims");
+};
+
+// Warp-uniform bounded wait: every lane polls, the give-up decision is lane 0's.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort, uint64_t timeout) {
+  const int lane = threadIdx.x & 31;
+  uint64_t t0 = lane == 0 ? global_timer_ns() : 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 63u) == 63u) {
+      int give_up = 0;
+      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > timeout);
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+template <int D, int DV, int NQ, int KST, int VST>
+__global__ void __launch_bounds__(Cfg<D, DV, NQ, KST, VST>::kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using C = Cfg<D, DV, NQ, KST, VST>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* bar_q = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + KST;
+  uint64_t* v_full = k_empty + KST;
+  uint64_t* v_empty = v_full + VST;
+  uint64_t* s_full = v_empty + VST;
+  uint64_t* p_full = s_full + NQ;
+  uint64_t* o_full = p_full + NQ;
+  uint64_t* bar_drain = o_full + NQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item: (tile of 128 rows of one segment, group of NQ heads) ----
+  const int hg = blockIdx.x % p.n_hgroups;
+  const int tile_idx = blockIdx.x / p.n_hgroups;
+  int seg_id = -1, t = 0;
+  if (p.tiles) {
+    if (tile_idx >= p.num_tiles) return;
+    seg_id = __ldg(p.tiles + 2 * tile_idx);
+    t = __ldg(p.tiles + 2 * tile_idx + 1);
+    if (seg_id < 0 || seg_id >= p.num_segs) {
+      if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+      return;
+    }
+  } else {
+    int acc = 0;
+    for (int s = 0; s < p.num_segs; ++s) {
+      const int ql = __ldg(&p.segs[s].q_len);
+      const int nt = ql > 0 ? (ql + BM - 1) / BM : 0;
+      if (tile_idx < acc + nt) { seg_id = s; t = tile_idx - acc; break; }
+      acc += nt;
+    }
+    if (seg_id < 0) return;
+  }
+  const cp_segment_t sg = p.segs[seg_id];
+  {
+    const long long last_pos = (long long)sg.q_pos0 + (long long)(sg.q_len - 1) * sg.q_pos_step;
+    const bool bad = sg.q_len <= 0 || sg.q_row0 < 0 || (long long)sg.q_row0 + sg.q_len > p.num_q_rows ||
+                     sg.q_pos0 < 0 || sg.q_pos_step < 1 || sg.kv_row0 < 0 ||
+                     (long long)sg.kv_row0 + sg.kv_len > p.num_kv_rows ||
+                     (long long)sg.q_row0 - p.out_row_base < 0 ||
+                     (long long)sg.q_row0 + sg.q_len - p.out_row_base > p.num_out_rows ||
+                     last_pos + 1 > sg.kv_len || t < 0 || (long long)t * BM >= sg.q_len;
+    if (bad) {
+      if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+      return;
+    }
+  }
+  const int r0 = t * BM;
+  const int rows_valid = min(BM, sg.q_len - r0);
+  const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
+  const int win_lo = max(p.kv_lo, 0);
+  const int win_hi_tile = p.kv_hi < 0 ? pos_max + 1 : min(p.kv_hi, pos_max + 1);
+  const int j0 = win_lo / BN;
+  const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + BN - 1) / BN - j0 : 0;
+  const int head0 = hg * NQ;            // query heads head0 .. head0+NQ-1
+  const int kv_head = head0 / p.g;      // shared by all NQ heads (g % NQ == 0)
+
+  // ---- setup: barriers, TMEM ----
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int i = 0; i < KST; ++i) { mbar_init(k_full + i, 1); mbar_init(k_empty + i, 1); }
+    for (int i = 0; i < VST; ++i) { mbar_init(v_full + i, 1); mbar_init(v_empty + i, 1); }
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(s_full + s, 1);
+      mbar_init(p_full + s, 128);
+      mbar_init(o_full + s, 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::kProducerWarp) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const uint32_t q_base = smem_u32(smem + C::kQOff);
+  const uint32_t k_base = smem_u32(smem + C::kKOff);
+  const uint32_t v_base = smem_u32(smem + C::kVOff);
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0 && n_kv > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(bar_q, NQ * C::kQTileBytes);
+      for (int s = 0; s < NQ; ++s)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kQOff + s * C::kQTileBytes + c * BM * 128, &tm_q, bar_q, c * 64,
+                      head0 + s, sg.q_row0 + r0);
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int it = 0; it < n_kv && ok; ++it) {
+        const int kv_row = sg.kv_row0 + (j0 + it) * BN;
+        const int ks = it % KST;
+        ok = mbar_wait(k_empty + ks, ((it / KST) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(k_full + ks, C::kKTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kKOff + ks * C::kKTileBytes + c * BN * 128, &tm_k, k_full + ks,
+                      c * 64, kv_head, kv_row);
+        ++k_issued;
+        const int vs = it % VST;
+        ok = mbar_wait(v_empty + vs, ((it / VST) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(v_full + vs, C::kVTileBytes);
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(smem + C::kVOff + vs * C::kVTileBytes + c * BN * 128, &tm_v, v_full + vs,
+                      c * 64, kv_head, kv_row);
+        ++v_issued;
+      }
+      if (!ok) {
+        set_status(p.status, CPATTN_ERR_TIMEOUT);
+        *abort_flag = 1;
+        // let this CTA's own copies land before the shared memory is released
+        mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
+        for (int i = std::max(0, k_issued - KST); i < k_issued; ++i)
+          mbar_wait(k_full + i % KST, (i / KST) & 1, nullptr, p.timeout_ns);
+        for (int i = std::max(0, v_issued - VST); i < v_issued; ++i)
+          mbar_wait(v_full + i % VST, (i / VST) & 1, nullptr, p.timeout_ns);
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer --
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, 0, 1);
+      auto issue_qk = [&](int s, int ks) {
+        const uint32_t qa = q_base + s * C::kQTileBytes;
+        const uint32_t ka = k_base + ks * C::kKTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_q = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          const uint32_t off_k = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
+          mma_ss(tmem_base + s * BN, smem_desc_sw128(qa + off_q, 16, 1024),
+                 smem_desc_sw128(ka + off_k, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int s, int vs, bool acc) {
+        const uint32_t va = v_base + vs * C::kVTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_ts(tmem_base + NQ * BN + s * DV, tmem_base + s * BN + kk * 8,
+                 smem_desc_sw128(va + kk * 16 * 128, BN * 128, 1024), kIdescPV,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
+      if (ok) ok = mbar_wait(k_full, 0, abort_flag, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        for (int s = 0; s < NQ; ++s) {
+          issue_qk(s, 0);
+          mma_commit(s_full + s);
+        }
+        mma_commit(k_empty);
+      }
+      for (int it = 0; it < n_kv && ok; ++it) {
+        const int vs = it % VST;
+        ok = mbar_wait(v_full + vs, (it / VST) & 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        const int ks_next = (it + 1) % KST;
+        for (int s = 0; s < NQ && ok; ++s) {
+          ok = mbar_wait(p_full + s, it & 1, abort_flag, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(s, vs, it > 0);
+          if (it == n_kv - 1) mma_commit(o_full + s);
+          if (it + 1 < n_kv) {
+            if (s == 0) {
+              ok = mbar_wait(k_full + ks_next, ((it + 1) / KST) & 1, abort_flag, p.timeout_ns);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(s, ks_next);
+            mma_commit(s_full + s);
+          }
+        }
+        if (!ok) break;
+        mma_commit(v_empty + vs);
+        if (it + 1 < n_kv) mma_commit(k_empty + ks_next);
+      }
+      if (!ok) {
+        set_status(p.status, CPATTN_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // drain: every MMA and commit issued by this thread has completed
+      mma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, nullptr, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax --
+    const int s = warp >> 2;               // query tile / head of this warpgroup
+    const int wq = warp & 3;               // TMEM lane quarter
+    const int row = wq * 32 + lane;        // row within the tile
+    const bool valid = row < rows_valid;
+    const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
+    const int row_hi = valid ? (p.kv_hi < 0 ? pos + 1 : min(p.kv_hi, pos + 1)) : 0;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_col = s * BN, o_col = NQ * BN + s * DV;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_kv; ++it) {
+      ok = mbar_wait_warp(s_full + s, it & 1, abort_flag, p.timeout_ns);
+      if (!ok) break;
+      tc_fence_after();
+      float x[BN];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) {
+          tmem_ld32(lane_addr + s_col + q * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[q * 32 + c] = __uint_as_float(r[c]);
+        }
+      }
+      const int key0 = (j0 + it) * BN;
+      if (key0 < win_lo || key0 + BN > row_hi) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int key = key0 + c;
+          if (key < win_lo || key >= row_hi) x[c] = -INFINITY;
+        }
+      }
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+      for (int c = 4; c < BN; c += 4) {
+        mx0 = fmaxf(mx0, x[c]);
+        mx1 = fmaxf(mx1, x[c + 1]);
+        mx2 = fmaxf(mx2, x[c + 2]);
+        mx3 = fmaxf(mx3, x[c + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = fmaxf(m_run, mx);
+      const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m_run - m_new_use);  // 0 while m_run = -inf
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float a = ex2_approx(fmaf(x[q * 32 + c], sl2, -m_new_use));
+          const float b = ex2_approx(fmaf(x[q * 32 + c + 1], sl2, -m_new_use));
+          sum0 += a;
+          sum1 += b;
+          pk[c >> 1] = pack_bf16x2(a, b);
+        }
+        tmem_st16(lane_addr + s_col + q * 16, pk);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      // rescale the running O (its previous PV has completed: S of this
+      // iteration was committed after it)
+      const bool need = (it > 0) && (alpha != 1.f);
+      if (__any_sync(0xffffffffu, need)) {
+        const float a = need ? alpha : 1.f;
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) {
+          tmem_ld32(lane_addr + o_col + q * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * a);
+          tmem_st32(lane_addr + o_col + q * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + s);
+      m_run = m_new;
+      m_use = m_new_use;
+    }
+    if (ok && n_kv > 0) ok = mbar_wait_warp(o_full + s, 0, abort_flag, p.timeout_ns);
+    if (!ok) {
+      if (lane == 0) {
+        set_status(p.status, CPATTN_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    } else {
+      tc_fence_after();
+      const int h = head0 + s;
+      const long long out_row = (long long)sg.q_row0 + r0 + row - p.out_row_base;
+      const bool has = l_run > 0.f;
+      const float inv = has ? 1.f / l_run : 0.f;
+#pragma unroll
+      for (int q = 0; q < DV / 32; ++q) {
+        uint32_t r[32];
+        if (n_kv > 0) {
+          tmem_ld32(lane_addr + o_col + q * 32, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (valid) {
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * inv;
+          const long long off = (out_row * p.Hq + h) * DV + q * 32;
+          if (p.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                  pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                  pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                  pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+          }
+        }
+      }
+      if (valid)
+        p.lse[out_row * p.Hq + h] = has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY;
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kProducerWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------- host --
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 map (cols, heads, rows) with a 64-column x 1-head x 128-row box,
+// 128-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, int cols, int heads, long long rows,
+              long long head_stride_el, long long row_stride_el) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)(head_stride_el * 2), (cuuint64_t)(row_stride_el * 2)};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int DV, int NQ, int KST, int VST>
+int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                const AttnParams& prm, long long tiles, cudaStream_t stream) {
+  using C = Cfg<D, DV, NQ, KST, VST>;
+  auto kern = attn_fwd_kernel<D, DV, NQ, KST, VST>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    configured = true;
+  }
+  const long long grid = tiles * prm.n_hgroups;
+  if (grid <= 0) return CPATTN_OK;
+  if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
+  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                               int num_tiles, const void* q, int num_q_rows, const void* k,
+                               int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                               int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                               int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
+                               int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
+                               int32_t* status_dev, cudaStream_t stream) {
+  if (num_segs < 0 || num_q_rows < 0 || num_kv_rows < 0 || num_out_rows < 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || !(scale > 0.f)) return CPATTN_ERR_INVALID_ARG;
+  const bool shape_ok = (d == 64 && dv == 64) || (d == 128 && dv == 128);
+  if (!shape_ok) return CPATTN_ERR_UNSUPPORTED;
+  if (tiles_dev && num_tiles < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_segs == 0 || (tiles_dev && num_tiles == 0)) return CPATTN_OK;
+  if (!segs_dev || !q || !k || !v || !o || !lse) return CPATTN_ERR_INVALID_ARG;
+  if (num_q_rows == 0 || num_kv_rows == 0 || num_out_rows == 0) return CPATTN_ERR_INVALID_ARG;
+  if (!a16(segs_dev) || !a16(q) || !a16(k) || !a16(v) || !a16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(tiles_dev) & 7u))
+    return CPATTN_ERR_ALIGNMENT;
+  if ((k_row_stride * 2) % 16 || (k_head_stride * 2) % 16 || (v_row_stride * 2) % 16 ||
+      (v_head_stride * 2) % 16)
+    return CPATTN_ERR_ALIGNMENT;
+  if (k_head_stride < d || v_head_stride < dv || k_row_stride < (int64_t)(Hkv - 1) * k_head_stride + d ||
+      v_row_stride < (int64_t)(Hkv - 1) * v_head_stride + dv)
+    return CPATTN_ERR_INVALID_ARG;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, d, Hq, num_q_rows, d, (long long)Hq * d) ||
+      !make_map(&mk, k, d, Hkv, num_kv_rows, k_head_stride, k_row_stride) ||
+      !make_map(&mv, v, dv, Hkv, num_kv_rows, v_head_stride, v_row_stride))
+    return CPATTN_ERR_CUDA;
+
+  const int g = Hq / Hkv;
+  const int nq = (g % 2 == 0) ? 2 : 1;
+  AttnParams prm;
+  prm.segs = segs_dev;
+  prm.tiles = tiles_dev;
+  prm.num_segs = num_segs;
+  prm.num_tiles = tiles_dev ? num_tiles : 0;
+  prm.Hq = Hq;
+  prm.g = g;
+  prm.n_hgroups = Hq / nq;
+  prm.scale_log2 = scale * kLog2e;
+  prm.kv_lo = kv_lo;
+  prm.kv_hi = kv_hi;
+  prm.o = o;
+  prm.o_f32 = o_is_fp32 ? 1 : 0;
+  prm.lse = lse;
+  prm.out_row_base = out_row_base;
+  prm.num_out_rows = num_out_rows;
+  prm.num_q_rows = num_q_rows;
+  prm.num_kv_rows = num_kv_rows;
+  prm.status = status_dev;
+  prm.timeout_ns = 4000000000ull;
+  const long long tiles =
+      tiles_dev ? num_tiles : ((long long)num_q_rows + BM - 1) / BM + (long long)num_segs;
+
+  if (d == 128) {
+    if (nq == 2) return launch_attn<128, 128, 2, 2, 2>(mq, mk, mv, prm, tiles, stream);
+    return launch_attn<128, 128, 1, 2, 2>(mq, mk, mv, prm, tiles, stream);
+  }
+  if (nq == 2) return launch_attn<64, 64, 2, 3, 3>(mq, mk, mv, prm, tiles, stream);
+  return launch_attn<64, 64, 1, 3, 3>(mq, mk, mv, prm, tiles, stream);
+}

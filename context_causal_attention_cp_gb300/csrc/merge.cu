@@ -1,0 +1,231 @@
+// LSE merge of partial attention results and the restore (row gather).
+//
+// Merge (blog "什么是 Context Parallelism", §3.6, the shared component of
+// pass-KV and pass-Q): partial j carries a normalised output O_j and its
+// log-sum-exp L_j; with m = max_j L_j and w_j = exp(L_j - m) the exact result
+// is L = m + ln(sum_j w_j) and O = sum_j w_j O_j / sum_j w_j.
+// Restore (same blog, §2.1): a restore index puts the all-gathered shard rows
+// back into causal token order.
+//
+// Both kernels are HBM-bound streams: one warp per (row, head) merge unit with
+// 16-byte loads of every partial issued before any use, and a flat
+// grid-stride 16-byte copy for the gather.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "../../include/cpattn.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int kMergeThreads = 256;
+constexpr int kMaxParts = 32;
+
+__device__ __forceinline__ float4 ld_stream(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Each warp merges one (row, head) unit per iteration; lane j < num_parts
+// holds L_j.  dv is split in 128-float chunks, one float4 per lane.
+template <bool OUT_F32, int NP>
+__global__ void __launch_bounds__(kMergeThreads)
+lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                 int num_parts, int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
+                 const int32_t* __restrict__ dst_rows, void* __restrict__ o_out,
+                 float* __restrict__ lse_out, int num_out_rows, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long units = (long long)rows * Hq;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long u = warp0; u < units; u += nwarps) {
+    const int row = (int)(u / Hq), h = (int)(u % Hq);
+    int out_row = row;
+    if (dst_rows) {
+      out_row = __ldg(dst_rows + row);
+      if (out_row < 0 || out_row >= num_out_rows) {
+        if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+        continue;
+      }
+    }
+    float lj = -INFINITY;
+    if (lane < num_parts) lj = __ldg(lse_parts + lane * l_stride + u);
+    float m = lj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const bool empty = (m == -INFINITY);
+    const float wj = (lane < num_parts && !empty) ? __expf(lj - m) : 0.f;
+    float ws = wj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    const float inv = empty ? 0.f : 1.f / ws;
+    const float* base = o_parts + u * dv;
+    for (int c = lane * 4; c < dv; c += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (NP > 0) {
+        float4 v[NP > 0 ? NP : 1];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) v[j] = ld_stream(base + j * o_stride + c);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          const float w = __shfl_sync(0xffffffffu, wj, j);
+          acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+        }
+      } else {
+        int j = 0;
+        for (; j + 4 <= num_parts; j += 4) {
+          float4 v0 = ld_stream(base + (j + 0) * o_stride + c);
+          float4 v1 = ld_stream(base + (j + 1) * o_stride + c);
+          float4 v2 = ld_stream(base + (j + 2) * o_stride + c);
+          float4 v3 = ld_stream(base + (j + 3) * o_stride + c);
+          const float w0 = __shfl_sync(0xffffffffu, wj, j + 0);
+          const float w1 = __shfl_sync(0xffffffffu, wj, j + 1);
+          const float w2 = __shfl_sync(0xffffffffu, wj, j + 2);
+          const float w3 = __shfl_sync(0xffffffffu, wj, j + 3);
+          acc.x += w0 * v0.x + w1 * v1.x + w2 * v2.x + w3 * v3.x;
+          acc.y += w0 * v0.y + w1 * v1.y + w2 * v2.y + w3 * v3.y;
+          acc.z += w0 * v0.z + w1 * v1.z + w2 * v2.z + w3 * v3.z;
+          acc.w += w0 * v0.w + w1 * v1.w + w2 * v2.w + w3 * v3.w;
+        }
+        for (; j < num_parts; ++j) {
+          float4 v0 = ld_stream(base + j * o_stride + c);
+          const float w0 = __shfl_sync(0xffffffffu, wj, j);
+          acc.x += w0 * v0.x; acc.y += w0 * v0.y; acc.z += w0 * v0.z; acc.w += w0 * v0.w;
+        }
+      }
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+      const long long oo = ((long long)out_row * Hq + h) * dv + c;
+      if (OUT_F32) {
+        __stcs(reinterpret_cast<float4*>(static_cast<float*>(o_out) + oo), acc);
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oo), pk);
+      }
+    }
+    if (lse_out && lane == 0)
+      lse_out[(long long)out_row * Hq + h] = empty ? -INFINITY : m + __logf(ws);
+  }
+}
+
+// dst[i] = src[idx[i]]: 16-byte chunks, consecutive threads on consecutive
+// chunks of the same row.
+__global__ void __launch_bounds__(256)
+row_gather_kernel(const uint4* __restrict__ src, int num_src_rows, const int32_t* __restrict__ idx,
+                  int rows, long long chunks_per_row, uint4* __restrict__ dst, int32_t* status) {
+  const long long total = (long long)rows * chunks_per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
+    const long long row = e / chunks_per_row, col = e - row * chunks_per_row;
+    const int s = __ldg(idx + row);
+    if (s < 0 || s >= num_src_rows) {
+      if (col == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const uint4 v = __ldcs(src + (long long)s * chunks_per_row + col);
+    __stcs(dst + e, v);
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <bool F32>
+void launch_merge(int grid, cudaStream_t st, const float* o_parts, const float* lse_parts,
+                  int num_parts, int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
+                  const int32_t* dst_rows, void* o_out, float* lse_out, int num_out_rows,
+                  int32_t* status) {
+#define CPATTN_MERGE_CASE(NPV)                                                                  \
+  lse_merge_kernel<F32, NPV><<<grid, kMergeThreads, 0, st>>>(o_parts, lse_parts, num_parts,    \
+                                                             o_stride, l_stride, rows, Hq, dv, \
+                                                             dst_rows, o_out, lse_out,         \
+                                                             num_out_rows, status)
+  switch (num_parts) {
+    case 2: CPATTN_MERGE_CASE(2); break;
+    case 4: CPATTN_MERGE_CASE(4); break;
+    case 8: CPATTN_MERGE_CASE(8); break;
+    case 16: CPATTN_MERGE_CASE(16); break;
+    default: CPATTN_MERGE_CASE(0); break;
+  }
+#undef CPATTN_MERGE_CASE
+}
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int num_parts,
+                            int64_t o_part_stride, int64_t lse_part_stride, int rows, int Hq,
+                            int dv, const int32_t* dst_rows, void* o_out, int o_out_is_fp32,
+                            float* lse_out, int num_out_rows, int32_t* status_dev,
+                            cudaStream_t stream) {
+  if (num_parts < 1 || num_parts > kMaxParts) return CPATTN_ERR_INVALID_ARG;
+  if (rows < 0 || Hq < 1 || dv < 4 || dv > 1024 || (dv % 4) != 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_out_rows < 0 || (!dst_rows && num_out_rows < rows)) return CPATTN_ERR_INVALID_ARG;
+  if (rows == 0) return CPATTN_OK;
+  if (!o_parts || !lse_parts || !o_out) return CPATTN_ERR_INVALID_ARG;
+  if (num_parts > 1 && (o_part_stride < (int64_t)rows * Hq * dv ||
+                        lse_part_stride < (int64_t)rows * Hq))
+    return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o_out) || (o_part_stride % 4) != 0 ||
+      (reinterpret_cast<uintptr_t>(lse_parts) & 3u) || (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+    return CPATTN_ERR_ALIGNMENT;
+  const long long units = (long long)rows * Hq;
+  const long long want = (units + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
+  const int grid = (int)std::min<long long>(want, (long long)sm_count() * 16);
+  if (o_out_is_fp32)
+    launch_merge<true>(grid, stream, o_parts, lse_parts, num_parts, o_part_stride,
+                       lse_part_stride, rows, Hq, dv, dst_rows, o_out, lse_out, num_out_rows,
+                       status_dev);
+  else
+    launch_merge<false>(grid, stream, o_parts, lse_parts, num_parts, o_part_stride,
+                        lse_part_stride, rows, Hq, dv, dst_rows, o_out, lse_out, num_out_rows,
+                        status_dev);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+extern "C" int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int rows,
+                          int64_t row_bytes, void* dst, int32_t* status_dev, cudaStream_t stream) {
+  if (rows < 0 || num_src_rows < 0 || row_bytes <= 0 || (row_bytes % 16) != 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (rows == 0) return CPATTN_OK;
+  if (!src || !dst || !idx_dev) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(idx_dev) & 3u))
+    return CPATTN_ERR_ALIGNMENT;
+  const long long cpr = row_bytes / 16;
+  const long long total = (long long)rows * cpr;
+  const int grid = (int)std::min<long long>((total + 255) / 256, (long long)sm_count() * 8);
+  row_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), num_src_rows, idx_dev,
+                                              rows, cpr, static_cast<uint4*>(dst), status_dev);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+extern "C" const char* cp_status_string(int status) {
+  switch (status) {
+    case CPATTN_OK: return "ok";
+    case CPATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CPATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case CPATTN_ERR_CUDA: return "CUDA error";
+    case CPATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case CPATTN_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case CPATTN_ERR_RANGE: return "index or segment out of range";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,194 @@
+/*
+ * cpattn.h -- C ABI of the GB300 (sm_103a) prefill context-parallel causal
+ * attention library.
+ *
+ * The hot path: shard a batch's new (uncached) query tokens over C logical
+ * context-parallel (CP) ranks, compute every shard's causal attention against
+ * the gathered KV (one KV buffer in HBM that all shards read) as a partial
+ * output O with its log-sum-exp L, merge partials with the log-sum-exp rule
+ * and put the result back in causal token order.
+ *
+ * Sources (the behaviour each call implements is defined there):
+ *   [SGL-ZZ]  SGLang docs, "Prefill Context Parallelism", section "Zigzag strategy"
+ *   [SGL-IL]  same page, section "Interleave strategy"
+ *   [SGL-BE]  same page, section "Attention backend integration"
+ *   [CPB-2.1] blog "什么是 Context Parallelism" (zhifeiding), section 2.1
+ *             (all-gather KV; restore index after the all-gather)
+ *   [CPB-3.3] same blog, sections 3.1 and 3.3 (per-shard partial O_j and LSE L_j)
+ *   [CPB-3.6] same blog, section 3.6 (merging partials: online-softmax / LSE rule)
+ *
+ * Conventions for every call:
+ *   - Return value: CPATTN_OK (0) or a negative CPATTN_ERR_* code.  Argument
+ *     errors are detected on the host and returned synchronously; nothing is
+ *     launched then.  No C++ exception crosses this boundary.
+ *   - Device work is asynchronous on the given stream.  Errors detected on the
+ *     device (bad segment metadata, an index out of range, a pipeline wait that
+ *     ran out) are written to the optional device word *status_dev (first error
+ *     wins; the caller zeroes it) and the offending work is skipped; the kernel
+ *     never traps.
+ *   - Ownership: the caller allocates and owns every buffer.  The library
+ *     allocates no device or host memory and writes only to output pointers.
+ *   - Device pointers must be 16-byte aligned (checked: CPATTN_ERR_ALIGNMENT).
+ *   - Tokens: the batch's new tokens are flattened in request order ("flat
+ *     index").  Request b has new_lens[b] new tokens at positions
+ *     prefix_lens[b] .. prefix_lens[b]+new_lens[b]-1 (positions count the
+ *     cached prefix).  The KV buffer holds, per request in batch order, key
+ *     positions 0 .. prefix_lens[b]+new_lens[b]-1 (prefix first).
+ *   - Shard order: "cat" rows are all shards' rows concatenated in rank order
+ *     (rank 0's rows, then rank 1's, ...): the layout an all-gather produces.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CPATTN_OK 0
+#define CPATTN_ERR_INVALID_ARG (-1)  /* bad size, count, enum or metadata */
+#define CPATTN_ERR_UNSUPPORTED (-2)  /* valid but unsupported shape (head dims, ...) */
+#define CPATTN_ERR_CUDA (-3)         /* a CUDA runtime/driver call failed */
+#define CPATTN_ERR_TIMEOUT (-4)      /* device: a pipeline wait exceeded its time limit */
+#define CPATTN_ERR_ALIGNMENT (-5)    /* a pointer or stride is not 16-byte aligned */
+#define CPATTN_ERR_RANGE (-6)        /* device: an index or segment lies outside its buffer */
+
+typedef enum { CP_ZIGZAG = 0, CP_INTERLEAVE = 1 } cp_strategy_t;
+
+/* One segment: a maximal run of one rank's query rows that belong to one
+ * request and whose positions advance by a constant step.  Row i of the
+ * segment (0 <= i < q_len) is cat row q_row0 + i, has position
+ * q_pos0 + i * q_pos_step and flat index tok0 + i * q_pos_step, and attends to
+ * key positions 0 .. its position (KV rows kv_row0 + key position).
+ * Zigzag: one segment per non-empty block, q_pos_step = 1.  Interleave: one
+ * segment per (rank, request) with rows in it, q_pos_step = C.
+ * [SGL-ZZ] "separate query and KV lengths for the early and late blocks,
+ * including any cached prefix"; [SGL-IL] "per-request sharding metadata
+ * preserves those boundaries and each query's causal extent". */
+typedef struct {
+  int32_t q_row0;     /* first cat row of the segment */
+  int32_t q_len;      /* rows in the segment (> 0) */
+  int32_t q_pos0;     /* position of row 0 within its request (prefix counted) */
+  int32_t q_pos_step; /* position (and flat index) increment per row */
+  int32_t kv_row0;    /* KV-buffer row of the request's key position 0 */
+  int32_t kv_len;     /* keys visible to the segment's last row = its position + 1 */
+  int32_t tok0;       /* flat index of row 0 */
+  int32_t req;        /* request index */
+} cp_segment_t;
+
+/* Query tiles of the attention kernel are this many rows of one segment. */
+#define CPATTN_TILE_ROWS 128
+
+/* ------------------------------------------------------------------------ */
+/* Plan sizes (host only, no device work).  [SGL-ZZ], [SGL-IL]
+ *   new_lens, prefix_lens: host arrays [num_reqs], entries >= 0.
+ *   num_reqs in [0, CPATTN_MAX_REQS]; cp_size in [1, CPATTN_MAX_CP].
+ * Outputs (host arrays [cp_size], any may be NULL): rows, segments and
+ * CPATTN_TILE_ROWS-row tiles owned by each rank.  The plan buffers of
+ * cp_shard_plan are sized from their sums.  Totals must stay below 2^31. */
+#define CPATTN_MAX_REQS 65536
+#define CPATTN_MAX_CP 1024
+int cp_shard_plan_sizes(const int32_t* new_lens, const int32_t* prefix_lens, int num_reqs,
+                        int cp_size, int strategy, int32_t* rows_per_rank,
+                        int32_t* segs_per_rank, int32_t* tiles_per_rank);
+
+/* Build the shard plan on the device.  [SGL-ZZ], [SGL-IL], [CPB-2.1]
+ *   new_lens_dev, prefix_lens_dev: device int32 [num_reqs].
+ *   total_rows / total_segs / total_tiles: the sums reported by
+ *     cp_shard_plan_sizes for the same lengths (checked on the device;
+ *     a mismatch sets CPATTN_ERR_INVALID_ARG in *status_dev).
+ * Outputs (device, caller-allocated):
+ *   segs_dev        [total_segs]   segments, rank by rank; within a rank in
+ *                                  cat-row order.  Zigzag: request by request,
+ *                                  early block (r) before late block (2C-1-r).
+ *   seg_offsets_dev [cp_size+1]    first segment of each rank
+ *   row_offsets_dev [cp_size+1]    first cat row of each rank
+ *   gather_idx_dev  [total_rows]   cat row -> flat index
+ *   positions_dev   [total_rows]   cat row -> position within its request
+ *   restore_idx_dev [total_rows]   flat index -> cat row (the restore index)
+ *   tiles_dev       [total_tiles]  (nullable) CPATTN_TILE_ROWS-row query tiles
+ *                                  as int32 pairs (segment, tile-in-segment),
+ *                                  heaviest first (descending count of keys
+ *                                  visible to the tile's last row); the order
+ *                                  among equal counts is unspecified.
+ *   status_dev      (nullable)     device error word. */
+int cp_shard_plan(const int32_t* new_lens_dev, const int32_t* prefix_lens_dev, int num_reqs,
+                  int cp_size, int strategy, int total_rows, int total_segs, int total_tiles,
+                  cp_segment_t* segs_dev, int32_t* seg_offsets_dev, int32_t* row_offsets_dev,
+                  int32_t* gather_idx_dev, int32_t* positions_dev, int32_t* restore_idx_dev,
+                  int32_t* tiles_dev, int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Causal attention of shard rows against the gathered KV, giving the partial
+ * output O and its log-sum-exp L.  [SGL-BE], [CPB-3.3]
+ *
+ * For every row of every segment and every query head h, with
+ * P = the row's position and key window [lo, hi) = [max(kv_lo,0), min(kv_hi, P+1))
+ * (kv_hi < 0 means unbounded):
+ *     S_k = scale * q[h] . K[kv_row0 + k, h / (Hq/Hkv)]      for k in [lo, hi)
+ *     L   = ln(sum_k exp(S_k))
+ *     O   = sum_k exp(S_k - L) * V[kv_row0 + k, h / (Hq/Hkv)]
+ * An empty window gives O = 0 and L = -inf (the identity of cp_lse_merge).
+ *
+ *   segs_dev, num_segs: segments (e.g. from cp_shard_plan, or a sub-range).
+ *   tiles_dev, num_tiles: (nullable) tile list from cp_shard_plan restricted to
+ *     these segments, in launch order (heaviest first).  NULL: all tiles of
+ *     all segments in segment order.
+ *   q:  bf16 [num_q_rows, Hq, d] (cat rows), contiguous.
+ *   k:  bf16 key rows; element (row, head, c) at k[row*k_row_stride + head*k_head_stride + c].
+ *   v:  bf16 value rows, same with v_row_stride / v_head_stride (v may alias k:
+ *       absorbed MLA passes v = k with the latent as the first dv columns).
+ *   num_kv_rows: rows addressable through k and v.
+ *   Hq % Hkv == 0.  Supported (d, dv): (64, 64), (128, 128), (576, 512).
+ *   o:  [num_out_rows, Hq, dv], bf16 (o_is_fp32 = 0) or fp32 (o_is_fp32 = 1);
+ *       segment row with cat row R is written at output row R - out_row_base.
+ *   lse: fp32 [num_out_rows, Hq] (natural log), same row mapping.
+ * Every row of every segment (and tile) is written exactly once.  Segments
+ * that point outside q, k, v or o set CPATTN_ERR_RANGE and are skipped. */
+int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                    int num_tiles, const void* q, int num_q_rows, const void* k,
+                    int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                    int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                    int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
+                    int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
+                    int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Merge num_parts partial results with the log-sum-exp rule.  [CPB-3.6]
+ * For each row i < rows and head h < Hq, partial j has
+ *     O_j = o_parts[j*o_part_stride + (i*Hq + h)*dv .. +dv]   (fp32)
+ *     L_j = lse_parts[j*lse_part_stride + i*Hq + h]            (fp32, natural log)
+ * and the result is
+ *     m = max_j L_j,  w_j = exp(L_j - m),  L = m + ln(sum_j w_j),
+ *     O = sum_j w_j O_j / sum_j w_j
+ * (parts with L_j = -inf have weight 0; all empty gives O = 0, L = -inf).
+ * The merged row i is written to output row dst_rows[i] (dst_rows non-NULL:
+ * a fused scatter such as the restore to causal order, each entry in
+ * [0, num_out_rows)) or row i (dst_rows NULL).  o_out: [num_out_rows, Hq, dv]
+ * bf16 or fp32; lse_out: fp32 [num_out_rows, Hq] (nullable).
+ * 1 <= num_parts <= 32; dv % 4 == 0 and dv <= 1024. */
+int cp_lse_merge(const float* o_parts, const float* lse_parts, int num_parts,
+                 int64_t o_part_stride, int64_t lse_part_stride, int rows, int Hq, int dv,
+                 const int32_t* dst_rows, void* o_out, int o_out_is_fp32, float* lse_out,
+                 int num_out_rows, int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Row gather: dst[i] = src[idx[i]] for i < rows, rows of row_bytes bytes
+ * (row_bytes % 16 == 0).  With idx = the plan's restore index and src = the
+ * all-gathered cat rows this restores causal token order [CPB-2.1]; with idx
+ * = the gather index it builds the shard-local (cat) layout from original
+ * order.  An index outside [0, num_src_rows) sets CPATTN_ERR_RANGE and its row
+ * is left unwritten. */
+int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int rows,
+               int64_t row_bytes, void* dst, int32_t* status_dev, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* cp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

@@ -1,0 +1,93 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every entry point
+declared in include/cpattn.h, and its host-side logic (plan sizes, argument
+validation that returns before any device work) matches the oracle."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_causal_attention_cp_gb300 import _lib as L
+from context_causal_attention_cp_gb300 import api, workloads as W
+from oracle import plan as oplan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "cpattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(cp_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = L.load()
+    names = header_functions()
+    assert {"cp_shard_plan_sizes", "cp_shard_plan", "cp_attn_partial", "cp_lse_merge",
+            "cp_restore"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in L.SIGNATURES, f"binding lacks {n}"
+
+
+def _oracle_sizes(new, pre, C, strategy):
+    plan = oplan.make_plan(new, pre, C, strategy)
+    rows = [len(plan.rank_rows[r]) for r in range(C)]
+    segs = [len(plan.segments[r]) for r in range(C)]
+    tiles = [sum((s.q_len + 127) // 128 for s in plan.segments[r]) for r in range(C)]
+    return rows, segs, tiles
+
+
+@pytest.mark.parametrize("seed", range(30))
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_plan_sizes_match_oracle(seed, strategy):
+    new, pre = W.random_batch(seed, max_new=700)
+    C = [1, 2, 3, 4, 8, 5][seed % 6]
+    assert api.cp_shard_plan_sizes(new, pre, C, strategy) == _oracle_sizes(new, pre, C, strategy)
+
+
+@pytest.mark.parametrize("name", sorted(W.WORKLOADS))
+def test_plan_sizes_workloads(name):
+    w = W.WORKLOADS[name]
+    for strategy in w.strategies:
+        got = api.cp_shard_plan_sizes(w.new_lens, w.prefix_lens, w.cp_size, strategy)
+        assert got == _oracle_sizes(w.new_lens, w.prefix_lens, w.cp_size, strategy)
+
+
+def test_invalid_arguments_are_rejected_on_host():
+    lib = L.load()
+    a = (ctypes.c_int32 * 2)(4, 5)
+    out = (ctypes.c_int32 * 4)()
+    assert lib.cp_shard_plan_sizes(a, a, 2, 0, 0, out, out, out) == L.ERR_INVALID_ARG
+    assert lib.cp_shard_plan_sizes(a, a, 2, 4, 7, out, out, out) == L.ERR_INVALID_ARG
+    neg = (ctypes.c_int32 * 2)(4, -1)
+    assert lib.cp_shard_plan_sizes(neg, a, 2, 4, 0, out, out, out) == L.ERR_INVALID_ARG
+    assert lib.cp_shard_plan_sizes(a, a, -1, 4, 0, out, out, out) == L.ERR_INVALID_ARG
+    # attention: Hq not a multiple of Hkv, unsupported head dims, bad scale
+    nul = None
+    args = [nul, 1, nul, 0, nul, 128, nul, 1024, 128, nul, 1024, 128, 256]
+    assert lib.cp_attn_partial(*args, 6, 4, 128, 128, 0.1, 0, -1, nul, 0, nul, 0, 128, nul,
+                               nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial(*args, 8, 4, 96, 96, 0.1, 0, -1, nul, 0, nul, 0, 128, nul,
+                               nul) == L.ERR_UNSUPPORTED
+    assert lib.cp_attn_partial(*args, 8, 4, 128, 128, 0.0, 0, -1, nul, 0, nul, 0, 128, nul,
+                               nul) == L.ERR_INVALID_ARG
+    # merge: part count and dv limits
+    assert lib.cp_lse_merge(nul, nul, 0, 0, 0, 4, 2, 128, nul, nul, 1, nul, 4, nul,
+                            nul) == L.ERR_INVALID_ARG
+    assert lib.cp_lse_merge(nul, nul, 33, 0, 0, 4, 2, 128, nul, nul, 1, nul, 4, nul,
+                            nul) == L.ERR_INVALID_ARG
+    assert lib.cp_lse_merge(nul, nul, 2, 0, 0, 4, 2, 126, nul, nul, 1, nul, 4, nul,
+                            nul) == L.ERR_INVALID_ARG
+    # restore: row bytes must be a multiple of 16
+    assert lib.cp_restore(nul, 4, nul, 4, 24, nul, nul, nul) == L.ERR_INVALID_ARG
+    # misaligned pointers are refused before any launch
+    assert lib.cp_restore(ctypes.c_void_p(0x1008), 4, ctypes.c_void_p(0x2000), 4, 32,
+                          ctypes.c_void_p(0x3000), nul, nul) == L.ERR_ALIGNMENT
+
+
+def test_status_strings():
+    for code in (L.OK, L.ERR_INVALID_ARG, L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_TIMEOUT,
+                 L.ERR_ALIGNMENT, L.ERR_RANGE):
+        assert L.status_string(code) not in ("", "unknown status")

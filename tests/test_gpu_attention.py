@@ -1,0 +1,241 @@
+"""GPU parity of shard attention, merge and restore against the oracle.
+
+Small workloads are compared on every row; the large ones (32K, MLA 16K,
+128K partial-KV) on seeded row samples that always include each segment's
+first and last rows and tile boundaries.  Tolerances: max-abs 2e-2 on O,
+1e-5 relative (floor 1) on the natural-log LSE, exact for permutations.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import context_causal_attention_cp_gb300 as cpa
+from context_causal_attention_cp_gb300 import workloads as W
+from oracle import attention as oatt
+from oracle import merge as omerge
+from oracle import plan as oplan
+
+from gpu_common import assert_attn_close, boundary_rows, np64, oracle_dense_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def run_full_kv(w, strategy, inputs):
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
+    q = inputs["q"].cuda()
+    k = inputs["k"].cuda()
+    v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].cuda()
+    o, lse = cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, w.name)
+    return o, lse
+
+
+def random_case(seed, Hq, Hkv, d, max_reqs=4, max_new=400, max_prefix=200):
+    new, pre = W.random_batch(seed, max_reqs=max_reqs, max_new=max_new, max_prefix=max_prefix)
+    if sum(new) == 0:
+        new[0] = 5
+    w = W.Workload(name=f"rand{seed}", new_lens=new, prefix_lens=pre, Hq=Hq, Hkv=Hkv, d=d,
+                   dv=d, scale=1.0 / math.sqrt(d), std=1.0, cp_size=[1, 2, 3, 4, 8][seed % 5],
+                   strategies=["zigzag", "interleave"], seed=5000 + seed)
+    return w
+
+
+# ------------------------------------------------------------- full rows ----
+
+@pytest.mark.parametrize("strategy", ["zigzag"])
+def test_single1k_d64_all_rows(strategy):
+    w = W.WORKLOADS["single1k_d64"]
+    inputs = W.make_inputs(w)
+    o, lse = run_full_kv(w, strategy, inputs)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    assert_attn_close(o, lse, O_ref, L_ref, w.name)
+
+
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_varlen6_gqa_all_rows(strategy):
+    w = W.WORKLOADS["varlen6_gqa"]
+    inputs = W.make_inputs(w)
+    o, lse = run_full_kv(w, strategy, inputs)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    assert_attn_close(o, lse, O_ref, L_ref, f"{w.name}/{strategy}")
+
+
+@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("heads", [(4, 2, 64), (2, 2, 128), (6, 2, 128), (3, 1, 64)])
+def test_random_batches_all_rows(seed, heads):
+    Hq, Hkv, d = heads
+    w = random_case(seed, Hq, Hkv, d)
+    inputs = W.make_inputs(w)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    for strategy in w.strategies:
+        o, lse = run_full_kv(w, strategy, inputs)
+        assert_attn_close(o, lse, O_ref, L_ref, f"{w.name}/{strategy}/{heads}")
+
+
+# ---------------------------------------------------------- large, sampled ----
+
+def test_llama8b_32k_sampled():
+    w = W.WORKLOADS["llama8b_32k"]
+    inputs = W.make_inputs(w)
+    o, lse = run_full_kv(w, "zigzag", inputs)
+    rows = boundary_rows(w.new_lens, w.prefix_lens, w.cp_size, "zigzag",
+                         W.sample_rows(7, w.total_new, 24))
+    O_ref, L_ref = oracle_dense_rows(inputs, w.new_lens, w.prefix_lens, w.scale, rows)
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    assert_attn_close(o[idx], lse[idx], O_ref, L_ref, w.name)
+
+
+def test_partial_kv_small_all_rows():
+    # ring-style decomposition on a small batch: windows of 192 keys (not a
+    # multiple of the 128-key tile), merged and scattered to original order
+    w = W.Workload(name="pkv_small", new_lens=[700, 300, 5], prefix_lens=[0, 130, 9], Hq=8,
+                   Hkv=2, d=128, dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=3,
+                   strategies=["zigzag", "interleave"], seed=777, kv_block=192)
+    inputs = W.make_inputs(w)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    for strategy in w.strategies:
+        status = cpa.new_status()
+        plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
+        q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+        o, lse = cpa.cp_partial_kv_attention(q_cat, inputs["k"].cuda(), inputs["v"].cuda(), plan,
+                                             w.scale, w.kv_block, status=status)
+        torch.cuda.synchronize()
+        cpa.check_status(status, "partial kv")
+        assert_attn_close(o, lse, O_ref, L_ref, f"pkv/{strategy}")
+
+
+def test_partialkv_128k_sampled():
+    w = W.WORKLOADS["partialkv_128k"]
+    inputs = W.make_inputs(w)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", status=status)
+    k = inputs["k"].cuda()
+    v = inputs["v"].cuda()
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+    o, lse = cpa.cp_partial_kv_attention(q_cat, k, v, plan, w.scale, w.kv_block, status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, w.name)
+    rows = sorted(set(W.sample_rows(11, w.total_new, 16) +
+                      [0, 8191, 8192, 65535, 65536, 131071]))
+    O_ref, L_ref = oracle_dense_rows(inputs, w.new_lens, w.prefix_lens, w.scale, rows)
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    assert_attn_close(o[idx], lse[idx], O_ref, L_ref, w.name)
+
+
+# --------------------------------------------------------------- partials ----
+
+def test_windowed_partials_and_empty_windows():
+    """cp_attn_partial in partial mode: fp32 O, windows, empty rows -> (0, -inf)."""
+    w = random_case(3, 4, 2, 128, max_new=500, max_prefix=50)
+    inputs = W.make_inputs(w)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, 2, "zigzag", status=status)
+    N = w.total_new
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[:N], status=status)
+    k, v = inputs["k"].cuda(), inputs["v"].cuda()
+    op = oplan.make_plan(w.new_lens, w.prefix_lens, 2, "zigzag")
+    pos = np.asarray(op.positions)
+    kv0 = np.asarray([oatt.token_tables(w.new_lens, w.prefix_lens)[1][i] for i in op.gather_idx])
+    q64 = np64(inputs["q"])[np.asarray(op.gather_idx)]
+    k64, v64 = np64(inputs["k"]), np64(inputs["v"])
+    for lo, hi in [(0, 100), (37, 300), (256, 384), (400, 10 ** 6), (10 ** 6, -1)]:
+        o, lse = cpa.cp_attn_partial(plan.segs, q_cat, k, v, w.scale,
+                                     num_segs=plan.total_segs, kv_lo=lo, kv_hi=hi,
+                                     out_fp32=True, status=status)
+        torch.cuda.synchronize()
+        cpa.check_status(status, "window")
+        O_ref, L_ref = oatt.attention_rows(q64, k64, v64, pos, kv0, w.scale, lo,
+                                           None if hi < 0 else hi)
+        assert o.dtype == torch.float32
+        assert_attn_close(o, lse, O_ref, L_ref, f"window {lo}:{hi}")
+
+
+def test_merge_matches_oracle():
+    g = torch.Generator().manual_seed(42)
+    for n, rows, Hq, dv in [(1, 5, 3, 128), (3, 77, 4, 64), (8, 64, 32, 128), (16, 33, 2, 512),
+                            (5, 10, 8, 4)]:
+        o = torch.randn(n, rows, Hq, dv, generator=g)
+        l = torch.randn(n, rows, Hq, generator=g) * 4
+        l[0, 0, 0] = -math.inf
+        if n > 1:
+            l[:, 1, :] = -math.inf                            # all parts empty
+            l[1:, 2, 1] = -math.inf
+        out, lse = cpa.cp_lse_merge(o.cuda(), l.cuda(), lse_out=torch.empty(rows, Hq).cuda())
+        O_ref, L_ref = omerge.lse_merge(o.double().numpy(), l.double().numpy())
+        err = np.abs(np64(out) - O_ref).max()
+        assert err < 1e-5, err
+        assert_attn_close(out, lse, O_ref, L_ref, f"merge n={n}")
+
+
+def test_merge_scatter_and_bf16_output():
+    g = torch.Generator().manual_seed(43)
+    o = torch.randn(4, 50, 8, 128, generator=g)
+    l = torch.randn(4, 50, 8, generator=g)
+    perm = torch.randperm(50, generator=g).to(torch.int32)
+    out = torch.zeros(50, 8, 128, dtype=torch.bfloat16).cuda()
+    lse = torch.zeros(50, 8).cuda()
+    cpa.cp_lse_merge(o.cuda(), l.cuda(), dst_rows=perm.cuda(), out=out, lse_out=lse)
+    O_ref, L_ref = omerge.lse_merge(o.double().numpy(), l.double().numpy())
+    inv = np.empty(50, dtype=np.int64)
+    inv[perm.numpy()] = np.arange(50)
+    assert_attn_close(out, lse, O_ref[inv], L_ref[inv], "merge scatter")
+
+
+def test_gpu_partials_merge_to_dense():
+    """Merging the kernel's per-block partials equals one full-window call."""
+    w = random_case(8, 4, 2, 64, max_new=600, max_prefix=100)
+    inputs = W.make_inputs(w)
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, 1, "zigzag")
+    N = w.total_new
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[:N])
+    k, v = inputs["k"].cuda(), inputs["v"].cuda()
+    full_o, full_l = cpa.cp_attn_partial(plan.segs, q_cat, k, v, w.scale, out_fp32=True,
+                                         num_segs=plan.total_segs)
+    cuts = [0, 128, 200, 512, 700, 10 ** 6]
+    po = torch.empty(len(cuts) - 1, N, w.Hq, w.dv, device="cuda")
+    pl = torch.empty(len(cuts) - 1, N, w.Hq, device="cuda")
+    for j, (a, b) in enumerate(zip(cuts, cuts[1:])):
+        cpa.cp_attn_partial(plan.segs, q_cat, k, v, w.scale, kv_lo=a, kv_hi=b, out=po[j],
+                            lse=pl[j], num_segs=plan.total_segs)
+    mo, ml = cpa.cp_lse_merge(po, pl, lse_out=torch.empty(N, w.Hq, device="cuda"))
+    assert (mo - full_o).abs().max().item() < 1e-4
+    fin = torch.isfinite(full_l)
+    assert ((ml - full_l).abs()[fin] <= 1e-5 * full_l.abs()[fin].clamp(min=1)).all()
+
+
+def test_restore_is_exact():
+    g = torch.Generator().manual_seed(3)
+    src = torch.randn(1000, 8, 64, generator=g).to(torch.bfloat16).cuda()
+    idx = torch.randperm(1000, generator=g).to(torch.int32).cuda()
+    out = cpa.cp_restore(src, idx)
+    assert torch.equal(out, src[idx.long()])
+    lse = torch.randn(1000, 4, generator=g).cuda()
+    assert torch.equal(cpa.cp_restore(lse, idx), lse[idx.long()])
+
+
+def test_bad_segment_sets_range_status():
+    q = torch.zeros(256, 2, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(256, 1, 64, dtype=torch.bfloat16, device="cuda")
+    seg = torch.tensor([[200, 100, 0, 1, 0, 100, 0, 0]], dtype=torch.int32, device="cuda")
+    status = cpa.new_status()
+    cpa.cp_attn_partial(seg, q, k, k, 0.125, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    bad_idx = torch.tensor([0, 5000], dtype=torch.int32, device="cuda")
+    status.zero_()
+    cpa.cp_restore(q, bad_idx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
