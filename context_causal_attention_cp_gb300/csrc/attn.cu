@@ -43,6 +43,7 @@ constexpr int BM = CPATTN_TILE_ROWS;  // query rows per tile (MMA M)
 constexpr int BN = 128;               // keys per KV tile (MMA N of Q K^T)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kMaxSlack = 8.0f;  // lazy-rescale threshold, log2 units
 
 struct AttnParams {
   const cp_segment_t* segs;
@@ -358,9 +359,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mx3 = fmaxf(mx3, x[c + 3]);
       }
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = fmaxf(m_run, mx);
+      // Lazy max: keep the running max unless the tile raises it by more than
+      // kMaxSlack (log2 units).  Exponentials against a stale max are at most
+      // 2^kMaxSlack, and l is accumulated against the same max, so O / l and
+      // L are unchanged; O in TMEM is rescaled only when the max moves.
+      const bool move = mx > m_run + kMaxSlack;
+      const float m_new = move ? mx : m_run;
       const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m_run - m_new_use);  // 0 while m_run = -inf
+      const float alpha = move ? ex2_approx(m_run - m_new_use) : 1.f;  // 0 while m_run = -inf
       float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int q = 0; q < BN / 32; ++q) {
@@ -378,7 +384,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       l_run = l_run * alpha + (sum0 + sum1);
       // rescale the running O (its previous PV has completed: S of this
       // iteration was committed after it)
-      const bool need = (it > 0) && (alpha != 1.f);
+      const bool need = (it > 0) && move;
       if (__any_sync(0xffffffffu, need)) {
         const float a = need ? alpha : 1.f;
         uint32_t r[32];

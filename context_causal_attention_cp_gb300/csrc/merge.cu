@@ -10,6 +10,7 @@
 // Both kernels are HBM-bound streams: one warp per (row, head) merge unit with
 // 16-byte loads of every partial issued before any use, and a flat
 // grid-stride 16-byte copy for the gather.
+#include <algorithm>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -65,12 +66,17 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     const float inv = empty ? 0.f : 1.f / ws;
     const float* base = o_parts + u * dv;
-    for (int c = lane * 4; c < dv; c += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // every lane runs the same number of chunks so that the weight shuffles
+    // below always see the full warp; lanes past dv load and store nothing
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+      const int c = c0 + lane * 4;
+      const bool act = c < dv;
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = zero;
       if (NP > 0) {
         float4 v[NP > 0 ? NP : 1];
 #pragma unroll
-        for (int j = 0; j < NP; ++j) v[j] = ld_stream(base + j * o_stride + c);
+        for (int j = 0; j < NP; ++j) v[j] = act ? ld_stream(base + j * o_stride + c) : zero;
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
           const float w = __shfl_sync(0xffffffffu, wj, j);
@@ -79,10 +85,10 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
       } else {
         int j = 0;
         for (; j + 4 <= num_parts; j += 4) {
-          float4 v0 = ld_stream(base + (j + 0) * o_stride + c);
-          float4 v1 = ld_stream(base + (j + 1) * o_stride + c);
-          float4 v2 = ld_stream(base + (j + 2) * o_stride + c);
-          float4 v3 = ld_stream(base + (j + 3) * o_stride + c);
+          const float4 v0 = act ? ld_stream(base + (j + 0) * o_stride + c) : zero;
+          const float4 v1 = act ? ld_stream(base + (j + 1) * o_stride + c) : zero;
+          const float4 v2 = act ? ld_stream(base + (j + 2) * o_stride + c) : zero;
+          const float4 v3 = act ? ld_stream(base + (j + 3) * o_stride + c) : zero;
           const float w0 = __shfl_sync(0xffffffffu, wj, j + 0);
           const float w1 = __shfl_sync(0xffffffffu, wj, j + 1);
           const float w2 = __shfl_sync(0xffffffffu, wj, j + 2);
@@ -93,11 +99,12 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
           acc.w += w0 * v0.w + w1 * v1.w + w2 * v2.w + w3 * v3.w;
         }
         for (; j < num_parts; ++j) {
-          float4 v0 = ld_stream(base + j * o_stride + c);
+          const float4 v0 = act ? ld_stream(base + j * o_stride + c) : zero;
           const float w0 = __shfl_sync(0xffffffffu, wj, j);
           acc.x += w0 * v0.x; acc.y += w0 * v0.y; acc.z += w0 * v0.z; acc.w += w0 * v0.w;
         }
       }
+      if (!act) continue;
       acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
       const long long oo = ((long long)out_row * Hq + h) * dv + c;
       if (OUT_F32) {
@@ -114,11 +121,12 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
   }
 }
 
-// dst[i] = src[idx[i]]: 16-byte chunks, consecutive threads on consecutive
-// chunks of the same row.
+// dst[i] = src[idx[i]]: vector chunks of type V (16 or 4 bytes), consecutive
+// threads on consecutive chunks of the same row.
+template <typename V>
 __global__ void __launch_bounds__(256)
-row_gather_kernel(const uint4* __restrict__ src, int num_src_rows, const int32_t* __restrict__ idx,
-                  int rows, long long chunks_per_row, uint4* __restrict__ dst, int32_t* status) {
+row_gather_kernel(const V* __restrict__ src, int num_src_rows, const int32_t* __restrict__ idx,
+                  int rows, long long chunks_per_row, V* __restrict__ dst, int32_t* status) {
   const long long total = (long long)rows * chunks_per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += stride) {
@@ -128,7 +136,7 @@ row_gather_kernel(const uint4* __restrict__ src, int num_src_rows, const int32_t
       if (col == 0) set_status(status, CPATTN_ERR_RANGE);
       continue;
     }
-    const uint4 v = __ldcs(src + (long long)s * chunks_per_row + col);
+    const V v = __ldcs(src + (long long)s * chunks_per_row + col);
     __stcs(dst + e, v);
   }
 }
@@ -203,17 +211,25 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
 
 extern "C" int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int rows,
                           int64_t row_bytes, void* dst, int32_t* status_dev, cudaStream_t stream) {
-  if (rows < 0 || num_src_rows < 0 || row_bytes <= 0 || (row_bytes % 16) != 0)
+  if (rows < 0 || num_src_rows < 0 || row_bytes <= 0 || (row_bytes % 4) != 0)
     return CPATTN_ERR_INVALID_ARG;
   if (rows == 0) return CPATTN_OK;
   if (!src || !dst || !idx_dev) return CPATTN_ERR_INVALID_ARG;
-  if (!aligned16(src) || !aligned16(dst) || (reinterpret_cast<uintptr_t>(idx_dev) & 3u))
+  if ((reinterpret_cast<uintptr_t>(src) & 3u) || (reinterpret_cast<uintptr_t>(dst) & 3u) ||
+      (reinterpret_cast<uintptr_t>(idx_dev) & 3u))
     return CPATTN_ERR_ALIGNMENT;
-  const long long cpr = row_bytes / 16;
+  const bool wide = (row_bytes % 16) == 0 && aligned16(src) && aligned16(dst);
+  const long long cpr = wide ? row_bytes / 16 : row_bytes / 4;
   const long long total = (long long)rows * cpr;
   const int grid = (int)std::min<long long>((total + 255) / 256, (long long)sm_count() * 8);
-  row_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), num_src_rows, idx_dev,
-                                              rows, cpr, static_cast<uint4*>(dst), status_dev);
+  if (wide)
+    row_gather_kernel<uint4><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), num_src_rows,
+                                                       idx_dev, rows, cpr,
+                                                       static_cast<uint4*>(dst), status_dev);
+  else
+    row_gather_kernel<uint32_t><<<grid, 256, 0, stream>>>(
+        static_cast<const uint32_t*>(src), num_src_rows, idx_dev, rows, cpr,
+        static_cast<uint32_t*>(dst), status_dev);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

@@ -28,7 +28,8 @@
  *     never traps.
  *   - Ownership: the caller allocates and owns every buffer.  The library
  *     allocates no device or host memory and writes only to output pointers.
- *   - Device pointers must be 16-byte aligned (checked: CPATTN_ERR_ALIGNMENT).
+ *   - Device pointers must be 16-byte aligned unless a call states otherwise
+ *     (checked: CPATTN_ERR_ALIGNMENT).
  *   - Tokens: the batch's new tokens are flattened in request order ("flat
  *     index").  Request b has new_lens[b] new tokens at positions
  *     prefix_lens[b] .. prefix_lens[b]+new_lens[b]-1 (positions count the
@@ -176,7 +177,8 @@ int cp_lse_merge(const float* o_parts, const float* lse_parts, int num_parts,
 
 /* ------------------------------------------------------------------------ */
 /* Row gather: dst[i] = src[idx[i]] for i < rows, rows of row_bytes bytes
- * (row_bytes % 16 == 0).  With idx = the plan's restore index and src = the
+ * (row_bytes % 4 == 0; src and dst 4-byte aligned; 16-byte rows and
+ * pointers take the vectorised path).  With idx = the plan's restore index and src = the
  * all-gathered cat rows this restores causal token order [CPB-2.1]; with idx
  * = the gather index it builds the shard-local (cat) layout from original
  * order.  An index outside [0, num_src_rows) sets CPATTN_ERR_RANGE and its row

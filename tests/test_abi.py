@@ -80,10 +80,10 @@ def test_invalid_arguments_are_rejected_on_host():
                             nul) == L.ERR_INVALID_ARG
     assert lib.cp_lse_merge(nul, nul, 2, 0, 0, 4, 2, 126, nul, nul, 1, nul, 4, nul,
                             nul) == L.ERR_INVALID_ARG
-    # restore: row bytes must be a multiple of 16
-    assert lib.cp_restore(nul, 4, nul, 4, 24, nul, nul, nul) == L.ERR_INVALID_ARG
+    # restore: row bytes must be a multiple of 4
+    assert lib.cp_restore(nul, 4, nul, 4, 22, nul, nul, nul) == L.ERR_INVALID_ARG
     # misaligned pointers are refused before any launch
-    assert lib.cp_restore(ctypes.c_void_p(0x1008), 4, ctypes.c_void_p(0x2000), 4, 32,
+    assert lib.cp_restore(ctypes.c_void_p(0x1002), 4, ctypes.c_void_p(0x2000), 4, 32,
                           ctypes.c_void_p(0x3000), nul, nul) == L.ERR_ALIGNMENT
 
 

@@ -211,7 +211,10 @@ def test_gpu_partials_merge_to_dense():
         cpa.cp_attn_partial(plan.segs, q_cat, k, v, w.scale, kv_lo=a, kv_hi=b, out=po[j],
                             lse=pl[j], num_segs=plan.total_segs)
     mo, ml = cpa.cp_lse_merge(po, pl, lse_out=torch.empty(N, w.Hq, device="cuda"))
-    assert (mo - full_o).abs().max().item() < 1e-4
+    # both sides round P to bf16 (relative 2^-9 per element) against different
+    # row maxima, so O may differ by about 2 * 2^-9 * max|v|
+    vmax = v.float().abs().max().item()
+    assert (mo - full_o).abs().max().item() < 2 * 2 ** -9 * vmax
     fin = torch.isfinite(full_l)
     assert ((ml - full_l).abs()[fin] <= 1e-5 * full_l.abs()[fin].clamp(min=1)).all()
 
