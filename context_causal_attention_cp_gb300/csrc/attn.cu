@@ -62,7 +62,14 @@ struct AttnParams {
 
 template <int D, int DV, int NQ, int KST, int VST>
 struct Cfg {
-  static constexpr int kThreads = NQ * 128 + 64;
+  // NQ = 2: two softmax warpgroups plus one warpgroup holding the producer and
+  // MMA warps, so that setmaxnreg can move registers to the softmax warps
+  // (168 x 384 at launch = 56 x 128 + 224 x 256 after the split).
+  static constexpr int kThreads = NQ == 2 ? 384 : NQ * 128 + 64;
+  static constexpr bool kSplitRegs = NQ == 2;
+  static constexpr int kRegsLaunch = 168, kRegsSoftmax = 208, kRegsOther = 80;
+  static_assert(!kSplitRegs || kRegsOther * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads,
+                "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = NQ * 4;
   static constexpr int kMmaWarp = NQ * 4 + 1;
   static constexpr int kQTileBytes = BM * D * 2;
@@ -105,6 +112,43 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Three-input maximum (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Paired fp32 FMA and add (one instruction for two lanes of work, sm_100+).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 template <int D, int DV, int NQ, int KST, int VST>
@@ -203,6 +247,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t k_base = smem_u32(smem + C::kKOff);
   const uint32_t v_base = smem_u32(smem + C::kVOff);
 
+  if (warp >= 4 * NQ) {
+    if constexpr (C::kSplitRegs)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsOther));
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_kv > 0) {
@@ -314,7 +361,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mma_commit(bar_drain);
       mbar_wait(bar_drain, 0, nullptr, p.timeout_ns);
     }
+  }
   } else {
+    if constexpr (C::kSplitRegs)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
     // ------------------------------------------------------------- softmax --
     const int s = warp >> 2;               // query tile / head of this warpgroup
     const int wq = warp & 3;               // TMEM lane quarter
@@ -333,14 +383,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_after();
       float x[BN];
       {
-        uint32_t r[32];
+        uint32_t r[BN];
 #pragma unroll
-        for (int q = 0; q < BN / 32; ++q) {
-          tmem_ld32(lane_addr + s_col + q * 32, r);
-          tmem_wait_ld();
+        for (int q = 0; q < BN / 32; ++q) tmem_ld32p(lane_addr + s_col + q * 32, r + q * 32);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) x[q * 32 + c] = __uint_as_float(r[c]);
-        }
+        for (int c = 0; c < BN; ++c) x[c] = __uint_as_float(r[c]);
       }
       const int key0 = (j0 + it) * BN;
       if (key0 < win_lo || key0 + BN > row_hi) {
@@ -352,11 +400,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
-      for (int c = 4; c < BN; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
+      for (int c = 4; c < BN; c += 8) {
+        mx0 = fmax3(mx0, x[c], x[c + 1]);
+        mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
+        mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
+        mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
       }
       const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       // Lazy max: keep the running max unless the tile raises it by more than
@@ -373,10 +421,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float a = ex2_approx(fmaf(x[q * 32 + c], sl2, -m_new_use));
-          const float b = ex2_approx(fmaf(x[q * 32 + c + 1], sl2, -m_new_use));
-          sum0 += a;
-          sum1 += b;
+          float a, b;
+          ffma2(a, b, x[q * 32 + c], x[q * 32 + c + 1], sl2, sl2, -m_new_use, -m_new_use);
+          a = ex2_approx(a);
+          b = ex2_approx(b);
+          fadd2(sum0, sum1, sum0, sum1, a, b);
           pk[c >> 1] = pack_bf16x2(a, b);
         }
         tmem_st16(lane_addr + s_col + q * 16, pk);
@@ -495,13 +544,21 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const AttnParams& prm, long long tiles, cudaStream_t stream) {
   using C = Cfg<D, DV, NQ, KST, VST>;
   auto kern = attn_fwd_kernel<D, DV, NQ, KST, VST>;
-  static bool configured = false;
-  if (!configured) {
+  static int configured = 0;  // 1 ok, -1 refused
+  if (configured == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
       return CPATTN_ERR_CUDA;
-    configured = true;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return CPATTN_ERR_CUDA;
+    // setmaxnreg.inc waits until the block's launch allocation can cover the
+    // split; refuse a build whose register count could not.
+    configured = (!C::kSplitRegs || fa.numRegs * C::kThreads >=
+                                        C::kRegsOther * 128 + C::kRegsSoftmax * 256)
+                     ? 1
+                     : -1;
   }
+  if (configured < 0) return CPATTN_ERR_UNSUPPORTED;
   const long long grid = tiles * prm.n_hgroups;
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
