@@ -58,6 +58,13 @@ def attention_flops(w):
     return 2.0 * w.Hq * (w.d + w.dv) * visible_pairs(w.new_lens, w.prefix_lens)
 
 
+def kernel_label(w):
+    if w.d == 576:
+        return "attn_mla_kernel (tcgen05; 128 rows x 1 head x one 256-column output half per CTA)"
+    nq = 2 if (w.Hq // w.Hkv) % 2 == 0 else 1
+    return f"attn_fwd_kernel (tcgen05; {nq} head(s) x 128 rows per CTA)"
+
+
 def config_of(w, extra=None):
     cfg = {"workload": f"{w.name}: {w.description}", "new_lens": w.new_lens,
            "prefix_lens": w.prefix_lens, "heads_q": w.Hq, "heads_kv": w.Hkv, "d": w.d,
@@ -281,7 +288,7 @@ def run_ours(args):
             "breakdown_ms": {"plan_and_q_gather": sum(prep_ms) / len(prep_ms),
                              "attention": attn_avg_ms,
                              "restore_o_lse": sum(rest_ms) / len(rest_ms)},
-            "roofline": {"kernel": "attn_fwd_kernel (tcgen05, 2 heads x 128 rows per CTA)",
+            "roofline": {"kernel": kernel_label(w),
                          "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
                          "traffic": None,

@@ -1,0 +1,182 @@
+// Shared pieces of the shard-attention kernels (sm_103a): launch parameters,
+// bounded warp-uniform waits, TMEM and packed-fp32 helpers, work-item
+// resolution and tensor-map encoding.
+#pragma once
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "../../include/cpattn.h"
+#include "ptx.cuh"
+
+namespace cpattn {
+
+constexpr int BM = CPATTN_TILE_ROWS;  // query rows per tile (MMA M)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kMaxSlack = 8.0f;  // lazy-rescale threshold, log2 units
+
+struct AttnParams {
+  const cp_segment_t* segs;
+  const int32_t* tiles;
+  int num_segs, num_tiles;
+  int Hq, g, n_hgroups;
+  float scale_log2;
+  int kv_lo, kv_hi;
+  void* o;
+  int o_f32;
+  float* lse;
+  int out_row_base, num_out_rows, num_q_rows, num_kv_rows;
+  int32_t* status;
+  unsigned long long timeout_ns;
+};
+
+// Warp-uniform bounded wait: every lane polls, the give-up decision is lane 0's.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort, uint64_t timeout) {
+  const int lane = threadIdx.x & 31;
+  uint64_t t0 = lane == 0 ? global_timer_ns() : 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 63u) == 63u) {
+      int give_up = 0;
+      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > timeout);
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32p(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Three-input maximum (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Paired fp32 FMA and add (one instruction for two lanes of work, sm_100+).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Resolve this CTA's query tile (segment, tile-in-segment) and check the
+// segment against the buffers.  Returns false (the whole CTA returns) when
+// there is no work or the metadata is out of range (then CPATTN_ERR_RANGE).
+__device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, cp_segment_t& sg,
+                                             int& t) {
+  int seg_id = -1;
+  t = 0;
+  if (p.tiles) {
+    if (tile_idx >= p.num_tiles) return false;
+    seg_id = __ldg(p.tiles + 2 * tile_idx);
+    t = __ldg(p.tiles + 2 * tile_idx + 1);
+    if (seg_id < 0 || seg_id >= p.num_segs) {
+      if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+      return false;
+    }
+  } else {
+    int acc = 0;
+    for (int s = 0; s < p.num_segs; ++s) {
+      const int ql = __ldg(&p.segs[s].q_len);
+      const int nt = ql > 0 ? (ql + BM - 1) / BM : 0;
+      if (tile_idx < acc + nt) {
+        seg_id = s;
+        t = tile_idx - acc;
+        break;
+      }
+      acc += nt;
+    }
+    if (seg_id < 0) return false;
+  }
+  sg = p.segs[seg_id];
+  const long long last_pos = (long long)sg.q_pos0 + (long long)(sg.q_len - 1) * sg.q_pos_step;
+  const bool bad = sg.q_len <= 0 || sg.q_row0 < 0 ||
+                   (long long)sg.q_row0 + sg.q_len > p.num_q_rows || sg.q_pos0 < 0 ||
+                   sg.q_pos_step < 0 || sg.kv_row0 < 0 ||
+                   (long long)sg.kv_row0 + sg.kv_len > p.num_kv_rows ||
+                   (long long)sg.q_row0 - p.out_row_base < 0 ||
+                   (long long)sg.q_row0 + sg.q_len - p.out_row_base > p.num_out_rows ||
+                   last_pos + 1 > sg.kv_len || t < 0 || (long long)t * BM >= sg.q_len;
+  if (bad) {
+    if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+    return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------- host --
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 map (cols, heads, rows) with a 64-column x 1-head x 128-row box,
+// 128-byte swizzle; out-of-range rows read as zero.
+inline bool make_map(CUtensorMap* m, const void* base, int cols, int heads, long long rows,
+                     long long head_stride_el, long long row_stride_el, int box_rows = 128) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)(head_stride_el * 2), (cuuint64_t)(row_stride_el * 2)};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+
+// Absorbed-MLA variant (d = 576, dv = 512 with V the first 512 columns of K);
+// defined in attn_mla.cu.
+int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
+                    int64_t k_head_stride, int num_kv_rows, int Hkv, AttnParams prm,
+                    long long tiles, cudaStream_t stream);
+
+}  // namespace cpattn

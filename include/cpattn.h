@@ -72,7 +72,9 @@ typedef struct {
   int32_t q_row0;     /* first cat row of the segment */
   int32_t q_len;      /* rows in the segment (> 0) */
   int32_t q_pos0;     /* position of row 0 within its request (prefix counted) */
-  int32_t q_pos_step; /* position (and flat index) increment per row */
+  int32_t q_pos_step; /* position (and flat index) increment per row; plans
+                         produce >= 1, attention also accepts 0 (all rows at
+                         one position, e.g. decode-style queries) */
   int32_t kv_row0;    /* KV-buffer row of the request's key position 0 */
   int32_t kv_len;     /* keys visible to the segment's last row = its position + 1 */
   int32_t tok0;       /* flat index of row 0 */
@@ -142,7 +144,9 @@ int cp_shard_plan(const int32_t* new_lens_dev, const int32_t* prefix_lens_dev, i
  *   v:  bf16 value rows, same with v_row_stride / v_head_stride (v may alias k:
  *       absorbed MLA passes v = k with the latent as the first dv columns).
  *   num_kv_rows: rows addressable through k and v.
- *   Hq % Hkv == 0.  Supported (d, dv): (64, 64), (128, 128), (576, 512).
+ *   Hq % Hkv == 0.  Supported (d, dv): (64, 64), (128, 128) and the absorbed-MLA
+ *   shape (576, 512), which requires v == k with equal strides (the value is
+ *   the first 512 columns of each key row); other shapes: CPATTN_ERR_UNSUPPORTED.
  *   o:  [num_out_rows, Hq, dv], bf16 (o_is_fp32 = 0) or fp32 (o_is_fp32 = 1);
  *       segment row with cat row R is written at output row R - out_row_base.
  *   lse: fp32 [num_out_rows, Hq] (natural log), same row mapping.

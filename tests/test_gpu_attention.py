@@ -242,3 +242,76 @@ def test_bad_segment_sets_range_status():
     cpa.cp_restore(q, bad_idx, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == -6
+
+
+# --------------------------------------------------------- absorbed MLA ----
+
+def mla_case(new, pre, Hq, C, seed):
+    return W.Workload(name=f"mla{seed}", new_lens=new, prefix_lens=pre, Hq=Hq, Hkv=1, d=576,
+                      dv=512, scale=1 / math.sqrt(192), std=0.1, cp_size=C,
+                      strategies=["interleave", "zigzag"], seed=seed, v_is_k_prefix=True)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_mla_small_all_rows(seed):
+    w = mla_case([300, 77, 5][: 1 + seed], [0, 40, 3][: 1 + seed], 4, [4, 2, 3][seed], 900 + seed)
+    inputs = W.make_inputs(w)
+    k64 = np64(inputs["k"])
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), k64, k64[:, :, :512],
+                                               w.new_lens, w.prefix_lens, w.scale)
+    for strategy in w.strategies:
+        o, lse = run_full_kv(w, strategy, inputs)
+        assert_attn_close(o, lse, O_ref, L_ref, f"mla/{strategy}")
+
+
+def test_mla_16k_sampled():
+    w = W.WORKLOADS["mla_16k"]
+    inputs = W.make_inputs(w)
+    o, lse = run_full_kv(w, "interleave", inputs)
+    rows = boundary_rows(w.new_lens, w.prefix_lens, w.cp_size, "interleave",
+                         W.sample_rows(13, w.total_new, 10) + [0, 1, 2, 3, 16383])
+    k64 = np64(inputs["k"])
+    O_ref, L_ref = oracle_dense_rows(inputs, w.new_lens, w.prefix_lens, w.scale, rows, k64=k64,
+                                     v64=k64[:, :, :512])
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    assert_attn_close(o[idx], lse[idx], O_ref, L_ref, w.name)
+
+
+def test_mla_requires_v_as_latent_view():
+    q = torch.zeros(128, 2, 576, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(128, 1, 576, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(128, 1, 512, dtype=torch.bfloat16, device="cuda")
+    seg = torch.tensor([[0, 128, 0, 1, 0, 128, 0, 0]], dtype=torch.int32, device="cuda")
+    with pytest.raises(cpa.api.L.CpAttnError):
+        cpa.cp_attn_partial(seg, q, k, v, 0.1)
+
+
+# ------------------------------------------------ decode-style merge sweep ----
+
+def test_merge_sweep_interleaved_kv_shards():
+    """64 single-token queries x 32 heads over 65536 keys, key i on shard i mod 8:
+    per-shard partials (no causal mask) merged by the LSE rule equal attention
+    over all keys."""
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q = inputs["q"].cuda()
+    k = inputs["k"].cuda()
+    v = inputs["v"].cuda()
+    S, n_kv = m["shards"], m["kv_tokens"] // m["shards"]
+    seg = torch.tensor([[0, m["queries"], n_kv - 1, 0, 0, n_kv, 0, 0]], dtype=torch.int32,
+                       device="cuda")
+    po = torch.empty(S, m["queries"], m["Hq"], m["dv"], device="cuda")
+    pl = torch.empty(S, m["queries"], m["Hq"], device="cuda")
+    status = cpa.new_status()
+    for j in range(S):
+        idx = torch.arange(j, m["kv_tokens"], S, dtype=torch.int32, device="cuda")
+        kj = cpa.cp_restore(k, idx, status=status)
+        vj = cpa.cp_restore(v, idx, status=status)
+        cpa.cp_attn_partial(seg, q, kj, vj, m["scale"], out=po[j], lse=pl[j], status=status)
+    out, lse = cpa.cp_lse_merge(po, pl, lse_out=torch.empty(m["queries"], m["Hq"], device="cuda"),
+                                status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "merge sweep")
+    O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
+                                         m["scale"], np.arange(m["kv_tokens"]))
+    assert_attn_close(out, lse, O_ref, L_ref, "merge sweep")
