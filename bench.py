@@ -58,6 +58,23 @@ def attention_flops(w):
     return 2.0 * w.Hq * (w.d + w.dv) * visible_pairs(w.new_lens, w.prefix_lens)
 
 
+def reduce_max_over_ranks(value, world, device="cpu"):
+    """Max of a per-rank float over the process group (identity at world 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank, world, steps, max_total_ms):
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return flops_per_rank * world * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def kernel_label(w):
     if w.d == 576:
         return "attn_mla_kernel (tcgen05; 128 rows x 1 head x one 256-column output half per CTA)"
@@ -268,13 +285,9 @@ def run_ours(args):
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
     rest_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
     flops = attention_flops(w)
-    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, args.steps, total_ms)
     pk = peaks()
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = flops / (attn_avg_ms * 1e-3) / 1e12
@@ -418,6 +431,56 @@ def bench_e2e(args, w, inputs, dev, stream):
             "path": "cp_prefill_attention via the C ABI, pinned host q/k/v in, O and LSE out"}
 
 
+def run_profile_case(args):
+    """One kernel, small case, for ncu: 3 warm-up launches then one launch.
+
+    attention: the default workload's attention launch (all 8 shards).
+    merge:     the heaviest query block of the 128K partial-KV workload
+               (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
+    restore:   the O restore of the default workload (268 MB each way)."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    status = cpa.new_status(dev)
+    if args.profile_case == "merge":
+        w = W.WORKLOADS[MERGE_WORKLOAD]
+        rows, Hq, dv, nb = w.total_new // 16, w.Hq, w.dv, 16
+        g = torch.Generator(device=dev).manual_seed(5)
+        po = torch.randn((nb, rows, Hq, dv), device=dev, generator=g)
+        pl = torch.randn((nb, rows, Hq), device=dev, generator=g)
+        dst = torch.randperm(rows, device=dev).to(torch.int32)
+        out = torch.empty((rows, Hq, dv), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((rows, Hq), device=dev)
+        run = lambda: cpa.cp_lse_merge(po, pl, dst_rows=dst, out=out, lse_out=lse,  # noqa: E731
+                                       num_out_rows=rows, status=status)
+    else:
+        w = W.WORKLOADS[args.workload]
+        inputs = W.make_inputs(w)
+        plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], device=dev)
+        q = cpa.cp_restore(inputs["q"].to(dev), plan.gather_idx[: w.total_new])
+        k = inputs["k"].to(dev)
+        v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].to(dev)
+        o, l = cpa.cp_attn_partial(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
+                                   tiles=plan.tiles, num_tiles=plan.total_tiles)
+        if args.profile_case == "attention":
+            run = lambda: cpa.cp_attn_partial(  # noqa: E731
+                plan.segs, q, k, v, w.scale, num_segs=plan.total_segs, tiles=plan.tiles,
+                num_tiles=plan.total_tiles, out=o, lse=l, status=status)
+        else:
+            out = torch.empty_like(o)
+            run = lambda: cpa.cp_restore(o, plan.restore_idx[: w.total_new], out=out,  # noqa: E731
+                                         status=status)
+    for _ in range(4):
+        run()
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, args.profile_case)
+    print(json.dumps({"profile_case": args.profile_case, "launches": 4}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -430,11 +493,15 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-merge", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--profile-case", choices=["attention", "merge", "restore"], default=None,
+                    help="run one kernel on a small case (for ncu) instead of the bench")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_case:
+        return run_profile_case(args)
     return run_ours(args)
 
 

@@ -17,6 +17,9 @@ ERR_TIMEOUT = -4
 ERR_ALIGNMENT = -5
 ERR_RANGE = -6
 
+DEBUG_WAIT_LIMIT_NS = 1
+DEBUG_WITHHOLD_Q = 2
+
 ZIGZAG = 0
 INTERLEAVE = 1
 TILE_ROWS = 128
@@ -36,6 +39,7 @@ SIGNATURES = {
                               vp, vp]),
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
+    "cp_attn_debug": (i32, [i32, ctypes.c_longlong]),
     "cp_status_string": (ctypes.c_char_p, [i32]),
 }
 

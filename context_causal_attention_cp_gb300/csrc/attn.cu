@@ -40,10 +40,10 @@ template <int D, int DV, int NQ, int KST, int VST>
 struct Cfg {
   // NQ = 2: two softmax warpgroups plus one warpgroup holding the producer and
   // MMA warps, so that setmaxnreg can move registers to the softmax warps
-  // (168 x 384 at launch >= 80 x 128 + 208 x 256 after the split).
+  // (168 x 384 at launch >= 64 x 128 + 216 x 256 after the split).
   static constexpr int kThreads = NQ == 2 ? 384 : NQ * 128 + 64;
   static constexpr bool kSplitRegs = NQ == 2;
-  static constexpr int kRegsLaunch = 168, kRegsSoftmax = 208, kRegsOther = 80;
+  static constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 64;
   static_assert(!kSplitRegs || kRegsOther * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads,
                 "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = NQ * 4;
@@ -56,6 +56,7 @@ struct Cfg {
   static constexpr int kVOff = kKOff + KST * kKTileBytes;
   static constexpr int kBarOff = kVOff + VST * kVTileBytes;
   static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 3 * NQ + 1;
+  // barriers, then TMEM slot, abort flag and two issued-load counters
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + align slack
   static constexpr int kTmemNeed = NQ * (BN + DV);
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
@@ -63,6 +64,19 @@ struct Cfg {
   static_assert(kTmemNeed <= 512, "TMEM budget");
   static_assert(D % 64 == 0 && DV % 64 == 0 && DV <= 256, "head dims");
 };
+
+// After an abort, let a CTA's own TMA copies land before its shared memory is
+// released: the query load and the last `stages` loads of each ring (every
+// wait is bounded).  Cold path, kept out of line.
+__device__ __noinline__ void drain_after_abort(uint64_t* bar_q, bool q_issued, uint64_t* k_full,
+                                               int kst, int k_issued, uint64_t* v_full, int vst,
+                                               int v_issued, unsigned long long timeout) {
+  if (q_issued) mbar_wait(bar_q, 0, nullptr, timeout);
+  for (int i = max(0, k_issued - kst); i < k_issued; ++i)
+    mbar_wait(k_full + i % kst, (i / kst) & 1, nullptr, timeout);
+  for (int i = max(0, v_issued - vst); i < v_issued; ++i)
+    mbar_wait(v_full + i % vst, (i / vst) & 1, nullptr, timeout);
+}
 
 template <int D, int DV, int NQ, int KST, int VST>
 __global__ void __launch_bounds__(Cfg<D, DV, NQ, KST, VST>::kThreads, 1)
@@ -115,6 +129,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
+    tmem_slot[2] = 0;
+    tmem_slot[3] = 0;
     fence_barrier_init();
   }
   if (warp == C::kProducerWarp) {
@@ -126,6 +142,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // producer's issued-load counts, kept in shared memory for the abort drain
+  volatile int* issued_kv = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const uint32_t q_base = smem_u32(smem + C::kQOff);
   const uint32_t k_base = smem_u32(smem + C::kKOff);
   const uint32_t v_base = smem_u32(smem + C::kVOff);
@@ -139,12 +157,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(bar_q, NQ * C::kQTileBytes);
-      for (int s = 0; s < NQ; ++s)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kQOff + s * C::kQTileBytes + c * BM * 128, &tm_q, bar_q, c * 64,
-                      head0 + s, sg.q_row0 + r0);
       int k_issued = 0, v_issued = 0;
+      if (!p.withhold_q) {
+        mbar_arrive_expect_tx(bar_q, NQ * C::kQTileBytes);
+        for (int s = 0; s < NQ; ++s)
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::kQOff + s * C::kQTileBytes + c * BM * 128, &tm_q, bar_q,
+                        c * 64, head0 + s, sg.q_row0 + r0);
+      }
       bool ok = true;
       for (int it = 0; it < n_kv && ok; ++it) {
         const int kv_row = sg.kv_row0 + (j0 + it) * BN;
@@ -165,15 +185,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                       c * 64, kv_head, kv_row);
         ++v_issued;
       }
+      issued_kv[0] = k_issued;
+      issued_kv[1] = v_issued;
       if (!ok) {
         set_status(p.status, CPATTN_ERR_TIMEOUT);
         *abort_flag = 1;
-        // let this CTA's own copies land before the shared memory is released
-        mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
-        for (int i = std::max(0, k_issued - KST); i < k_issued; ++i)
-          mbar_wait(k_full + i % KST, (i / KST) & 1, nullptr, p.timeout_ns);
-        for (int i = std::max(0, v_issued - VST); i < v_issued; ++i)
-          mbar_wait(v_full + i % VST, (i / VST) & 1, nullptr, p.timeout_ns);
       }
     }
   } else if (warp == C::kMmaWarp) {
@@ -387,6 +403,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   if (warp == C::kProducerWarp) {
+    if (lane == 0 && *abort_flag && n_kv > 0)
+      drain_after_abort(bar_q, !p.withhold_q, k_full, KST, issued_kv[0], v_full, VST,
+                        issued_kv[1], p.timeout_ns);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
@@ -425,6 +445,25 @@ bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace cpattn
 
 using namespace cpattn;
+
+AttnDebug& cpattn::attn_debug() {
+  static AttnDebug d;
+  return d;
+}
+
+extern "C" int cp_attn_debug(int knob, long long value) {
+  switch (knob) {
+    case CPATTN_DEBUG_WAIT_LIMIT_NS:
+      if (value <= 0) return CPATTN_ERR_INVALID_ARG;
+      attn_debug().timeout_ns = (unsigned long long)value;
+      return CPATTN_OK;
+    case CPATTN_DEBUG_WITHHOLD_Q:
+      attn_debug().withhold_q = value ? 1 : 0;
+      return CPATTN_OK;
+    default:
+      return CPATTN_ERR_INVALID_ARG;
+  }
+}
 
 extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
                                int num_tiles, const void* q, int num_q_rows, const void* k,
@@ -477,7 +516,8 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
   prm.num_q_rows = num_q_rows;
   prm.num_kv_rows = num_kv_rows;
   prm.status = status_dev;
-  prm.timeout_ns = 4000000000ull;
+  prm.timeout_ns = attn_debug().timeout_ns;
+  prm.withhold_q = attn_debug().withhold_q;
   const long long tiles =
       tiles_dev ? num_tiles : ((long long)num_q_rows + BM - 1) / BM + (long long)num_segs;
   if (mla)

@@ -32,7 +32,15 @@ struct AttnParams {
   int out_row_base, num_out_rows, num_q_rows, num_kv_rows;
   int32_t* status;
   unsigned long long timeout_ns;
+  int withhold_q;  // test hook: the producer skips the Q load (see cp_attn_debug)
 };
+
+// Host-side settings of the test hook (cp_attn_debug); defaults: 4 s, off.
+struct AttnDebug {
+  unsigned long long timeout_ns = 4000000000ull;
+  int withhold_q = 0;
+};
+AttnDebug& attn_debug();
 
 // Warp-uniform bounded wait: every lane polls, the give-up decision is lane 0's.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,

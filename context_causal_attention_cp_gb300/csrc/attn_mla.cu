@@ -96,6 +96,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(o_full, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
+    tmem_slot[2] = 0;
     fence_barrier_init();
   }
   if (warp == 4) {
@@ -106,6 +107,8 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // producer's issued chunk-load count, kept in shared memory for the abort drain
+  volatile int* issued_ctr = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const uint32_t q_base = smem_u32(smem);
   const uint32_t k_base = smem_u32(smem + kKOffM);
   constexpr uint32_t kOCol = 256;
@@ -115,11 +118,13 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0 && n_kv > 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      mbar_arrive_expect_tx(bar_q, kQBytes);
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_3d(smem + c * (BM * 128), &tm_q, bar_q, c * 64, h, sg.q_row0 + r0);
+      int issued = 0;
+      if (!p.withhold_q) {
+        mbar_arrive_expect_tx(bar_q, kQBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(smem + c * (BM * 128), &tm_q, bar_q, c * 64, h, sg.q_row0 + r0);
+      }
       bool ok = true;
-      int issued = 0;  // chunk loads issued
       for (int it = 0; it < n_kv && ok; ++it) {
         const int kv_row = sg.kv_row0 + (j0 + it) * kBNm;
         for (int i = 0; i < kChunks; ++i) {
@@ -131,17 +136,10 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++issued;
         }
       }
+      *issued_ctr = issued;
       if (!ok) {
         set_status(p.status, CPATTN_ERR_TIMEOUT);
         *abort_flag = 1;
-        mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
-        // the last load of every chunk may still be in flight
-        const int it_last = (issued - 1) / kChunks;
-        for (int i = 0; i < kChunks; ++i) {
-          const int c = order[i];
-          const int it_c = (i < issued - it_last * kChunks) ? it_last : it_last - 1;
-          if (it_c >= 0) mbar_wait(k_full + c, it_c & 1, nullptr, p.timeout_ns);
-        }
       }
     }
   } else if (warp == 5) {
@@ -339,6 +337,19 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
+    if (lane == 0 && *abort_flag && n_kv > 0) {
+      // after an abort, let this CTA's own copies land before its shared
+      // memory is released: Q, and the last load of every chunk
+      const int issued = *issued_ctr;
+      if (!p.withhold_q) mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
+      const int it_last = (issued - 1) / kChunks;
+      for (int i = 0; i < kChunks && issued > 0; ++i) {
+        const int c = order[i];
+        const int it_c = (i < issued - it_last * kChunks) ? it_last : it_last - 1;
+        if (it_c >= 0) mbar_wait(k_full + c, it_c & 1, nullptr, p.timeout_ns);
+      }
+    }
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }

@@ -190,6 +190,21 @@ int cp_lse_merge(const float* o_parts, const float* lse_parts, int num_parts,
 int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int rows,
                int64_t row_bytes, void* dst, int32_t* status_dev, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Test hook for the failure path of the attention pipeline (no counterpart on
+ * the source pages).  Process-wide; affects launches made after the call.
+ *   CPATTN_DEBUG_WAIT_LIMIT_NS: time limit of every mbarrier wait inside the
+ *     attention kernels, in ns (default 4e9).  value > 0.
+ *   CPATTN_DEBUG_WITHHOLD_Q: value != 0 makes the TMA producer skip the query
+ *     load, so the MMA thread's wait on it runs out: the kernel then writes
+ *     CPATTN_ERR_TIMEOUT to the status word, drains its own copies, frees its
+ *     tensor memory and returns (outputs of the affected tiles are not
+ *     written).  Nothing traps and no wait is unbounded.  Reset to 0 after use.
+ * Returns CPATTN_OK or CPATTN_ERR_INVALID_ARG. */
+#define CPATTN_DEBUG_WAIT_LIMIT_NS 1
+#define CPATTN_DEBUG_WITHHOLD_Q 2
+int cp_attn_debug(int knob, long long value);
+
 /* Human-readable name of a status code (static string). */
 const char* cp_status_string(int status);
 

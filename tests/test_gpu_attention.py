@@ -315,3 +315,38 @@ def test_merge_sweep_interleaved_kv_shards():
     O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
                                          m["scale"], np.arange(m["kv_tokens"]))
     assert_attn_close(out, lse, O_ref, L_ref, "merge sweep")
+
+
+# ------------------------------------------------- bounded pipeline waits ----
+
+@pytest.mark.parametrize("shape", [(2, 1, 128, 128), (1, 1, 64, 64), (1, 1, 576, 512)])
+def test_wait_limit_reports_timeout_and_context_survives(shape):
+    """With the query load withheld, the MMA thread's wait runs out: the kernel
+    reports CPATTN_ERR_TIMEOUT, drains its own copies, frees TMEM and returns.
+    The CUDA context stays usable: the same call without the hook is correct."""
+    Hq, Hkv, d, dv = shape
+    lib = cpa.api.L.load()
+    g = torch.Generator().manual_seed(17)
+    n = 300
+    q = (torch.randn(n, Hq, d, generator=g) * 0.3).to(torch.bfloat16).cuda()
+    k = (torch.randn(n, Hkv, d, generator=g) * 0.3).to(torch.bfloat16).cuda()
+    v = k[:, :, :dv] if d == 576 else (torch.randn(n, Hkv, dv, generator=g)).to(torch.bfloat16).cuda()
+    seg = torch.tensor([[0, n, 0, 1, 0, n, 0, 0]], dtype=torch.int32, device="cuda")
+    status = cpa.new_status()
+    assert lib.cp_attn_debug(cpa.api.L.DEBUG_WAIT_LIMIT_NS, 20_000_000) == 0
+    assert lib.cp_attn_debug(cpa.api.L.DEBUG_WITHHOLD_Q, 1) == 0
+    try:
+        cpa.cp_attn_partial(seg, q, k, v, 0.1, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == cpa.api.L.ERR_TIMEOUT
+    finally:
+        lib.cp_attn_debug(cpa.api.L.DEBUG_WITHHOLD_Q, 0)
+        lib.cp_attn_debug(cpa.api.L.DEBUG_WAIT_LIMIT_NS, 4_000_000_000)
+    status.zero_()
+    o, lse = cpa.cp_attn_partial(seg, q, k, v, 0.1, status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "after timeout")
+    pos = np.arange(n)
+    O_ref, L_ref = oatt.attention_rows(np64(q), np64(k), np64(v), pos, np.zeros(n, np.int64), 0.1)
+    assert_attn_close(o, lse, O_ref, L_ref, "after timeout")
+    assert lib.cp_attn_debug(99, 1) == cpa.api.L.ERR_INVALID_ARG
