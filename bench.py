@@ -315,6 +315,9 @@ def run_ours(args):
     if not args.skip_merge:
         line["merge"] = bench_merge(args, dev, stream, pk)
         line["gpu_launches"] += line["merge"].pop("launches")
+    if not args.skip_merge:
+        line["partial_kv"] = bench_partial_kv(args, dev, stream, pk)
+        line["gpu_launches"] += line["partial_kv"].pop("launches")
     if not args.skip_e2e:
         line["e2e"] = bench_e2e(args, w, inputs, dev, stream)
     del q, k, v, ws, flush
@@ -383,6 +386,66 @@ def bench_merge(args, dev, stream, pk):
             "bytes_read": read, "bytes_written": written, "parts": slot_rows // (N // 16),
             "launches": len(segs) * (reps + 3),
             "note": "partials exceed L2 (18 GB), so every read comes from HBM"}
+
+
+def bench_partial_kv(args, dev, stream, pk):
+    """The 128K partial-KV decomposition as one library call per step.
+
+    Step = plan + query gather + cp_attn_partial_kv (layout, split-KV
+    attention over the 136 visible (query block, KV block) pairs, fp32
+    partials in an 18.4 GB workspace, LSE merge scattered to causal order)."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    torch.cuda.empty_cache()
+    w = W.WORKLOADS[MERGE_WORKLOAD]
+    inputs = W.make_inputs(w)
+    q = inputs["q"].to(dev)
+    k = inputs["k"].to(dev)
+    v = inputs["v"].to(dev)
+    del inputs
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    status = cpa.new_status(dev)
+    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev)
+    nbytes, _ = cpa.cp_partial_kv_workspace_size(w.new_lens, w.prefix_lens, w.cp_size, "zigzag",
+                                                 w.kv_block, Hq, dv)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    q_cat = torch.empty_like(q)
+    out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+
+    def step():
+        cpa.cp_shard_plan(plan, status=status, stream=stream)
+        cpa.cp_restore(q, plan.gather_idx[:N], out=q_cat, status=status, stream=stream)
+        cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
+                               prefix_lens=w.prefix_lens, workspace=ws, out=out, lse_out=lse,
+                               status=status, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    reps = 3
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    cpa.check_status(status, "partial kv")
+    ms = sorted(times)[len(times) // 2]
+    flops = attention_flops(w)
+    tf = flops / (ms * 1e-3) / 1e12
+    del ws, q, k, v, q_cat, out, lse
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: {w.description}", "ms_per_step": ms,
+            "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+            "workspace_bytes": nbytes, "launches": (3 + 1 + 3) * (reps + 3),
+            "path": "cp_shard_plan + cp_restore + cp_attn_partial_kv (one call: layout, "
+                    "split-KV attention, merge + restore)"}
 
 
 def bench_e2e(args, w, inputs, dev, stream):

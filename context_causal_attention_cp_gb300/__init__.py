@@ -11,7 +11,9 @@ from .api import (  # noqa: F401
     alloc_plan,
     check_status,
     cp_attn_partial,
+    cp_attn_partial_kv,
     cp_lse_merge,
+    cp_partial_kv_workspace_size,
     cp_partial_kv_attention,
     cp_prefill_attention,
     cp_restore,

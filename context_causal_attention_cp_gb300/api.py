@@ -239,14 +239,59 @@ def partial_kv_layout(segs_host, kv_block):
     return out, slot
 
 
+def cp_partial_kv_workspace_size(new_lens, prefix_lens, cp_size, strategy, kv_block, Hq, dv):
+    """(workspace bytes, max blocks per segment) for cp_attn_partial_kv."""
+    lib = L.load()
+    nl, n = _i32_array(new_lens)
+    pl, _ = _i32_array(prefix_lens)
+    nbytes = ctypes.c_int64()
+    mb = ctypes.c_int32()
+    L.check(lib.cp_partial_kv_workspace_size(nl, pl, n, cp_size, _strategy(strategy), kv_block,
+                                             Hq, dv, ctypes.byref(nbytes), ctypes.byref(mb)),
+            "cp_partial_kv_workspace_size")
+    return nbytes.value, mb.value
+
+
+def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_lens, prefix_lens,
+                       workspace=None, dst_rows="restore", out=None, lse_out=None,
+                       out_fp32=False, status=None, stream=None):
+    """Partial-KV decomposition in one library call (layout, split attention, merge).
+
+    ``dst_rows="restore"`` scatters the merged rows to original token order
+    (the plan's gather index); ``None`` keeps cat order.  Returns (O, LSE, workspace).
+    """
+    lib = L.load()
+    N, Hq, d = q_cat.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    nbytes, max_blocks = cp_partial_kv_workspace_size(new_lens, prefix_lens, plan.cp_size,
+                                                      plan.strategy, kv_block, Hq, dv)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_cat.device)
+    idx = plan.gather_idx[:N] if isinstance(dst_rows, str) else dst_rows
+    if out is None:
+        out = torch.empty((N, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q_cat.device)
+    if lse_out is None:
+        lse_out = torch.empty((N, Hq), dtype=torch.float32, device=q_cat.device)
+    L.check(lib.cp_attn_partial_kv(
+        _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
+        k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
+        float(scale), int(kv_block), int(max_blocks), _p(idx), _p(out),
+        1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
+        workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
+    return out, lse_out, workspace
+
+
 def cp_partial_kv_attention(q_cat, k, v, plan: ShardPlan, scale, kv_block, *, segs_host=None,
                             parts_o=None, parts_lse=None, out=None, lse_out=None, status=None,
                             stream=None):
-    """Partial-KV (ring-style) CP on one GPU.
+    """Partial-KV (ring-style) CP on one GPU, one KV block at a time.
 
-    Every segment's rows meet the KV one block of ``kv_block`` keys at a time
-    (fp32 partial O_j and L_j per visible block), then the partials are
-    LSE-merged and scattered straight to original token order.
+    Emulates the ring schedule step by step: for every segment and every
+    visible block of ``kv_block`` keys, one cp_attn_partial call gives the fp32
+    partial (O_j, L_j); then one cp_lse_merge per segment merges them and
+    scatters straight to original token order.  cp_attn_partial_kv computes
+    the same in three launches.
     Returns (O [N, Hq, dv] bf16, LSE [N, Hq]).
     """
     N, Hq, _ = q_cat.shape

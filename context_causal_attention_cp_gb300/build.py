@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcpattn.so")
-SOURCES = ["plan.cu", "merge.cu", "attn.cu", "attn_mla.cu"]
+SOURCES = ["plan.cu", "merge.cu", "attn.cu", "attn_mla.cu", "partial_kv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

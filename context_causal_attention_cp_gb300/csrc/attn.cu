@@ -103,15 +103,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   // ---- work item: (tile of 128 rows of one segment, group of NQ heads) ----
   const int hg = blockIdx.x % p.n_hgroups;
-  const int tile_idx = blockIdx.x / p.n_hgroups;
+  const int rest = blockIdx.x / p.n_hgroups;
+  const int jblk = p.split_block > 0 ? rest % p.max_blocks : 0;
+  const int tile_idx = p.split_block > 0 ? rest / p.max_blocks : rest;
   cp_segment_t sg;
-  int t;
-  if (!resolve_tile(p, tile_idx, sg, t)) return;
+  int t, seg_id, kv_lo, kv_hi;
+  long long out_row0;
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
+  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
   const int r0 = t * BM;
   const int rows_valid = min(BM, sg.q_len - r0);
   const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
-  const int win_lo = max(p.kv_lo, 0);
-  const int win_hi_tile = p.kv_hi < 0 ? pos_max + 1 : min(p.kv_hi, pos_max + 1);
+  const int win_lo = max(kv_lo, 0);
+  const int win_hi_tile = kv_hi < 0 ? pos_max + 1 : min(kv_hi, pos_max + 1);
   const int j0 = win_lo / BN;
   const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + BN - 1) / BN - j0 : 0;
   const int head0 = hg * NQ;            // query heads head0 .. head0+NQ-1
@@ -270,7 +274,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int row = wq * 32 + lane;        // row within the tile
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
-    const int row_hi = valid ? (p.kv_hi < 0 ? pos + 1 : min(p.kv_hi, pos + 1)) : 0;
+    const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_col = s * BN, o_col = NQ * BN + s * DV;
     const float sl2 = p.scale_log2;
@@ -360,7 +364,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else {
       tc_fence_after();
       const int h = head0 + s;
-      const long long out_row = (long long)sg.q_row0 + r0 + row - p.out_row_base;
+      const long long out_row = out_row0 + r0 + row;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
 #pragma unroll
@@ -432,14 +436,12 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                      : -1;
   }
   if (configured < 0) return CPATTN_ERR_UNSUPPORTED;
-  const long long grid = tiles * prm.n_hgroups;
+  const long long grid = tiles * prm.n_hgroups;  // tiles x KV blocks (split mode) x head groups
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
   kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
-
-bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 }  // namespace cpattn
@@ -465,15 +467,13 @@ extern "C" int cp_attn_debug(int knob, long long value) {
   }
 }
 
-extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
-                               int num_tiles, const void* q, int num_q_rows, const void* k,
-                               int64_t k_row_stride, int64_t k_head_stride, const void* v,
-                               int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
-                               int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
-                               int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
-                               int32_t* status_dev, cudaStream_t stream) {
-  if (num_segs < 0 || num_q_rows < 0 || num_kv_rows < 0 || num_out_rows < 0)
-    return CPATTN_ERR_INVALID_ARG;
+int cpattn::attn_launch(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                        int num_tiles, const void* q, int num_q_rows, const void* k,
+                        int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                        int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                        int Hkv, int d, int dv, float scale, AttnParams& prm,
+                        cudaStream_t stream) {
+  if (num_segs < 0 || num_q_rows < 0 || num_kv_rows < 0) return CPATTN_ERR_INVALID_ARG;
   if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || !(scale > 0.f)) return CPATTN_ERR_INVALID_ARG;
   const bool mla = (d == 576 && dv == 512);
   const bool shape_ok = (d == 64 && dv == 64) || (d == 128 && dv == 128) || mla;
@@ -483,21 +483,21 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
     return CPATTN_ERR_UNSUPPORTED;
   if (tiles_dev && num_tiles < 0) return CPATTN_ERR_INVALID_ARG;
   if (num_segs == 0 || (tiles_dev && num_tiles == 0)) return CPATTN_OK;
-  if (!segs_dev || !q || !k || !v || !o || !lse) return CPATTN_ERR_INVALID_ARG;
-  if (num_q_rows == 0 || num_kv_rows == 0 || num_out_rows == 0) return CPATTN_ERR_INVALID_ARG;
-  if (!a16(segs_dev) || !a16(q) || !a16(k) || !a16(v) || !a16(o) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(tiles_dev) & 7u))
+  if (!segs_dev || !q || !k || !v) return CPATTN_ERR_INVALID_ARG;
+  if (num_q_rows == 0 || num_kv_rows == 0) return CPATTN_ERR_INVALID_ARG;
+  if (!a16(segs_dev) || !a16(q) || !a16(k) || !a16(v) ||
+      (reinterpret_cast<uintptr_t>(tiles_dev) & 7u))
     return CPATTN_ERR_ALIGNMENT;
   if ((k_row_stride * 2) % 16 || (k_head_stride * 2) % 16 || (v_row_stride * 2) % 16 ||
       (v_head_stride * 2) % 16)
     return CPATTN_ERR_ALIGNMENT;
-  if (k_head_stride < d || v_head_stride < dv || k_row_stride < (int64_t)(Hkv - 1) * k_head_stride + d ||
+  if (k_head_stride < d || v_head_stride < dv ||
+      k_row_stride < (int64_t)(Hkv - 1) * k_head_stride + d ||
       v_row_stride < (int64_t)(Hkv - 1) * v_head_stride + dv)
     return CPATTN_ERR_INVALID_ARG;
 
   const int g = Hq / Hkv;
   const int nq = (g % 2 == 0) ? 2 : 1;
-  AttnParams prm;
   prm.segs = segs_dev;
   prm.tiles = tiles_dev;
   prm.num_segs = num_segs;
@@ -506,6 +506,40 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
   prm.g = g;
   prm.n_hgroups = Hq / nq;
   prm.scale_log2 = scale * kLog2e;
+  prm.num_q_rows = num_q_rows;
+  prm.num_kv_rows = num_kv_rows;
+  prm.timeout_ns = attn_debug().timeout_ns;
+  prm.withhold_q = attn_debug().withhold_q;
+  long long units =
+      tiles_dev ? num_tiles : ((long long)num_q_rows + BM - 1) / BM + (long long)num_segs;
+  if (prm.split_block > 0) units *= prm.max_blocks;
+  if (mla)
+    return launch_attn_mla(q, num_q_rows, k, k_row_stride, k_head_stride, num_kv_rows, Hkv, prm,
+                           units, stream);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, d, Hq, num_q_rows, d, (long long)Hq * d) ||
+      !make_map(&mk, k, d, Hkv, num_kv_rows, k_head_stride, k_row_stride) ||
+      !make_map(&mv, v, dv, Hkv, num_kv_rows, v_head_stride, v_row_stride))
+    return CPATTN_ERR_CUDA;
+  if (d == 128) {
+    if (nq == 2) return launch_attn<128, 128, 2, 2, 2>(mq, mk, mv, prm, units, stream);
+    return launch_attn<128, 128, 1, 2, 2>(mq, mk, mv, prm, units, stream);
+  }
+  if (nq == 2) return launch_attn<64, 64, 2, 3, 3>(mq, mk, mv, prm, units, stream);
+  return launch_attn<64, 64, 1, 3, 3>(mq, mk, mv, prm, units, stream);
+}
+
+extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                               int num_tiles, const void* q, int num_q_rows, const void* k,
+                               int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                               int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                               int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
+                               int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
+                               int32_t* status_dev, cudaStream_t stream) {
+  if (num_out_rows < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_segs > 0 && (!o || !lse || num_out_rows == 0)) return CPATTN_ERR_INVALID_ARG;
+  if (o && (!a16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))) return CPATTN_ERR_ALIGNMENT;
+  AttnParams prm{};
   prm.kv_lo = kv_lo;
   prm.kv_hi = kv_hi;
   prm.o = o;
@@ -513,26 +547,9 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
   prm.lse = lse;
   prm.out_row_base = out_row_base;
   prm.num_out_rows = num_out_rows;
-  prm.num_q_rows = num_q_rows;
-  prm.num_kv_rows = num_kv_rows;
   prm.status = status_dev;
-  prm.timeout_ns = attn_debug().timeout_ns;
-  prm.withhold_q = attn_debug().withhold_q;
-  const long long tiles =
-      tiles_dev ? num_tiles : ((long long)num_q_rows + BM - 1) / BM + (long long)num_segs;
-  if (mla)
-    return launch_attn_mla(q, num_q_rows, k, k_row_stride, k_head_stride, num_kv_rows, Hkv, prm,
-                           tiles, stream);
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, d, Hq, num_q_rows, d, (long long)Hq * d) ||
-      !make_map(&mk, k, d, Hkv, num_kv_rows, k_head_stride, k_row_stride) ||
-      !make_map(&mv, v, dv, Hkv, num_kv_rows, v_head_stride, v_row_stride))
-    return CPATTN_ERR_CUDA;
-
-  if (d == 128) {
-    if (nq == 2) return launch_attn<128, 128, 2, 2, 2>(mq, mk, mv, prm, tiles, stream);
-    return launch_attn<128, 128, 1, 2, 2>(mq, mk, mv, prm, tiles, stream);
-  }
-  if (nq == 2) return launch_attn<64, 64, 2, 3, 3>(mq, mk, mv, prm, tiles, stream);
-  return launch_attn<64, 64, 1, 3, 3>(mq, mk, mv, prm, tiles, stream);
+  prm.split_block = 0;
+  return attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
+                     k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
+                     scale, prm, stream);
 }

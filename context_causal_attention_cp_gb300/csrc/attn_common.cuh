@@ -33,7 +33,19 @@ struct AttnParams {
   int32_t* status;
   unsigned long long timeout_ns;
   int withhold_q;  // test hook: the producer skips the Q load (see cp_attn_debug)
+  // split-KV mode (cp_attn_partial_kv): split_block > 0 splits every segment's
+  // keys into blocks [j*split_block, (j+1)*split_block); the CTA for block j
+  // writes its fp32 partial at workspace row ws_slot[seg] + j*q_len + row.
+  int split_block, max_blocks;
+  const long long* ws_slot;
+  long long ws_rows;  // capacity of the partial buffers, rows
 };
+
+// Number of split_block-key blocks a segment sees (key 0 is always visible).
+__host__ __device__ __forceinline__ int segment_blocks(const cp_segment_t& s, int split_block) {
+  const long long last = (long long)s.q_pos0 + (long long)(s.q_len - 1) * s.q_pos_step;
+  return (int)(last / split_block) + 1;
+}
 
 // Host-side settings of the test hook (cp_attn_debug); defaults: 4 s, off.
 struct AttnDebug {
@@ -109,8 +121,8 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
 // segment against the buffers.  Returns false (the whole CTA returns) when
 // there is no work or the metadata is out of range (then CPATTN_ERR_RANGE).
 __device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, cp_segment_t& sg,
-                                             int& t) {
-  int seg_id = -1;
+                                             int& t, int& seg_id) {
+  seg_id = -1;
   t = 0;
   if (p.tiles) {
     if (tile_idx >= p.num_tiles) return false;
@@ -150,6 +162,34 @@ __device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, 
   return true;
 }
 
+// The key window and output placement of this CTA.  Normal mode: the call's
+// window, output row = cat row - out_row_base.  Split-KV mode: block j of the
+// segment's keys, output row = ws_slot[seg] + j * q_len + row-in-segment.
+// Returns false when the CTA has no block to do (or its slot is out of range).
+__device__ __forceinline__ bool split_window(const AttnParams& p, const cp_segment_t& sg, int seg_id,
+                                             int j, int& kv_lo, int& kv_hi, long long& out_row0) {
+  if (p.split_block <= 0) {
+    kv_lo = p.kv_lo;
+    kv_hi = p.kv_hi;
+    out_row0 = (long long)sg.q_row0 - p.out_row_base;  // output row of segment row 0
+    return true;
+  }
+  const int nb = segment_blocks(sg, p.split_block);
+  if (j >= nb) return false;
+  if (nb > p.max_blocks) {
+    if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_INVALID_ARG);
+    return false;
+  }
+  kv_lo = j * p.split_block;
+  kv_hi = kv_lo + p.split_block;
+  out_row0 = p.ws_slot[seg_id] + (long long)j * sg.q_len;
+  if (out_row0 < 0 || out_row0 + sg.q_len > p.ws_rows) {
+    if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+    return false;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------- host --
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -181,10 +221,21 @@ inline bool make_map(CUtensorMap* m, const void* base, int cols, int heads, long
 }
 
 
+inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 // Absorbed-MLA variant (d = 576, dv = 512 with V the first 512 columns of K);
 // defined in attn_mla.cu.
 int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
                     int64_t k_head_stride, int num_kv_rows, int Hkv, AttnParams prm,
                     long long tiles, cudaStream_t stream);
+
+// Shared host front end of cp_attn_partial and cp_attn_partial_kv: validates
+// the shape arguments, fills prm (everything but the split fields and the
+// output pointers) and launches the kernel for the shape.
+int attn_launch(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
+                const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
+                int64_t k_head_stride, const void* v, int64_t v_row_stride, int64_t v_head_stride,
+                int num_kv_rows, int Hq, int Hkv, int d, int dv, float scale, AttnParams& prm,
+                cudaStream_t stream);
 
 }  // namespace cpattn

@@ -61,15 +61,19 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // ---- work item: (128-row tile, query head, output half) ----
   const int half = blockIdx.x & 1;
   const int h = (blockIdx.x >> 1) % p.Hq;
-  const int tile_idx = (blockIdx.x >> 1) / p.Hq;
+  const int rest = (blockIdx.x >> 1) / p.Hq;
+  const int jblk = p.split_block > 0 ? rest % p.max_blocks : 0;
+  const int tile_idx = p.split_block > 0 ? rest / p.max_blocks : rest;
   cp_segment_t sg;
-  int t;
-  if (!resolve_tile(p, tile_idx, sg, t)) return;
+  int t, seg_id, kv_lo, kv_hi;
+  long long out_row0;
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
+  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
   const int r0 = t * BM;
   const int rows_valid = min(BM, sg.q_len - r0);
   const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
-  const int win_lo = max(p.kv_lo, 0);
-  const int win_hi_tile = p.kv_hi < 0 ? pos_max + 1 : min(p.kv_hi, pos_max + 1);
+  const int win_lo = max(kv_lo, 0);
+  const int win_hi_tile = kv_hi < 0 ? pos_max + 1 : min(kv_hi, pos_max + 1);
   const int j0 = win_lo / kBNm;
   const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + kBNm - 1) / kBNm - j0 : 0;
   const int kv_head = h / p.g;
@@ -213,7 +217,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int row = warp * 32 + lane;
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
-    const int row_hi = valid ? (p.kv_hi < 0 ? pos + 1 : min(p.kv_hi, pos + 1)) : 0;
+    const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
@@ -295,7 +299,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else {
       tc_fence_after();
-      const long long out_row = (long long)sg.q_row0 + r0 + row - p.out_row_base;
+      const long long out_row = out_row0 + r0 + row;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
 #pragma unroll 1
@@ -371,7 +375,7 @@ int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_
       return CPATTN_ERR_CUDA;
     configured = true;
   }
-  const long long grid = tiles * prm.Hq * 2;
+  const long long grid = tiles * prm.Hq * 2;  // tiles x KV blocks (split mode) x heads x halves
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
   attn_mla_kernel<<<(unsigned)grid, kThreadsM, kSmemM, stream>>>(mq, mk, prm);

@@ -8,7 +8,7 @@
 // back into causal token order.
 //
 // Both kernels are HBM-bound streams: one warp per (row, head) merge unit with
-// 16-byte loads of every partial issued before any use, and a flat
+// groups of 16-byte partial loads issued before any use, and a flat
 // grid-stride 16-byte copy for the gather.
 #include <algorithm>
 #include <cstdint>
@@ -33,9 +33,14 @@ __device__ __forceinline__ float4 ld_stream(const float* p) {
 }
 
 // Each warp merges one (row, head) unit per iteration; lane j < num_parts
-// holds L_j.  dv is split in 128-float chunks, one float4 per lane.
-template <bool OUT_F32, int NP>
-__global__ void __launch_bounds__(kMergeThreads)
+// holds L_j.  dv is split in 128-float chunks, one float4 per lane, and the
+// partials are streamed in groups of kGroup 16-byte loads that are all issued
+// before any is used.  Registers stay under 85 so that three 256-thread blocks
+// share an SM (24 warps, about 96 KB of loads in flight per SM).
+constexpr int kGroup = 8;
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kMergeThreads, 3)
 lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
                  int num_parts, int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
                  const int32_t* __restrict__ dst_rows, void* __restrict__ o_out,
@@ -66,42 +71,25 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     const float inv = empty ? 0.f : 1.f / ws;
     const float* base = o_parts + u * dv;
-    // every lane runs the same number of chunks so that the weight shuffles
-    // below always see the full warp; lanes past dv load and store nothing
+    // every lane runs the same number of chunks and groups so that the weight
+    // shuffles always see the full warp; lanes past dv load and store nothing
     for (int c0 = 0; c0 < dv; c0 += 128) {
       const int c = c0 + lane * 4;
       const bool act = c < dv;
       const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc = zero;
-      if (NP > 0) {
-        float4 v[NP > 0 ? NP : 1];
+      for (int j0 = 0; j0 < num_parts; j0 += kGroup) {
+        float4 v[kGroup];
 #pragma unroll
-        for (int j = 0; j < NP; ++j) v[j] = act ? ld_stream(base + j * o_stride + c) : zero;
+        for (int jj = 0; jj < kGroup; ++jj)
+          v[jj] = (act && j0 + jj < num_parts) ? ld_stream(base + (j0 + jj) * o_stride + c) : zero;
 #pragma unroll
-        for (int j = 0; j < NP; ++j) {
-          const float w = __shfl_sync(0xffffffffu, wj, j);
-          acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
-        }
-      } else {
-        int j = 0;
-        for (; j + 4 <= num_parts; j += 4) {
-          const float4 v0 = act ? ld_stream(base + (j + 0) * o_stride + c) : zero;
-          const float4 v1 = act ? ld_stream(base + (j + 1) * o_stride + c) : zero;
-          const float4 v2 = act ? ld_stream(base + (j + 2) * o_stride + c) : zero;
-          const float4 v3 = act ? ld_stream(base + (j + 3) * o_stride + c) : zero;
-          const float w0 = __shfl_sync(0xffffffffu, wj, j + 0);
-          const float w1 = __shfl_sync(0xffffffffu, wj, j + 1);
-          const float w2 = __shfl_sync(0xffffffffu, wj, j + 2);
-          const float w3 = __shfl_sync(0xffffffffu, wj, j + 3);
-          acc.x += w0 * v0.x + w1 * v1.x + w2 * v2.x + w3 * v3.x;
-          acc.y += w0 * v0.y + w1 * v1.y + w2 * v2.y + w3 * v3.y;
-          acc.z += w0 * v0.z + w1 * v1.z + w2 * v2.z + w3 * v3.z;
-          acc.w += w0 * v0.w + w1 * v1.w + w2 * v2.w + w3 * v3.w;
-        }
-        for (; j < num_parts; ++j) {
-          const float4 v0 = act ? ld_stream(base + j * o_stride + c) : zero;
-          const float w0 = __shfl_sync(0xffffffffu, wj, j);
-          acc.x += w0 * v0.x; acc.y += w0 * v0.y; acc.z += w0 * v0.z; acc.w += w0 * v0.w;
+        for (int jj = 0; jj < kGroup; ++jj) {
+          const float w = __shfl_sync(0xffffffffu, wj, (j0 + jj) & 31);
+          acc.x = fmaf(w, v[jj].x, acc.x);
+          acc.y = fmaf(w, v[jj].y, acc.y);
+          acc.z = fmaf(w, v[jj].z, acc.z);
+          acc.w = fmaf(w, v[jj].w, acc.w);
         }
       }
       if (!act) continue;
@@ -154,26 +142,6 @@ int sm_count() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <bool F32>
-void launch_merge(int grid, cudaStream_t st, const float* o_parts, const float* lse_parts,
-                  int num_parts, int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
-                  const int32_t* dst_rows, void* o_out, float* lse_out, int num_out_rows,
-                  int32_t* status) {
-#define CPATTN_MERGE_CASE(NPV)                                                                  \
-  lse_merge_kernel<F32, NPV><<<grid, kMergeThreads, 0, st>>>(o_parts, lse_parts, num_parts,    \
-                                                             o_stride, l_stride, rows, Hq, dv, \
-                                                             dst_rows, o_out, lse_out,         \
-                                                             num_out_rows, status)
-  switch (num_parts) {
-    case 2: CPATTN_MERGE_CASE(2); break;
-    case 4: CPATTN_MERGE_CASE(4); break;
-    case 8: CPATTN_MERGE_CASE(8); break;
-    case 16: CPATTN_MERGE_CASE(16); break;
-    default: CPATTN_MERGE_CASE(0); break;
-  }
-#undef CPATTN_MERGE_CASE
-}
-
 }  // namespace
 }  // namespace cpattn
 
@@ -197,15 +165,15 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
     return CPATTN_ERR_ALIGNMENT;
   const long long units = (long long)rows * Hq;
   const long long want = (units + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
-  const int grid = (int)std::min<long long>(want, (long long)sm_count() * 16);
+  const int grid = (int)std::min<long long>(want, (long long)sm_count() * 3 * 8);
   if (o_out_is_fp32)
-    launch_merge<true>(grid, stream, o_parts, lse_parts, num_parts, o_part_stride,
-                       lse_part_stride, rows, Hq, dv, dst_rows, o_out, lse_out, num_out_rows,
-                       status_dev);
+    lse_merge_kernel<true><<<grid, kMergeThreads, 0, stream>>>(
+        o_parts, lse_parts, num_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows,
+        o_out, lse_out, num_out_rows, status_dev);
   else
-    launch_merge<false>(grid, stream, o_parts, lse_parts, num_parts, o_part_stride,
-                        lse_part_stride, rows, Hq, dv, dst_rows, o_out, lse_out, num_out_rows,
-                        status_dev);
+    lse_merge_kernel<false><<<grid, kMergeThreads, 0, stream>>>(
+        o_parts, lse_parts, num_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows,
+        o_out, lse_out, num_out_rows, status_dev);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

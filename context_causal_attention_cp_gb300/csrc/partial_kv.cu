@@ -1,0 +1,339 @@
+// Partial-KV (ring-style) decomposition of shard attention in one call.
+//
+// Blog "什么是 Context Parallelism", §2.1 item 2 and §3.1: when the whole KV
+// does not fit, a rank's queries meet the KV one block at a time, each block
+// giving a partial output O_j with its log-sum-exp L_j, and the LSE merge
+// (§3.6) makes the result equal to attention over all keys.  On one GPU the
+// ring's rotation becomes a loop over KV blocks in HBM; here every visible
+// (query tile, KV block) pair runs in a single split-KV attention launch.
+//
+// Three launches on the caller's stream:
+//   1. pkv_layout_kernel: per segment, the number of visible KV blocks nb_s
+//      and the first workspace row of its partials (slot_s, an exclusive scan
+//      of nb_s * q_len_s), plus the running count of segment rows.
+//   2. the attention kernel in split mode: CTA (tile, block j, heads) writes
+//      its fp32 partial (O_j, L_j) at workspace rows slot_s + j*q_len_s + i.
+//   3. pkv_merge_kernel: per (segment row, head), the LSE merge of its nb_s
+//      partials, written to output row dst_rows[cat row] (the restore).
+//
+// Workspace layout (caller-allocated, see cp_partial_kv_workspace_size):
+//   int64 slot[num_segs] | int64 rows_before[num_segs + 1] | int64 total
+//   (padded to 256 B) | fp32 O partials [cap_rows, Hq, dv] (padded to 256 B) |
+//   fp32 L partials [cap_rows, Hq]; cap_rows follows from the byte size.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "attn_common.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int kLayoutThreads = 1024;
+
+__host__ __device__ inline long long round256(long long x) { return (x + 255) & ~255LL; }
+
+struct PkvLayout {
+  long long header_bytes, cap_rows, o_off, l_off;
+};
+
+inline PkvLayout pkv_layout(int num_segs, int Hq, int dv, long long workspace_bytes) {
+  PkvLayout L;
+  L.header_bytes = round256((2LL * num_segs + 2) * 8);
+  const long long per_row = (long long)Hq * (dv + 1) * 4;
+  const long long avail = workspace_bytes - L.header_bytes - 256;
+  L.cap_rows = avail > 0 ? avail / per_row : 0;
+  L.o_off = L.header_bytes;
+  L.l_off = L.o_off + round256(L.cap_rows * Hq * dv * 4);
+  return L;
+}
+
+// Block-wide exclusive scan of one 64-bit value per thread (blockDim == 1024).
+__device__ long long block_scan64(long long v, long long* buf /* >= 33 */, long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) buf[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const long long w = lane < (int)(blockDim.x >> 5) ? buf[lane] : 0;
+    long long s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    buf[lane] = s - w;
+    if (lane == 31) buf[32] = s;
+  }
+  __syncthreads();
+  const long long r = buf[wid] + x - v;
+  *total = buf[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+pkv_layout_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_block,
+                  int max_blocks, long long cap_rows, long long* __restrict__ slot,
+                  long long* __restrict__ rows_before, long long* __restrict__ total,
+                  int32_t* status) {
+  __shared__ long long buf[33];
+  long long slot_carry = 0, row_carry = 0;
+  for (int c0 = 0; c0 < num_segs; c0 += kLayoutThreads) {
+    const int s = c0 + threadIdx.x;
+    long long parts = 0, rows = 0;
+    if (s < num_segs) {
+      const cp_segment_t sg = segs[s];
+      if (sg.q_len <= 0 || sg.q_pos0 < 0 || sg.q_pos_step < 0) {
+        set_status(status, CPATTN_ERR_RANGE);
+      } else {
+        const int nb = segment_blocks(sg, kv_block);
+        if (nb > max_blocks) set_status(status, CPATTN_ERR_INVALID_ARG);
+        rows = sg.q_len;
+        parts = (long long)nb * sg.q_len;
+      }
+    }
+    long long t1, t2;
+    const long long so = slot_carry + block_scan64(parts, buf, &t1);
+    const long long ro = row_carry + block_scan64(rows, buf, &t2);
+    if (s < num_segs) {
+      slot[s] = so;
+      rows_before[s] = ro;
+    }
+    slot_carry += t1;
+    row_carry += t2;
+  }
+  if (threadIdx.x == 0) {
+    rows_before[num_segs] = row_carry;
+    *total = slot_carry;
+    if (slot_carry > cap_rows) set_status(status, CPATTN_ERR_INVALID_ARG);
+  }
+}
+
+constexpr int kMergeThreadsP = 256;
+constexpr int kGroupP = 8;
+
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// One warp per (segment row, head): find the segment (binary search on
+// rows_before), merge its nb partials (lane j holds L_j), write the result.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kMergeThreadsP, 3)
+pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_block,
+                 const long long* __restrict__ slot, const long long* __restrict__ rows_before,
+                 const float* __restrict__ ws_o, const float* __restrict__ ws_l, long long cap_rows,
+                 int Hq, int dv, int num_q_rows, const int32_t* __restrict__ dst_rows,
+                 void* __restrict__ o_out, float* __restrict__ lse_out, int num_out_rows,
+                 int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const long long total_rows = rows_before[num_segs];
+  const long long units = total_rows * Hq;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long u = warp0; u < units; u += nwarps) {
+    const long long gr = u / Hq;
+    const int h = (int)(u - gr * Hq);
+    int lo = 0, hi = num_segs;  // last segment with rows_before <= gr
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (rows_before[mid] <= gr) lo = mid; else hi = mid;
+    }
+    const cp_segment_t sg = segs[lo];
+    const int i = (int)(gr - rows_before[lo]);
+    if (i < 0 || i >= sg.q_len) {
+      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const int nb = segment_blocks(sg, kv_block);
+    const long long first = slot[lo] + i;          // partial 0 of this row
+    const long long cat_row = (long long)sg.q_row0 + i;
+    if (cat_row < 0 || cat_row >= num_q_rows) {
+      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const long long out_row = dst_rows ? (long long)__ldg(dst_rows + cat_row) : cat_row;
+    if (nb > 32 || first + (long long)(nb - 1) * sg.q_len >= cap_rows || out_row < 0 ||
+        out_row >= num_out_rows) {
+      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const long long stride_rows = sg.q_len;
+    float lj = -INFINITY;
+    if (lane < nb) lj = __ldg(ws_l + (first + lane * stride_rows) * Hq + h);
+    float m = lj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const bool empty = (m == -INFINITY);
+    const float wj = (lane < nb && !empty) ? __expf(lj - m) : 0.f;
+    float ws = wj;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    const float inv = empty ? 0.f : 1.f / ws;
+    const long long part_stride = stride_rows * Hq * dv;
+    const float* base = ws_o + (first * Hq + h) * dv;
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+      const int c = c0 + lane * 4;
+      const bool act = c < dv;
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = zero;
+      for (int j0 = 0; j0 < nb; j0 += kGroupP) {
+        float4 v[kGroupP];
+#pragma unroll
+        for (int jj = 0; jj < kGroupP; ++jj)
+          v[jj] = (act && j0 + jj < nb) ? ld_stream4(base + (j0 + jj) * part_stride + c) : zero;
+#pragma unroll
+        for (int jj = 0; jj < kGroupP; ++jj) {
+          const float w = __shfl_sync(0xffffffffu, wj, (j0 + jj) & 31);
+          acc.x = fmaf(w, v[jj].x, acc.x);
+          acc.y = fmaf(w, v[jj].y, acc.y);
+          acc.z = fmaf(w, v[jj].z, acc.z);
+          acc.w = fmaf(w, v[jj].w, acc.w);
+        }
+      }
+      if (!act) continue;
+      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+      const long long oo = (out_row * Hq + h) * dv + c;
+      if (OUT_F32) {
+        __stcs(reinterpret_cast<float4*>(static_cast<float*>(o_out) + oo), acc);
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc.x, acc.y);
+        pk.y = pack_bf16x2(acc.z, acc.w);
+        __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oo), pk);
+      }
+    }
+    if (lse_out && lane == 0) lse_out[out_row * Hq + h] = empty ? -INFINITY : m + __logf(ws);
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+using namespace cpattn;
+
+extern "C" int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
+                                            int num_reqs, int cp_size, int strategy, int kv_block,
+                                            int Hq, int dv, int64_t* bytes, int32_t* max_blocks) {
+  if (num_reqs < 0 || num_reqs > CPATTN_MAX_REQS || cp_size < 1 || cp_size > CPATTN_MAX_CP)
+    return CPATTN_ERR_INVALID_ARG;
+  if (strategy != CP_ZIGZAG && strategy != CP_INTERLEAVE) return CPATTN_ERR_INVALID_ARG;
+  if (kv_block < 1 || Hq < 1 || dv < 4 || (dv % 4) != 0 || !bytes) return CPATTN_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (!new_lens || !prefix_lens)) return CPATTN_ERR_INVALID_ARG;
+  const long long C = cp_size;
+  long long rows = 0, segs = 0, flat0 = 0, mb = 0;
+  auto add = [&](long long len, long long last_pos) {
+    if (len <= 0) return;
+    const long long nb = last_pos / kv_block + 1;
+    rows += nb * len;
+    segs += 1;
+    mb = std::max(mb, nb);
+  };
+  for (int b = 0; b < num_reqs; ++b) {
+    const long long n = new_lens[b], p = prefix_lens[b];
+    if (n < 0 || p < 0) return CPATTN_ERR_INVALID_ARG;
+    if (strategy == CP_ZIGZAG) {
+      // the segments cp_shard_plan makes: one per non-empty block
+      const long long nb2 = 2 * C, base = n / nb2, rem = n % nb2;
+      long long st = 0;
+      for (long long k = 0; k < nb2; ++k) {
+        const long long sz = base + (k < rem);
+        add(sz, p + st + sz - 1);
+        st += sz;
+      }
+    } else {
+      for (long long r = 0; r < C; ++r) {
+        const long long i0 = flat0 + (((r - flat0 % C) % C) + C) % C;
+        const long long cnt = (i0 < flat0 + n) ? (flat0 + n - 1 - i0) / C + 1 : 0;
+        if (cnt > 0) add(cnt, p + (i0 + (cnt - 1) * C - flat0));
+      }
+    }
+    flat0 += n;
+  }
+  const long long header = round256((2 * segs + 2) * 8);
+  *bytes = header + round256(rows * Hq * dv * 4) + round256(rows * Hq * 4) + 256;
+  if (max_blocks) *max_blocks = (int32_t)std::min<long long>(mb, 0x7fffffff);
+  return CPATTN_OK;
+}
+
+extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
+                                  const int32_t* tiles_dev, int num_tiles, const void* q,
+                                  int num_q_rows, const void* k, int64_t k_row_stride,
+                                  int64_t k_head_stride, const void* v, int64_t v_row_stride,
+                                  int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
+                                  int dv, float scale, int kv_block, int max_blocks,
+                                  const int32_t* dst_rows, void* o_out, int o_is_fp32,
+                                  float* lse_out, int num_out_rows, void* workspace,
+                                  int64_t workspace_bytes, int32_t* status_dev,
+                                  cudaStream_t stream) {
+  if (num_segs < 0 || kv_block < 1 || max_blocks < 1 || max_blocks > 32 || num_out_rows < 0)
+    return CPATTN_ERR_INVALID_ARG;
+  if (num_segs == 0) return CPATTN_OK;
+  if (!o_out || !workspace || num_out_rows == 0 || Hq < 1 || dv < 4) return CPATTN_ERR_INVALID_ARG;
+  if (!a16(o_out) || !a16(workspace) || (reinterpret_cast<uintptr_t>(lse_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dst_rows) & 3u))
+    return CPATTN_ERR_ALIGNMENT;
+  const PkvLayout L = pkv_layout(num_segs, Hq, dv, workspace_bytes);
+  if (L.cap_rows <= 0) return CPATTN_ERR_INVALID_ARG;
+  auto* base = static_cast<uint8_t*>(workspace);
+  long long* slot = reinterpret_cast<long long*>(base);
+  long long* rows_before = slot + num_segs;
+  long long* total = rows_before + num_segs + 1;
+  float* ws_o = reinterpret_cast<float*>(base + L.o_off);
+  float* ws_l = reinterpret_cast<float*>(base + L.l_off);
+
+  pkv_layout_kernel<<<1, kLayoutThreads, 0, stream>>>(segs_dev, num_segs, kv_block, max_blocks,
+                                                      L.cap_rows, slot, rows_before, total,
+                                                      status_dev);
+  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_CUDA;
+
+  AttnParams prm{};
+  prm.kv_lo = 0;
+  prm.kv_hi = -1;
+  prm.o = ws_o;
+  prm.o_f32 = 1;
+  prm.lse = ws_l;
+  prm.out_row_base = 0;
+  prm.num_out_rows = num_q_rows;  // output placement comes from the workspace slots
+  prm.status = status_dev;
+  prm.split_block = kv_block;
+  prm.max_blocks = max_blocks;
+  prm.ws_slot = slot;
+  prm.ws_rows = L.cap_rows;
+  int rc = attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
+                       k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
+                       scale, prm, stream);
+  if (rc != CPATTN_OK) return rc;
+
+  const int grid = num_sms() * 3 * 8;
+  if (o_is_fp32)
+    pkv_merge_kernel<true><<<grid, kMergeThreadsP, 0, stream>>>(
+        segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
+        o_out, lse_out, num_out_rows, status_dev);
+  else
+    pkv_merge_kernel<false><<<grid, kMergeThreadsP, 0, stream>>>(
+        segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
+        o_out, lse_out, num_out_rows, status_dev);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}

@@ -161,6 +161,44 @@ int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* t
                     int32_t* status_dev, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Partial-KV (ring-style) decomposition in one call.  [CPB-2.1] item 2,
+ * [CPB-3.3] (pass-KV: a rank's queries meet the KV one block at a time, each
+ * block giving (O_j, L_j)), [CPB-3.6] (the merge).
+ *
+ * Every segment's keys are cut into blocks of kv_block key positions, block j
+ * = [j*kv_block, (j+1)*kv_block); a segment whose last row is at position P
+ * sees blocks 0 .. P / kv_block.  For every visible (segment, block) pair and
+ * every head, the fp32 partial (O_j, L_j) of cp_attn_partial with that window
+ * is written to the workspace (one launch over all pairs), then the partials
+ * of each row are LSE-merged (cp_lse_merge's rule) and written to output row
+ * dst_rows[cat row] (dst_rows non-NULL: e.g. the plan's gather index, which
+ * restores causal order) or to the cat row.  The result equals cp_attn_partial
+ * over the full window up to rounding.
+ *
+ *   Arguments shared with cp_attn_partial keep its meaning.
+ *   kv_block > 0; max_blocks: an upper bound on the blocks any segment sees,
+ *     1 <= max_blocks <= 32 (a segment with more sets CPATTN_ERR_INVALID_ARG).
+ *   dst_rows: nullable, [num_q_rows] output row of each cat row.
+ *   o_out: [num_out_rows, Hq, dv] bf16 or fp32; lse_out fp32 [num_out_rows, Hq]
+ *     (nullable).
+ *   workspace: device scratch of workspace_bytes (16-byte aligned), at least
+ *     cp_partial_kv_workspace_size for the plan's lengths; its contents are
+ *     overwritten.  Too small: CPATTN_ERR_INVALID_ARG in *status_dev and the
+ *     partials that do not fit are skipped.
+ * Three launches on the stream (layout, attention, merge). */
+int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
+                                 int num_reqs, int cp_size, int strategy, int kv_block, int Hq,
+                                 int dv, int64_t* bytes, int32_t* max_blocks);
+int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                       int num_tiles, const void* q, int num_q_rows, const void* k,
+                       int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                       int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                       int Hkv, int d, int dv, float scale, int kv_block, int max_blocks,
+                       const int32_t* dst_rows, void* o_out, int o_is_fp32, float* lse_out,
+                       int num_out_rows, void* workspace, int64_t workspace_bytes,
+                       int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Merge num_parts partial results with the log-sum-exp rule.  [CPB-3.6]
  * For each row i < rows and head h < Hq, partial j has
  *     O_j = o_parts[j*o_part_stride + (i*Hq + h)*dv .. +dv]   (fp32)

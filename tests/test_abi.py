@@ -65,14 +65,30 @@ def test_invalid_arguments_are_rejected_on_host():
     assert lib.cp_shard_plan_sizes(neg, a, 2, 4, 0, out, out, out) == L.ERR_INVALID_ARG
     assert lib.cp_shard_plan_sizes(a, a, -1, 4, 0, out, out, out) == L.ERR_INVALID_ARG
     # attention: Hq not a multiple of Hkv, unsupported head dims, bad scale
+    # (never dereferenced: every call below fails validation before any launch)
     nul = None
-    args = [nul, 1, nul, 0, nul, 128, nul, 1024, 128, nul, 1024, 128, 256]
-    assert lib.cp_attn_partial(*args, 6, 4, 128, 128, 0.1, 0, -1, nul, 0, nul, 0, 128, nul,
+    fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(5)]
+    args = [fake[0], 1, nul, 0, fake[1], 128, fake[2], 1024, 128, fake[3], 1024, 128, 256]
+    o, lse = fake[4], ctypes.c_void_p(0x90000)
+    assert lib.cp_attn_partial(*args, 6, 4, 128, 128, 0.1, 0, -1, o, 0, lse, 0, 128, nul,
                                nul) == L.ERR_INVALID_ARG
-    assert lib.cp_attn_partial(*args, 8, 4, 96, 96, 0.1, 0, -1, nul, 0, nul, 0, 128, nul,
+    assert lib.cp_attn_partial(*args, 8, 4, 96, 96, 0.1, 0, -1, o, 0, lse, 0, 128, nul,
                                nul) == L.ERR_UNSUPPORTED
-    assert lib.cp_attn_partial(*args, 8, 4, 128, 128, 0.0, 0, -1, nul, 0, nul, 0, 128, nul,
+    assert lib.cp_attn_partial(*args, 8, 4, 128, 128, 0.0, 0, -1, o, 0, lse, 0, 128, nul,
                                nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial(*args, 8, 4, 128, 128, 0.1, 0, -1, nul, 0, lse, 0, 128, nul,
+                               nul) == L.ERR_INVALID_ARG
+    # partial-KV: block count limits and workspace sizing on the host
+    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 33, nul, o, 0, lse, 128,
+                                  fake[1], 1 << 20, nul, nul) == L.ERR_INVALID_ARG
+    nbytes, mb = ctypes.c_int64(), ctypes.c_int32()
+    one = (ctypes.c_int32 * 1)(1000)
+    zero = (ctypes.c_int32 * 1)(0)
+    assert lib.cp_partial_kv_workspace_size(one, zero, 1, 2, 0, 0, 8, 128, ctypes.byref(nbytes),
+                                            ctypes.byref(mb)) == L.ERR_INVALID_ARG
+    assert lib.cp_partial_kv_workspace_size(one, zero, 1, 2, 0, 256, 8, 128, ctypes.byref(nbytes),
+                                            ctypes.byref(mb)) == L.OK
+    assert mb.value == 4
     # merge: part count and dv limits
     assert lib.cp_lse_merge(nul, nul, 0, 0, 0, 4, 2, 128, nul, nul, 1, nul, 4, nul,
                             nul) == L.ERR_INVALID_ARG
@@ -91,3 +107,20 @@ def test_status_strings():
     for code in (L.OK, L.ERR_INVALID_ARG, L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_TIMEOUT,
                  L.ERR_ALIGNMENT, L.ERR_RANGE):
         assert L.status_string(code) not in ("", "unknown status")
+
+
+@pytest.mark.parametrize("seed", range(20))
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_partial_kv_workspace_matches_oracle_segments(seed, strategy):
+    """Workspace rows = sum over the oracle plan's segments of (visible KV blocks x rows)."""
+    new, pre = W.random_batch(seed, max_new=700, max_prefix=300)
+    C = [1, 2, 3, 4, 8][seed % 5]
+    kv_block = [64, 100, 128, 1000][seed % 4]
+    Hq, dv = 4, 64
+    op = oplan.make_plan(new, pre, C, strategy)
+    segs = [s for r in range(C) for s in op.segments[r]]
+    rows = sum(((s.q_pos0 + (s.q_len - 1) * s.q_pos_step) // kv_block + 1) * s.q_len for s in segs)
+    mb = max([(s.q_pos0 + (s.q_len - 1) * s.q_pos_step) // kv_block + 1 for s in segs] or [0])
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    expect = r256((2 * len(segs) + 2) * 8) + r256(rows * Hq * dv * 4) + r256(rows * Hq * 4) + 256
+    assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv) == (expect, mb)

@@ -350,3 +350,85 @@ def test_wait_limit_reports_timeout_and_context_survives(shape):
     O_ref, L_ref = oatt.attention_rows(np64(q), np64(k), np64(v), pos, np.zeros(n, np.int64), 0.1)
     assert_attn_close(o, lse, O_ref, L_ref, "after timeout")
     assert lib.cp_attn_debug(99, 1) == cpa.api.L.ERR_INVALID_ARG
+
+
+# ------------------------------------------- partial-KV in one library call ----
+
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_partial_kv_fused_small_all_rows(strategy):
+    w = W.Workload(name="pkv_fused", new_lens=[700, 300, 5], prefix_lens=[0, 130, 9], Hq=8,
+                   Hkv=2, d=128, dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=3,
+                   strategies=[strategy], seed=778, kv_block=192)
+    inputs = W.make_inputs(w)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+    k, v = inputs["k"].cuda(), inputs["v"].cuda()
+    o, lse, ws = cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
+                                        new_lens=w.new_lens, prefix_lens=w.prefix_lens,
+                                        status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "fused partial kv")
+    assert_attn_close(o, lse, O_ref, L_ref, f"pkv fused/{strategy}")
+    # cat order, fp32 output, workspace reused
+    o2, lse2, _ = cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
+                                         new_lens=w.new_lens, prefix_lens=w.prefix_lens,
+                                         workspace=ws, dst_rows=None, out_fp32=True,
+                                         status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "fused partial kv, cat order")
+    gi = plan.gather_idx[: w.total_new].long().cpu().numpy()
+    assert_attn_close(o2, lse2, O_ref[gi], L_ref[gi], "pkv fused cat order")
+
+
+def test_partial_kv_fused_mla_small():
+    w = mla_case([260, 70], [0, 33], 4, 2, 990)
+    inputs = W.make_inputs(w)
+    k64 = np64(inputs["k"])
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), k64, k64[:, :, :512],
+                                               w.new_lens, w.prefix_lens, w.scale)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", status=status)
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+    k = inputs["k"].cuda()
+    o, lse, _ = cpa.cp_attn_partial_kv(plan, q_cat, k, k[:, :, :512], w.scale, 100,
+                                       new_lens=w.new_lens, prefix_lens=w.prefix_lens,
+                                       status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "fused partial kv mla")
+    assert_attn_close(o, lse, O_ref, L_ref, "pkv fused mla")
+
+
+def test_partialkv_128k_fused_sampled():
+    w = W.WORKLOADS["partialkv_128k"]
+    inputs = W.make_inputs(w)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", status=status)
+    q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+    o, lse, ws = cpa.cp_attn_partial_kv(plan, q_cat, inputs["k"].cuda(), inputs["v"].cuda(),
+                                        w.scale, w.kv_block, new_lens=w.new_lens,
+                                        prefix_lens=w.prefix_lens, status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, w.name)
+    del ws
+    rows = sorted(set(W.sample_rows(12, w.total_new, 16) +
+                      [0, 8191, 8192, 65535, 65536, 131071]))
+    O_ref, L_ref = oracle_dense_rows(inputs, w.new_lens, w.prefix_lens, w.scale, rows)
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    assert_attn_close(o[idx], lse[idx], O_ref, L_ref, w.name + " fused")
+
+
+def test_partial_kv_workspace_too_small_is_reported():
+    plan = cpa.make_plan([500], [0], 2, "zigzag")
+    q = torch.zeros(500, 2, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(500, 1, 64, dtype=torch.bfloat16, device="cuda")
+    need, _ = cpa.cp_partial_kv_workspace_size([500], [0], 2, "zigzag", 64, 2, 64)
+    small = torch.empty(need // 3, dtype=torch.uint8, device="cuda")
+    status = cpa.new_status()
+    cpa.cp_attn_partial_kv(plan, q, k, k, 0.125, 64, new_lens=[500], prefix_lens=[0],
+                           workspace=small, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) in (cpa.api.L.ERR_INVALID_ARG, cpa.api.L.ERR_RANGE)
