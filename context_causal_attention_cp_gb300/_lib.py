@@ -16,6 +16,8 @@ ERR_CUDA = -3
 ERR_TIMEOUT = -4
 ERR_ALIGNMENT = -5
 ERR_RANGE = -6
+ERR_TOO_LARGE = -7
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 DEBUG_WAIT_LIMIT_NS = 1
 DEBUG_WITHHOLD_Q = 2
@@ -44,6 +46,9 @@ SIGNATURES = {
     "cp_attn_partial_kv": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32,
                                  i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, vp, i32, vp,
                                  i32, vp, i64, vp, vp]),
+    "cp_attn_partial_kv_noalloc": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
+                                         i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
+                                         vp, i32, vp, i32, i64, vp, vp]),
     "cp_attn_debug": (i32, [i32, ctypes.c_longlong]),
     "cp_status_string": (ctypes.c_char_p, [i32]),
 }

@@ -210,6 +210,7 @@ extern "C" const char* cp_status_string(int status) {
     case CPATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
     case CPATTN_ERR_ALIGNMENT: return "misaligned pointer or stride";
     case CPATTN_ERR_RANGE: return "index or segment out of range";
+    case CPATTN_ERR_TOO_LARGE: return "problem needs more scratch than the static buffer";
     default: return "unknown status";
   }
 }

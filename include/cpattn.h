@@ -55,6 +55,7 @@ extern "C" {
 #define CPATTN_ERR_TIMEOUT (-4)      /* device: a pipeline wait exceeded its time limit */
 #define CPATTN_ERR_ALIGNMENT (-5)    /* a pointer or stride is not 16-byte aligned */
 #define CPATTN_ERR_RANGE (-6)        /* device: an index or segment lies outside its buffer */
+#define CPATTN_ERR_TOO_LARGE (-7)    /* the problem needs more scratch than the static buffer */
 
 typedef enum { CP_ZIGZAG = 0, CP_INTERLEAVE = 1 } cp_strategy_t;
 
@@ -197,6 +198,35 @@ int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t
                        const int32_t* dst_rows, void* o_out, int o_is_fp32, float* lse_out,
                        int num_out_rows, void* workspace, int64_t workspace_bytes,
                        int32_t* status_dev, cudaStream_t stream);
+
+/* The same computation as cp_attn_partial_kv, for callers that cannot
+ * allocate device memory: a framework or serving engine whose allocator owns
+ * all device memory, a deployment with a fixed memory budget set at start-up,
+ * or a hot path that cannot take the implicit synchronisation of cudaMalloc /
+ * cudaFree.  There is no counterpart on the source pages.
+ *   The caller still passes inputs and outputs; the scratch is a static device
+ *   array of CPATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
+ *   that loads the library keeps until the process exits.
+ *   workspace_bytes_needed: what cp_partial_kv_workspace_size reports for
+ *     the plan's lengths; above CPATTN_NOALLOC_SCRATCH_BYTES the call returns
+ *     CPATTN_ERR_TOO_LARGE and launches nothing.
+ *   The first call on a device looks up the scratch address on that device
+ *   (cudaGetSymbolAddress, with the device current); make that first call
+ *   before any stream capture.  It allocates nothing (no cudaMalloc/cudaFree).
+ *   All calls share one scratch array, which keeps the last call's contents:
+ *   calls that overlap on the GPU (other streams, other host threads) race on
+ *   it and must be serialised by the caller.  Nothing in it needs clearing.
+ * Other arguments and errors: as cp_attn_partial_kv. */
+#define CPATTN_NOALLOC_SCRATCH_BYTES (64 << 20)
+int cp_attn_partial_kv_noalloc(const cp_segment_t* segs_dev, int num_segs,
+                               const int32_t* tiles_dev, int num_tiles, const void* q,
+                               int num_q_rows, const void* k, int64_t k_row_stride,
+                               int64_t k_head_stride, const void* v, int64_t v_row_stride,
+                               int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
+                               int dv, float scale, int kv_block, int max_blocks,
+                               const int32_t* dst_rows, void* o_out, int o_is_fp32,
+                               float* lse_out, int num_out_rows, int64_t workspace_bytes_needed,
+                               int32_t* status_dev, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Merge num_parts partial results with the log-sum-exp rule.  [CPB-3.6]

@@ -105,7 +105,7 @@ def test_invalid_arguments_are_rejected_on_host():
 
 def test_status_strings():
     for code in (L.OK, L.ERR_INVALID_ARG, L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_TIMEOUT,
-                 L.ERR_ALIGNMENT, L.ERR_RANGE):
+                 L.ERR_ALIGNMENT, L.ERR_RANGE, L.ERR_TOO_LARGE):
         assert L.status_string(code) not in ("", "unknown status")
 
 
