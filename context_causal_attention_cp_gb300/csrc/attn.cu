@@ -40,10 +40,10 @@ template <int D, int DV, int NQ, int KST, int VST>
 struct Cfg {
   // NQ = 2: two softmax warpgroups plus one warpgroup holding the producer and
   // MMA warps, so that setmaxnreg can move registers to the softmax warps
-  // (168 x 384 at launch >= 64 x 128 + 216 x 256 after the split).
+  // (168 x 384 at launch >= 104 x 128 + 200 x 256 after the split).
   static constexpr int kThreads = NQ == 2 ? 384 : NQ * 128 + 64;
   static constexpr bool kSplitRegs = NQ == 2;
-  static constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 64;
+  static constexpr int kRegsLaunch = 168, kRegsSoftmax = 200, kRegsOther = 104;
   static_assert(!kSplitRegs || kRegsOther * 128 + kRegsSoftmax * 256 <= kRegsLaunch * kThreads,
                 "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = NQ * 4;
@@ -201,25 +201,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, 0, 1);
+      // Descriptors are built once; each MMA adds a compile-time offset
+      // (start address >> 4 in the low bits), so the single issuing thread
+      // spends a few independent instructions per MMA instead of a long
+      // dependent chain.
+      const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(k_base, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(v_base, BN * 128, 1024);
       auto issue_qk = [&](int s, int ks) {
-        const uint32_t qa = q_base + s * C::kQTileBytes;
-        const uint32_t ka = k_base + ks * C::kKTileBytes;
+        const uint64_t qd = dq0 + (uint64_t)((s * C::kQTileBytes) >> 4);
+        const uint64_t kd = dk0 + (uint64_t)((ks * C::kKTileBytes) >> 4);
+        const uint32_t dt = tmem_base + s * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          const uint32_t off_k = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-          mma_ss(tmem_base + s * BN, smem_desc_sw128(qa + off_q, 16, 1024),
-                 smem_desc_sw128(ka + off_k, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+          constexpr int kQChunk = (BM * 128) >> 4, kKChunk = (BN * 128) >> 4;
+          const uint64_t oq = (uint64_t)((kk >> 2) * kQChunk + (kk & 3) * 2);
+          const uint64_t ok_ = (uint64_t)((kk >> 2) * kKChunk + (kk & 3) * 2);
+          mma_ss(dt, qd + oq, kd + ok_, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int s, int vs, bool acc) {
-        const uint32_t va = v_base + vs * C::kVTileBytes;
+        const uint64_t vd = dv0 + (uint64_t)((vs * C::kVTileBytes) >> 4);
+        const uint32_t dt = tmem_base + NQ * BN + s * DV;
+        const uint32_t pt = tmem_base + s * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ts(tmem_base + NQ * BN + s * DV, tmem_base + s * BN + kk * 8,
-                 smem_desc_sw128(va + kk * 16 * 128, BN * 128, 1024), kIdescPV,
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(dt, pt + kk * 8, vd + (uint64_t)(kk * ((16 * 128) >> 4)), kIdescPV,
                  (acc || kk > 0) ? 1u : 0u);
-        }
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
       if (ok) ok = mbar_wait(k_full, 0, abort_flag, p.timeout_ns);

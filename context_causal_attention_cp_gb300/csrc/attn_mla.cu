@@ -151,21 +151,24 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, kBNm, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kDVH, 0, 1);
+      // descriptors built once; per MMA only a constant offset is added
+      const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(k_base, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(k_base + 4 * half * kKChunkBytes, kKChunkBytes, 1024);
       auto qk_chunk = [&](int c, uint32_t s_col, bool first) {
+        const uint64_t qd = dq0 + (uint64_t)((c * (BM * 128)) >> 4);
+        const uint64_t kd = dk0 + (uint64_t)((c * kKChunkBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem_base + s_col, smem_desc_sw128(q_base + c * (BM * 128) + kk * 32, 16, 1024),
-                 smem_desc_sw128(k_base + c * kKChunkBytes + kk * 32, 16, 1024), kIdescQK,
+          mma_ss(tmem_base + s_col, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), kIdescQK,
                  (first && kk == 0) ? 0u : 1u);
       };
       auto pv = [&](int j) {
         const uint32_t p_col = (j & 1) * kBNm;
-        const uint32_t v0 = k_base + 4 * half * kKChunkBytes;
 #pragma unroll
         for (int kk = 0; kk < kBNm / 16; ++kk)
           mma_ts(tmem_base + kOCol, tmem_base + p_col + kk * 8,
-                 smem_desc_sw128(v0 + kk * 16 * 128, kKChunkBytes, 1024), kIdescPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+                 dv0 + (uint64_t)(kk * ((16 * 128) >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
       for (int j = 0; j < n_kv && ok; ++j) {

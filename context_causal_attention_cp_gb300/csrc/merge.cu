@@ -35,12 +35,12 @@ __device__ __forceinline__ float4 ld_stream(const float* p) {
 // Each warp merges one (row, head) unit per iteration; lane j < num_parts
 // holds L_j.  dv is split in 128-float chunks, one float4 per lane, and the
 // partials are streamed in groups of kGroup 16-byte loads that are all issued
-// before any is used.  Registers stay under 85 so that three 256-thread blocks
-// share an SM (24 warps, about 96 KB of loads in flight per SM).
-constexpr int kGroup = 8;
+// before any is used (the first group together with the L_j load).  Two
+// 256-thread blocks share an SM: 16 warps, about 128 KB of loads in flight.
+constexpr int kGroup = 16;
 
 template <bool OUT_F32>
-__global__ void __launch_bounds__(kMergeThreads, 3)
+__global__ void __launch_bounds__(kMergeThreads, 2)
 lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
                  int num_parts, int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
                  const int32_t* __restrict__ dst_rows, void* __restrict__ o_out,
@@ -59,8 +59,20 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
         continue;
       }
     }
+    const float* base = o_parts + u * dv;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    // issue the L_j load and the first group of partial loads together, so a
+    // unit with up to kGroup partials costs one memory round trip
     float lj = -INFINITY;
     if (lane < num_parts) lj = __ldg(lse_parts + lane * l_stride + u);
+    float4 v[kGroup];
+    {
+      const int c = lane * 4;
+      const bool act = c < dv;
+#pragma unroll
+      for (int jj = 0; jj < kGroup; ++jj)
+        v[jj] = (act && jj < num_parts) ? ld_stream(base + jj * o_stride + c) : zero;
+    }
     float m = lj;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -70,19 +82,19 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     const float inv = empty ? 0.f : 1.f / ws;
-    const float* base = o_parts + u * dv;
     // every lane runs the same number of chunks and groups so that the weight
     // shuffles always see the full warp; lanes past dv load and store nothing
     for (int c0 = 0; c0 < dv; c0 += 128) {
       const int c = c0 + lane * 4;
       const bool act = c < dv;
-      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc = zero;
       for (int j0 = 0; j0 < num_parts; j0 += kGroup) {
-        float4 v[kGroup];
+        if (c0 > 0 || j0 > 0) {
 #pragma unroll
-        for (int jj = 0; jj < kGroup; ++jj)
-          v[jj] = (act && j0 + jj < num_parts) ? ld_stream(base + (j0 + jj) * o_stride + c) : zero;
+          for (int jj = 0; jj < kGroup; ++jj)
+            v[jj] = (act && j0 + jj < num_parts) ? ld_stream(base + (j0 + jj) * o_stride + c)
+                                                 : zero;
+        }
 #pragma unroll
         for (int jj = 0; jj < kGroup; ++jj) {
           const float w = __shfl_sync(0xffffffffu, wj, (j0 + jj) & 31);
@@ -165,7 +177,7 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
     return CPATTN_ERR_ALIGNMENT;
   const long long units = (long long)rows * Hq;
   const long long want = (units + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
-  const int grid = (int)std::min<long long>(want, (long long)sm_count() * 3 * 8);
+  const int grid = (int)std::min<long long>(want, (long long)sm_count() * 2 * 8);
   if (o_out_is_fp32)
     lse_merge_kernel<true><<<grid, kMergeThreads, 0, stream>>>(
         o_parts, lse_parts, num_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows,

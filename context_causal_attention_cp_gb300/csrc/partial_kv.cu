@@ -116,7 +116,7 @@ pkv_layout_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_bl
 }
 
 constexpr int kMergeThreadsP = 256;
-constexpr int kGroupP = 8;
+constexpr int kGroupP = 16;
 
 __device__ __forceinline__ float4 ld_stream4(const float* p) {
   float4 v;
@@ -129,7 +129,7 @@ __device__ __forceinline__ float4 ld_stream4(const float* p) {
 // One warp per (segment row, head): find the segment (binary search on
 // rows_before), merge its nb partials (lane j holds L_j), write the result.
 template <bool OUT_F32>
-__global__ void __launch_bounds__(kMergeThreadsP, 3)
+__global__ void __launch_bounds__(kMergeThreadsP, 2)
 pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_block,
                  const long long* __restrict__ slot, const long long* __restrict__ rows_before,
                  const float* __restrict__ ws_o, const float* __restrict__ ws_l, long long cap_rows,
@@ -169,8 +169,20 @@ pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_blo
       continue;
     }
     const long long stride_rows = sg.q_len;
+    const long long part_stride = stride_rows * Hq * dv;
+    const float* base = ws_o + (first * Hq + h) * dv;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the L_j load and the first group of partial loads go out together
     float lj = -INFINITY;
     if (lane < nb) lj = __ldg(ws_l + (first + lane * stride_rows) * Hq + h);
+    float4 v[kGroupP];
+    {
+      const int c = lane * 4;
+      const bool act = c < dv;
+#pragma unroll
+      for (int jj = 0; jj < kGroupP; ++jj)
+        v[jj] = (act && jj < nb) ? ld_stream4(base + jj * part_stride + c) : zero;
+    }
     float m = lj;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -180,18 +192,16 @@ pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_blo
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
     const float inv = empty ? 0.f : 1.f / ws;
-    const long long part_stride = stride_rows * Hq * dv;
-    const float* base = ws_o + (first * Hq + h) * dv;
     for (int c0 = 0; c0 < dv; c0 += 128) {
       const int c = c0 + lane * 4;
       const bool act = c < dv;
-      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
       float4 acc = zero;
       for (int j0 = 0; j0 < nb; j0 += kGroupP) {
-        float4 v[kGroupP];
+        if (c0 > 0 || j0 > 0) {
 #pragma unroll
-        for (int jj = 0; jj < kGroupP; ++jj)
-          v[jj] = (act && j0 + jj < nb) ? ld_stream4(base + (j0 + jj) * part_stride + c) : zero;
+          for (int jj = 0; jj < kGroupP; ++jj)
+            v[jj] = (act && j0 + jj < nb) ? ld_stream4(base + (j0 + jj) * part_stride + c) : zero;
+        }
 #pragma unroll
         for (int jj = 0; jj < kGroupP; ++jj) {
           const float w = __shfl_sync(0xffffffffu, wj, (j0 + jj) & 31);
@@ -326,7 +336,7 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                        scale, prm, stream);
   if (rc != CPATTN_OK) return rc;
 
-  const int grid = num_sms() * 3 * 8;
+  const int grid = num_sms() * 2 * 8;
   if (o_is_fp32)
     pkv_merge_kernel<true><<<grid, kMergeThreadsP, 0, stream>>>(
         segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
