@@ -49,9 +49,42 @@ def peaks():
                     source="fallback")
 
 
+def profiled_traffic(kernel_md="attn_fwd_llama8b_32k.md"):
+    """DRAM bytes per launch recorded by the ncu summary under profiles/, or
+    None when the kernel's sources changed since the counters were taken
+    (the summary records a SHA-256 prefix of each source file)."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", kernel_md)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"source_sha256_prefix:\s*(.+)", text)
+    if not m or not h:
+        return None
+    csrc = os.path.join(ROOT, "context_causal_attention_cp_gb300", "csrc")
+    for name, prefix in re.findall(r"([\w.]+) ([0-9a-f]{16})", h.group(1)):
+        try:
+            digest = hashlib.sha256(open(os.path.join(csrc, name), "rb").read()).hexdigest()
+        except OSError:
+            return None
+        if not digest.startswith(prefix):
+            return None
+    return int(m.group(1))
+
+
 def visible_pairs(new_lens, prefix_lens):
     # every new token at position P sees P + 1 keys
     return sum(n * p + n * (n + 1) // 2 for n, p in zip(new_lens, prefix_lens))
+
+
+def algorithmic_bytes(w):
+    """Bytes an attention launch must move: Q, K, V once, O (bf16) and LSE once."""
+    kv = w.total_kv * w.Hkv * (w.d + (0 if w.v_is_k_prefix else w.dv)) * 2
+    return w.total_new * w.Hq * (w.d * 2 + w.dv * 2 + 4) + kv
 
 
 def attention_flops(w):
@@ -304,7 +337,9 @@ def run_ours(args):
             "roofline": {"kernel": kernel_label(w),
                          "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                         "traffic": None,
+                         "traffic": profiled_traffic() if w.name == WORKLOAD else None,
+                         "traffic_unit": "bytes per launch (ncu dram read + write)",
+                         "algorithmic_bytes": algorithmic_bytes(w),
                          "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
             "restore": {"gbs": restore_bytes / (sum(rest_ms) / len(rest_ms) * 1e-3) / 1e9,
                         "bytes_per_step": restore_bytes},
