@@ -121,6 +121,101 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
   }
 }
 
+// Few partials (NP <= 8): a warp step merges U = 16 / NP consecutive units so that
+// every lane still has about 16 partial loads in flight.  Lane L < U*NP owns
+// L_j of (unit L / NP, part L % NP); weights are normalised in the owning lane
+// and broadcast by shuffles.
+template <bool OUT_F32, int NP>
+__global__ void __launch_bounds__(kMergeThreads, 2)
+lse_merge_batched_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                         int64_t o_stride, int64_t l_stride, int rows, int Hq, int dv,
+                         const int32_t* __restrict__ dst_rows, void* __restrict__ o_out,
+                         float* __restrict__ lse_out, int num_out_rows, int32_t* status) {
+  constexpr int U = kGroup / NP;
+  const int lane = threadIdx.x & 31;
+  const long long units = (long long)rows * Hq;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int ui_l = lane / NP, j_l = lane - ui_l * NP;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long ub = warp0 * U; ub < units; ub += nwarps * U) {
+    // output unit (out row * Hq + head) of each unit of this step, -1 when out
+    // of range or past the end (the host keeps num_out_rows * Hq < 2^31 here)
+    int orow[U];
+#pragma unroll
+    for (int ui = 0; ui < U; ++ui) {
+      const long long u = ub + ui;
+      int r = -1;
+      if (u < units) {
+        const int row = (int)(u / Hq), h = (int)(u % Hq);
+        const int dr = dst_rows ? __ldg(dst_rows + row) : row;
+        if (dr >= 0 && dr < num_out_rows) r = dr * Hq + h;
+        else if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      }
+      orow[ui] = r;
+    }
+    const long long u_l = ub + ui_l;
+    float lj = -INFINITY;
+    if (lane < U * NP && u_l < units) lj = __ldg(lse_parts + j_l * l_stride + u_l);
+    float v4[U * NP][4];
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+      const int c = c0 + lane * 4;
+      const bool act = c < dv;
+#pragma unroll
+      for (int sl = 0; sl < U * NP; ++sl) {
+        const int ui = sl / NP, j = sl - ui * NP;
+        const float4 v = (act && orow[ui] >= 0)
+                             ? ld_stream(o_parts + j * o_stride + (ub + ui) * dv + c)
+                             : zero;
+        v4[sl][0] = v.x; v4[sl][1] = v.y; v4[sl][2] = v.z; v4[sl][3] = v.w;
+      }
+      if (c0 == 0) {
+        // per-unit max and normalised weight of the owned (unit, part)
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+          m = fmaxf(m, __shfl_sync(0xffffffffu, lj, (ui_l * NP + j) & 31));
+        const bool empty = (m == -INFINITY);
+        const float w = empty ? 0.f : __expf(lj - m);
+        float sw = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) sw += __shfl_sync(0xffffffffu, w, (ui_l * NP + j) & 31);
+        lj = empty ? 0.f : w / sw;  // lj now holds the normalised weight
+        if (lse_out && lane < U * NP && j_l == 0 && u_l < units) {
+          int r = -1;
+#pragma unroll
+          for (int ui = 0; ui < U; ++ui)
+            if (ui == ui_l) r = orow[ui];
+          if (r >= 0) lse_out[r] = empty ? -INFINITY : m + __logf(sw);
+        }
+      }
+#pragma unroll
+      for (int ui = 0; ui < U; ++ui) {
+        float ax = 0.f, ay = 0.f, az = 0.f, aw = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          const float w = __shfl_sync(0xffffffffu, lj, ui * NP + j);
+          ax = fmaf(w, v4[ui * NP + j][0], ax);
+          ay = fmaf(w, v4[ui * NP + j][1], ay);
+          az = fmaf(w, v4[ui * NP + j][2], az);
+          aw = fmaf(w, v4[ui * NP + j][3], aw);
+        }
+        if (!act || orow[ui] < 0) continue;
+        const long long oo = (long long)orow[ui] * dv + c;
+        if (OUT_F32) {
+          __stcs(reinterpret_cast<float4*>(static_cast<float*>(o_out) + oo),
+                 make_float4(ax, ay, az, aw));
+        } else {
+          uint2 pk;
+          pk.x = pack_bf16x2(ax, ay);
+          pk.y = pack_bf16x2(az, aw);
+          __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oo), pk);
+        }
+      }
+    }
+  }
+}
+
 // dst[i] = src[idx[i]]: vector chunks of type V (16 or 4 bytes), consecutive
 // threads on consecutive chunks of the same row.
 template <typename V>
@@ -178,14 +273,34 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
   const long long units = (long long)rows * Hq;
   const long long want = (units + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
   const int grid = (int)std::min<long long>(want, (long long)sm_count() * 2 * 8);
-  if (o_out_is_fp32)
+  if (num_parts <= kGroup / 2 && (long long)num_out_rows * Hq < (1LL << 31) &&
+      (long long)rows * Hq < (1LL << 31)) {
+#define CPATTN_BATCHED(NPV)                                                                      \
+  case NPV:                                                                                      \
+    if (o_out_is_fp32)                                                                           \
+      lse_merge_batched_kernel<true, NPV><<<grid, kMergeThreads, 0, stream>>>(                   \
+          o_parts, lse_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows, o_out,     \
+          lse_out, num_out_rows, status_dev);                                                    \
+    else                                                                                         \
+      lse_merge_batched_kernel<false, NPV><<<grid, kMergeThreads, 0, stream>>>(                  \
+          o_parts, lse_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows, o_out,     \
+          lse_out, num_out_rows, status_dev);                                                    \
+    break;
+    switch (num_parts) {
+      CPATTN_BATCHED(1) CPATTN_BATCHED(2) CPATTN_BATCHED(3) CPATTN_BATCHED(4)
+      CPATTN_BATCHED(5) CPATTN_BATCHED(6) CPATTN_BATCHED(7) CPATTN_BATCHED(8)
+      default: break;
+    }
+#undef CPATTN_BATCHED
+  } else if (o_out_is_fp32) {
     lse_merge_kernel<true><<<grid, kMergeThreads, 0, stream>>>(
         o_parts, lse_parts, num_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows,
         o_out, lse_out, num_out_rows, status_dev);
-  else
+  } else {
     lse_merge_kernel<false><<<grid, kMergeThreads, 0, stream>>>(
         o_parts, lse_parts, num_parts, o_part_stride, lse_part_stride, rows, Hq, dv, dst_rows,
         o_out, lse_out, num_out_rows, status_dev);
+  }
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
