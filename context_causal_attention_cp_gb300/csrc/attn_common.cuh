@@ -39,6 +39,7 @@ struct AttnParams {
   int split_block, max_blocks;
   const long long* ws_slot;
   long long ws_rows;  // capacity of the partial buffers, rows
+  const void* q;      // query rows (read directly by kernels that stage part of Q in TMEM)
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).

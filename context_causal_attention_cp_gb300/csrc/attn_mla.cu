@@ -11,17 +11,17 @@
 // so the output is split in two 256-column halves computed by sibling CTAs
 // that each recompute S = Q K^T.  One CTA: 128 query rows of one head, one
 // output half, keys in tiles of 64.
-//   shared memory: Q tile 128 x 576 (9 swizzled 64-column chunks, 144 KB) and
-//     one K tile 64 x 576 (9 chunks, 72 KB) with a barrier pair per chunk.  The
-//     K tile also serves as V: the four chunks of this CTA's output half are
-//     the B operand (MN-major) of P V.
-//   tensor memory: S double-buffered (2 x 64 columns, P aliased as bf16) and
-//     the 256-column O half.
-//   order of the MMA thread for key tile j: Q K_j^T over the five chunks that
-//     P V does not read (they were released as soon as S_{j-1} was done),
-//     then P_{j-1} V_{j-1}, which frees the V chunks of tile j-1 for the
-//     producer, then the rest of Q K_j^T on those chunks.  Softmax of tile
-//     j-1 overlaps the first part.
+//   tensor memory (512 columns): S double-buffered (2 x 64, P aliased as
+//     bf16), query chunks 5..8 as the A operand of their Q K^T MMAs (4 x 32
+//     columns of packed bf16) and the 256-column O half.
+//   shared memory: query chunks 0..4 (5 x 16 KB) and two K tiles of
+//     64 x 576 (2 x 72 KB, nine 64-column swizzled chunks each).  A K tile
+//     doubles as V: the four chunks of this CTA's output half are the B
+//     operand (MN-major) of P V.
+//   MMA order: Q K_j^T, then P_{j-1} V_{j-1}.  The softmax of tile j runs
+//     while the tensor core does P_{j-1} V_{j-1} and Q K_{j+1}^T; a K stage is
+//     released once P V has read it.  A rescale of O (rare: lazy max) first
+//     waits for the P V in flight (o_ready).
 #include <algorithm>
 #include <cstdint>
 
@@ -31,14 +31,19 @@ namespace cpattn {
 namespace {
 
 constexpr int kD = 576, kDV = 512, kDVH = 256, kBNm = 64, kChunks = kD / 64;
+constexpr int kQSmemChunks = 5;                       // query chunks 0..4 in shared memory
+constexpr int kQTmemChunks = kChunks - kQSmemChunks;  // chunks 5..8 in tensor memory
 constexpr int kThreadsM = 192;  // 4 softmax warps, producer warp, MMA warp
-constexpr int kQBytes = BM * kD * 2;          // 147456
-constexpr int kKChunkBytes = kBNm * 128;      // 8192 (64 keys x 64 bf16)
-constexpr int kKOffM = kQBytes;
-constexpr int kBarOffM = kKOffM + kChunks * kKChunkBytes;
-constexpr int kNumBarsM = 1 + 2 * kChunks + 2 + 2 + 1 + 1;
+constexpr int kQChunkBytes = BM * 128;               // 16384
+constexpr int kKChunkBytes = kBNm * 128;             // 8192 (64 keys x 64 bf16)
+constexpr int kKTileBytes = kChunks * kKChunkBytes;  // 73728
+constexpr int kKOffM = kQSmemChunks * kQChunkBytes;  // 81920
+constexpr int kBarOffM = kKOffM + 2 * kKTileBytes;   // 229376
+// bar_q, qt_full, k_full[2], k_empty[2], s_full[2], p_full[2], o_ready, o_full, drain
+constexpr int kNumBarsM = 13;
 constexpr int kSmemM = kBarOffM + kNumBarsM * 8 + 16 + 1024;
 static_assert(kSmemM <= 232448, "MLA tile exceeds shared memory");
+constexpr uint32_t kSCol = 0, kQtCol = 128, kOCol = 256;  // TMEM column map
 
 __global__ void __launch_bounds__(kThreadsM, 1)
 attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -48,17 +53,20 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffM);
   uint64_t* bar_q = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + kChunks;
-  uint64_t* s_full = k_empty + kChunks;  // [2]
-  uint64_t* p_full = s_full + 2;         // [2]
-  uint64_t* o_full = p_full + 2;
-  uint64_t* bar_drain = o_full + 1;
+  uint64_t* qt_full = bars + 1;
+  uint64_t* k_full = bars + 2;   // [2]
+  uint64_t* k_empty = bars + 4;  // [2]
+  uint64_t* s_full = bars + 6;   // [2]
+  uint64_t* p_full = bars + 8;   // [2]
+  uint64_t* o_ready = bars + 10;
+  uint64_t* o_full = bars + 11;
+  uint64_t* bar_drain = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarsM);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* issued_ctr = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item: (128-row tile, query head, output half) ----
+  // ---- work item: (128-row tile [, KV block], query head, output half) ----
   const int half = blockIdx.x & 1;
   const int h = (blockIdx.x >> 1) % p.Hq;
   const int rest = (blockIdx.x >> 1) / p.Hq;
@@ -77,26 +85,17 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int j0 = win_lo / kBNm;
   const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + kBNm - 1) / kBNm - j0 : 0;
   const int kv_head = h / p.g;
-  // chunk order: the five chunks P V does not read, then this half's V chunks
-  int order[kChunks];
-  {
-    int n = 0;
-    for (int c = 0; c < kChunks; ++c)
-      if (c < 4 * half || c >= 4 * half + 4) order[n++] = c;
-    for (int c = 4 * half; c < 4 * half + 4; ++c) order[n++] = c;
-  }
-  constexpr int kNonV = kChunks - 4;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int c = 0; c < kChunks; ++c) {
-      mbar_init(k_full + c, 1);
-      mbar_init(k_empty + c, 1);
+    mbar_init(qt_full, 128);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(k_full + st, 1);
+      mbar_init(k_empty + st, 1);
+      mbar_init(s_full + st, 1);
+      mbar_init(p_full + st, 128);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full + b, 1);
-      mbar_init(p_full + b, 128);
-    }
+    mbar_init(o_ready, 1);
     mbar_init(o_full, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -111,34 +110,31 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // producer's issued chunk-load count, kept in shared memory for the abort drain
-  volatile int* issued_ctr = reinterpret_cast<volatile int*>(tmem_slot + 2);
   const uint32_t q_base = smem_u32(smem);
   const uint32_t k_base = smem_u32(smem + kKOffM);
-  constexpr uint32_t kOCol = 256;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer --
     if (lane == 0 && n_kv > 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      int issued = 0;
       if (!p.withhold_q) {
-        mbar_arrive_expect_tx(bar_q, kQBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(smem + c * (BM * 128), &tm_q, bar_q, c * 64, h, sg.q_row0 + r0);
+        mbar_arrive_expect_tx(bar_q, kQSmemChunks * kQChunkBytes);
+        for (int c = 0; c < kQSmemChunks; ++c)
+          tma_load_3d(smem + c * kQChunkBytes, &tm_q, bar_q, c * 64, h, sg.q_row0 + r0);
       }
       bool ok = true;
-      for (int it = 0; it < n_kv && ok; ++it) {
-        const int kv_row = sg.kv_row0 + (j0 + it) * kBNm;
-        for (int i = 0; i < kChunks; ++i) {
-          const int c = order[i];
-          ok = mbar_wait(k_empty + c, (it & 1) ^ 1, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          mbar_arrive_expect_tx(k_full + c, kKChunkBytes);
-          tma_load_3d(smem + kKOffM + c * kKChunkBytes, &tm_k, k_full + c, c * 64, kv_head, kv_row);
-          ++issued;
-        }
+      int issued = 0;  // K tiles issued
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j & 1;
+        ok = mbar_wait(k_empty + st, ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        const int kv_row = sg.kv_row0 + (j0 + j) * kBNm;
+        mbar_arrive_expect_tx(k_full + st, kKTileBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(smem + kKOffM + st * kKTileBytes + c * kKChunkBytes, &tm_k, k_full + st,
+                      c * 64, kv_head, kv_row);
+        ++issued;
       }
       *issued_ctr = issued;
       if (!ok) {
@@ -155,56 +151,56 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(k_base, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(k_base + 4 * half * kKChunkBytes, kKChunkBytes, 1024);
-      auto qk_chunk = [&](int c, uint32_t s_col, bool first) {
-        const uint64_t qd = dq0 + (uint64_t)((c * (BM * 128)) >> 4);
-        const uint64_t kd = dk0 + (uint64_t)((c * kKChunkBytes) >> 4);
+      auto qk = [&](int j) {
+        const uint32_t s_tm = tmem_base + kSCol + (j & 1) * kBNm;
+        const uint64_t kd = dk0 + (uint64_t)(((j & 1) * kKTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem_base + s_col, qd + (uint64_t)(kk * 2), kd + (uint64_t)(kk * 2), kIdescQK,
-                 (first && kk == 0) ? 0u : 1u);
+        for (int c = 0; c < kQSmemChunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(s_tm, dq0 + (uint64_t)((c * kQChunkBytes) >> 4) + kk * 2,
+                   kd + (uint64_t)((c * kKChunkBytes) >> 4) + kk * 2, kIdescQK,
+                   (c == 0 && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int c = 0; c < kQTmemChunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(s_tm, tmem_base + kQtCol + c * 32 + kk * 8,
+                   kd + (uint64_t)(((kQSmemChunks + c) * kKChunkBytes) >> 4) + kk * 2, kIdescQK,
+                   1u);
       };
       auto pv = [&](int j) {
-        const uint32_t p_col = (j & 1) * kBNm;
+        const uint32_t p_tm = tmem_base + kSCol + (j & 1) * kBNm;
+        const uint64_t vd = dv0 + (uint64_t)(((j & 1) * kKTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBNm / 16; ++kk)
-          mma_ts(tmem_base + kOCol, tmem_base + p_col + kk * 8,
-                 dv0 + (uint64_t)(kk * ((16 * 128) >> 4)), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem_base + kOCol, p_tm + kk * 8, vd + (uint64_t)(kk * ((16 * 128) >> 4)),
+                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
+      if (ok) ok = mbar_wait(qt_full, 0, abort_flag, p.timeout_ns);
       for (int j = 0; j < n_kv && ok; ++j) {
-        const uint32_t s_col = (j & 1) * kBNm;
-        for (int i = 0; i < kNonV && ok; ++i) {
-          const int c = order[i];
-          ok = mbar_wait(k_full + c, j & 1, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          qk_chunk(c, s_col, i == 0);
-          mma_commit(k_empty + c);
-        }
+        ok = mbar_wait(k_full + (j & 1), (j >> 1) & 1, abort_flag, p.timeout_ns);
         if (!ok) break;
-        if (j > 0) {
-          ok = mbar_wait(p_full + ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          pv(j - 1);
-          for (int i = kNonV; i < kChunks; ++i) mma_commit(k_empty + order[i]);
-        }
-        for (int i = kNonV; i < kChunks && ok; ++i) {
-          const int c = order[i];
-          ok = mbar_wait(k_full + c, j & 1, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          qk_chunk(c, s_col, false);
-        }
-        if (!ok) break;
+        tc_fence_after();
+        qk(j);
         mma_commit(s_full + (j & 1));
+        if (j > 0) {
+          const int jp = j - 1;
+          ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          pv(jp);
+          mma_commit(o_ready);
+          mma_commit(k_empty + (jp & 1));
+        }
       }
       if (ok) {
-        const int j = n_kv - 1;
-        ok = mbar_wait(p_full + (j & 1), (j >> 1) & 1, abort_flag, p.timeout_ns);
+        const int jp = n_kv - 1;
+        ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
         if (ok) {
           tc_fence_after();
-          pv(j);
+          pv(jp);
           mma_commit(o_full);
         }
       }
@@ -225,6 +221,30 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
     bool ok = true;
+    if (n_kv > 0) {
+      // query chunks 5..8 of this row into tensor memory (packed bf16 pairs,
+      // the A-operand layout: row = lane, K along columns)
+      const long long qrow = (long long)sg.q_row0 + r0 + row;
+      const bool in_q = qrow < p.num_q_rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + (in_q ? qrow * p.Hq + h : 0) * kD);
+#pragma unroll
+      for (int c = 0; c < kQTmemChunks; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w = in_q ? __ldg(src + (kQSmemChunks + c) * 8 + v) : make_uint4(0, 0, 0, 0);
+          r[4 * v] = w.x;
+          r[4 * v + 1] = w.y;
+          r[4 * v + 2] = w.z;
+          r[4 * v + 3] = w.w;
+        }
+        tmem_st32(lane_addr + kQtCol + c * 32, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qt_full);
+    }
     for (int j = 0; j < n_kv; ++j) {
       const int b = j & 1;
       ok = mbar_wait_warp(s_full + b, (j >> 1) & 1, abort_flag, p.timeout_ns);
@@ -233,8 +253,8 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float x[kBNm];
       {
         uint32_t r[kBNm];
-        tmem_ld32p(lane_addr + b * kBNm, r);
-        tmem_ld32p(lane_addr + b * kBNm + 32, r + 32);
+        tmem_ld32p(lane_addr + kSCol + b * kBNm, r);
+        tmem_ld32p(lane_addr + kSCol + b * kBNm + 32, r + 32);
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < kBNm; ++c) x[c] = __uint_as_float(r[c]);
@@ -258,6 +278,24 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const float m_new = move ? mx : m_run;
       const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = move ? ex2_approx(m_run - m_new_use) : 1.f;
+      // O rescale (rare: lazy max): P V of tile j-1 may still be in flight,
+      // so wait for it first (o_ready completes once per P V)
+      const bool need = (j > 0) && move;
+      if (__any_sync(0xffffffffu, need)) {
+        ok = mbar_wait_warp(o_ready, (j - 1) & 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const float a = need ? alpha : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < kDVH / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32p(lane_addr + kOCol + q * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * a);
+          tmem_st32(lane_addr + kOCol + q * 32, r);
+        }
+      }
       float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int q = 0; q < kBNm / 32; ++q) {
@@ -271,23 +309,9 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           fadd2(sum0, sum1, sum0, sum1, a, bb);
           pk[c >> 1] = pack_bf16x2(a, bb);
         }
-        tmem_st16(lane_addr + b * kBNm + q * 16, pk);
+        tmem_st16(lane_addr + kSCol + b * kBNm + q * 16, pk);
       }
       l_run = l_run * alpha + (sum0 + sum1);
-      // P_{j-1} V_{j-1} has completed: S_j was committed after it was issued
-      const bool need = (j > 0) && move;
-      if (__any_sync(0xffffffffu, need)) {
-        const float a = need ? alpha : 1.f;
-#pragma unroll 1
-        for (int q = 0; q < kDVH / 32; ++q) {
-          uint32_t r[32];
-          tmem_ld32p(lane_addr + kOCol + q * 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * a);
-          tmem_st32(lane_addr + kOCol + q * 32, r);
-        }
-      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + b);
@@ -346,15 +370,11 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 4) {
     if (lane == 0 && *abort_flag && n_kv > 0) {
       // after an abort, let this CTA's own copies land before its shared
-      // memory is released: Q, and the last load of every chunk
+      // memory is released: Q and the last load of each K stage
       const int issued = *issued_ctr;
       if (!p.withhold_q) mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
-      const int it_last = (issued - 1) / kChunks;
-      for (int i = 0; i < kChunks && issued > 0; ++i) {
-        const int c = order[i];
-        const int it_c = (i < issued - it_last * kChunks) ? it_last : it_last - 1;
-        if (it_c >= 0) mbar_wait(k_full + c, it_c & 1, nullptr, p.timeout_ns);
-      }
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait(k_full + (j & 1), (j >> 1) & 1, nullptr, p.timeout_ns);
     }
     __syncwarp();
     tc_fence_after();
@@ -371,6 +391,7 @@ int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_
   if (!make_map(&mq, q, kD, prm.Hq, num_q_rows, kD, (long long)prm.Hq * kD) ||
       !make_map(&mk, k, kD, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBNm))
     return CPATTN_ERR_CUDA;
+  prm.q = q;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
