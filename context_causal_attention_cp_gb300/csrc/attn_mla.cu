@@ -14,14 +14,15 @@
 //   tensor memory (512 columns): S double-buffered (2 x 64, P aliased as
 //     bf16), query chunks 5..8 as the A operand of their Q K^T MMAs (4 x 32
 //     columns of packed bf16) and the 256-column O half.
-//   shared memory: query chunks 0..4 (5 x 16 KB) and two K tiles of
-//     64 x 576 (2 x 72 KB, nine 64-column swizzled chunks each).  A K tile
-//     doubles as V: the four chunks of this CTA's output half are the B
-//     operand (MN-major) of P V.
-//   MMA order: Q K_j^T, then P_{j-1} V_{j-1}.  The softmax of tile j runs
-//     while the tensor core does P_{j-1} V_{j-1} and Q K_{j+1}^T; a K stage is
-//     released once P V has read it.  A rescale of O (rare: lazy max) first
-//     waits for the P V in flight (o_ready).
+//   shared memory: query chunks 0..4 (5 x 16 KB) and K tiles of 64 x 576 in
+//     two double-buffered rings of 64-column swizzled chunks: the four chunks
+//     of this CTA's output half (the V ring; they double as V, the B operand
+//     of P V, MN-major) and the other five (the non-V ring).
+//   MMA order per tile j: Q K_j^T over the non-V chunks (their stage is
+//     released right after), P_{j-1} V_{j-1} (releases the V stage of tile
+//     j-1), then Q K_j^T over the V chunks, so a stage's reload has a whole
+//     tile of MMAs to land.  A rescale of O (rare: lazy max) first waits for
+//     the P V in flight (o_ready).
 #include <algorithm>
 #include <cstdint>
 
@@ -36,11 +37,13 @@ constexpr int kQTmemChunks = kChunks - kQSmemChunks;  // chunks 5..8 in tensor m
 constexpr int kThreadsM = 192;  // 4 softmax warps, producer warp, MMA warp
 constexpr int kQChunkBytes = BM * 128;               // 16384
 constexpr int kKChunkBytes = kBNm * 128;             // 8192 (64 keys x 64 bf16)
-constexpr int kKTileBytes = kChunks * kKChunkBytes;  // 73728
-constexpr int kKOffM = kQSmemChunks * kQChunkBytes;  // 81920
-constexpr int kBarOffM = kKOffM + 2 * kKTileBytes;   // 229376
-// bar_q, qt_full, k_full[2], k_empty[2], s_full[2], p_full[2], o_ready, o_full, drain
-constexpr int kNumBarsM = 13;
+constexpr int kVChunks = 4, kNChunks = kChunks - kVChunks;  // per K tile: V part, non-V part
+constexpr int kNOff = kQSmemChunks * kQChunkBytes;            // non-V ring: 2 x 5 chunks
+constexpr int kVOff = kNOff + 2 * kNChunks * kKChunkBytes;    // V ring: 2 x 4 chunks
+constexpr int kBarOffM = kVOff + 2 * kVChunks * kKChunkBytes;  // 229376
+// bar_q, qt_full, n_full[2], n_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
+// o_ready, o_full, drain
+constexpr int kNumBarsM = 17;
 constexpr int kSmemM = kBarOffM + kNumBarsM * 8 + 16 + 1024;
 static_assert(kSmemM <= 232448, "MLA tile exceeds shared memory");
 constexpr uint32_t kSCol = 0, kQtCol = 128, kOCol = 256;  // TMEM column map
@@ -54,16 +57,19 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOffM);
   uint64_t* bar_q = bars;
   uint64_t* qt_full = bars + 1;
-  uint64_t* k_full = bars + 2;   // [2]
-  uint64_t* k_empty = bars + 4;  // [2]
-  uint64_t* s_full = bars + 6;   // [2]
-  uint64_t* p_full = bars + 8;   // [2]
-  uint64_t* o_ready = bars + 10;
-  uint64_t* o_full = bars + 11;
-  uint64_t* bar_drain = bars + 12;
+  uint64_t* n_full = bars + 2;    // [2] non-V chunks of a K tile
+  uint64_t* n_empty = bars + 4;   // [2]
+  uint64_t* v_full = bars + 6;    // [2] this half's V chunks of a K tile
+  uint64_t* v_empty = bars + 8;   // [2]
+  uint64_t* s_full = bars + 10;   // [2]
+  uint64_t* p_full = bars + 12;   // [2]
+  uint64_t* o_ready = bars + 14;
+  uint64_t* o_full = bars + 15;
+  uint64_t* bar_drain = bars + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBarsM);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* issued_ctr = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* issued_n = reinterpret_cast<volatile int*>(tmem_slot + 2);  // non-V loads issued
+  volatile int* issued_v = reinterpret_cast<volatile int*>(tmem_slot + 3);  // V loads issued
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: (128-row tile [, KV block], query head, output half) ----
@@ -90,8 +96,10 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_q, 1);
     mbar_init(qt_full, 128);
     for (int st = 0; st < 2; ++st) {
-      mbar_init(k_full + st, 1);
-      mbar_init(k_empty + st, 1);
+      mbar_init(n_full + st, 1);
+      mbar_init(n_empty + st, 1);
+      mbar_init(v_full + st, 1);
+      mbar_init(v_empty + st, 1);
       mbar_init(s_full + st, 1);
       mbar_init(p_full + st, 128);
     }
@@ -100,6 +108,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     tmem_slot[2] = 0;
+    tmem_slot[3] = 0;
     fence_barrier_init();
   }
   if (warp == 4) {
@@ -111,7 +120,10 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t q_base = smem_u32(smem);
-  const uint32_t k_base = smem_u32(smem + kKOffM);
+  // chunk c of the K tile is a V chunk of this half iff 4*half <= c < 4*half+4;
+  // non-V chunks are numbered 0..4 in increasing c
+  auto is_v = [&](int c) { return c >= kVChunks * half && c < kVChunks * (half + 1); };
+  auto n_slot = [&](int c) { return c < kVChunks * half ? c : c - kVChunks; };
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer --
@@ -124,19 +136,28 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tma_load_3d(smem + c * kQChunkBytes, &tm_q, bar_q, c * 64, h, sg.q_row0 + r0);
       }
       bool ok = true;
-      int issued = 0;  // K tiles issued
+      int in = 0, iv = 0;  // loads issued per ring
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
-        ok = mbar_wait(k_empty + st, ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
-        if (!ok) break;
         const int kv_row = sg.kv_row0 + (j0 + j) * kBNm;
-        mbar_arrive_expect_tx(k_full + st, kKTileBytes);
+        ok = mbar_wait(n_empty + st, ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(n_full + st, kNChunks * kKChunkBytes);
         for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(smem + kKOffM + st * kKTileBytes + c * kKChunkBytes, &tm_k, k_full + st,
-                      c * 64, kv_head, kv_row);
-        ++issued;
+          if (!is_v(c))
+            tma_load_3d(smem + kNOff + (st * kNChunks + n_slot(c)) * kKChunkBytes, &tm_k,
+                        n_full + st, c * 64, kv_head, kv_row);
+        ++in;
+        ok = mbar_wait(v_empty + st, ((j >> 1) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        mbar_arrive_expect_tx(v_full + st, kVChunks * kKChunkBytes);
+        for (int c = kVChunks * half; c < kVChunks * (half + 1); ++c)
+          tma_load_3d(smem + kVOff + (st * kVChunks + c - kVChunks * half) * kKChunkBytes, &tm_k,
+                      v_full + st, c * 64, kv_head, kv_row);
+        ++iv;
       }
-      *issued_ctr = issued;
+      *issued_n = in;
+      *issued_v = iv;
       if (!ok) {
         set_status(p.status, CPATTN_ERR_TIMEOUT);
         *abort_flag = 1;
@@ -149,42 +170,54 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kDVH, 0, 1);
       // descriptors built once; per MMA only a constant offset is added
       const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(k_base, 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(k_base + 4 * half * kKChunkBytes, kKChunkBytes, 1024);
-      auto qk = [&](int j) {
+      const uint64_t dn0 = smem_desc_sw128(smem_u32(smem + kNOff), 16, 1024);
+      const uint64_t dkv0 = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kVOff), kKChunkBytes, 1024);
+      // Q K^T over chunk c of tile j (Q chunk from shared or tensor memory,
+      // K chunk from the ring that holds it)
+      auto qk_chunk = [&](int j, int c, bool first) {
         const uint32_t s_tm = tmem_base + kSCol + (j & 1) * kBNm;
-        const uint64_t kd = dk0 + (uint64_t)(((j & 1) * kKTileBytes) >> 4);
-#pragma unroll
-        for (int c = 0; c < kQSmemChunks; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(s_tm, dq0 + (uint64_t)((c * kQChunkBytes) >> 4) + kk * 2,
-                   kd + (uint64_t)((c * kKChunkBytes) >> 4) + kk * 2, kIdescQK,
-                   (c == 0 && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int c = 0; c < kQTmemChunks; ++c)
+        const int st = j & 1;
+        const uint64_t kd = is_v(c)
+            ? dkv0 + (uint64_t)(((st * kVChunks + c - kVChunks * half) * kKChunkBytes) >> 4)
+            : dn0 + (uint64_t)(((st * kNChunks + n_slot(c)) * kKChunkBytes) >> 4);
+        if (c < kQSmemChunks) {
+          const uint64_t qd = dq0 + (uint64_t)((c * kQChunkBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(s_tm, tmem_base + kQtCol + c * 32 + kk * 8,
-                   kd + (uint64_t)(((kQSmemChunks + c) * kKChunkBytes) >> 4) + kk * 2, kIdescQK,
-                   1u);
+            mma_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
+        } else {
+          const uint32_t qt = tmem_base + kQtCol + (c - kQSmemChunks) * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(s_tm, qt + kk * 8, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
+        }
       };
       auto pv = [&](int j) {
         const uint32_t p_tm = tmem_base + kSCol + (j & 1) * kBNm;
-        const uint64_t vd = dv0 + (uint64_t)(((j & 1) * kKTileBytes) >> 4);
+        const uint64_t vd = dv0 + (uint64_t)((((j & 1) * kVChunks) * kKChunkBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBNm / 16; ++kk)
           mma_ts(tmem_base + kOCol, p_tm + kk * 8, vd + (uint64_t)(kk * ((16 * 128) >> 4)),
                  kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
+      // Per tile j: Q K_j^T on the non-V chunks (released right after), then
+      // P_{j-1} V_{j-1} (frees the V chunks of tile j-1), then Q K_j^T on the
+      // V chunks; the V reload of a stage has a whole tile of MMAs to land.
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
       if (ok) ok = mbar_wait(qt_full, 0, abort_flag, p.timeout_ns);
       for (int j = 0; j < n_kv && ok; ++j) {
-        ok = mbar_wait(k_full + (j & 1), (j >> 1) & 1, abort_flag, p.timeout_ns);
+        const int st = j & 1;
+        ok = mbar_wait(n_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        qk(j);
-        mma_commit(s_full + (j & 1));
+        bool first = true;
+        for (int c = 0; c < kChunks; ++c)
+          if (!is_v(c)) {
+            qk_chunk(j, c, first);
+            first = false;
+          }
+        mma_commit(n_empty + st);
         if (j > 0) {
           const int jp = j - 1;
           ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
@@ -192,8 +225,13 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tc_fence_after();
           pv(jp);
           mma_commit(o_ready);
-          mma_commit(k_empty + (jp & 1));
+          mma_commit(v_empty + (jp & 1));
         }
+        ok = mbar_wait(v_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        for (int c = kVChunks * half; c < kVChunks * (half + 1); ++c) qk_chunk(j, c, false);
+        mma_commit(s_full + st);
       }
       if (ok) {
         const int jp = n_kv - 1;
@@ -370,11 +408,13 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 4) {
     if (lane == 0 && *abort_flag && n_kv > 0) {
       // after an abort, let this CTA's own copies land before its shared
-      // memory is released: Q and the last load of each K stage
-      const int issued = *issued_ctr;
+      // memory is released: Q and the last load of each stage of both rings
+      const int in = *issued_n, iv = *issued_v;
       if (!p.withhold_q) mbar_wait(bar_q, 0, nullptr, p.timeout_ns);
-      for (int j = max(0, issued - 2); j < issued; ++j)
-        mbar_wait(k_full + (j & 1), (j >> 1) & 1, nullptr, p.timeout_ns);
+      for (int j = max(0, in - 2); j < in; ++j)
+        mbar_wait(n_full + (j & 1), (j >> 1) & 1, nullptr, p.timeout_ns);
+      for (int j = max(0, iv - 2); j < iv; ++j)
+        mbar_wait(v_full + (j & 1), (j >> 1) & 1, nullptr, p.timeout_ns);
     }
     __syncwarp();
     tc_fence_after();
