@@ -11,15 +11,19 @@ from .api import (  # noqa: F401
     alloc_plan,
     check_status,
     cp_attn_partial,
+    cp_attn_partial_accumulate,
     cp_attn_partial_kv,
+    cp_attn_partial_restore,
     cp_lse_merge,
     cp_partial_kv_workspace_size,
     cp_partial_kv_attention,
+    cp_pass_q_attention,
     cp_prefill_attention,
     cp_restore,
     cp_shard_plan,
     cp_shard_plan_sizes,
     make_plan,
     new_status,
+    pass_q_kv_blocks,
     segments_host,
 )

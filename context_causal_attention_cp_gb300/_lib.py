@@ -39,6 +39,12 @@ SIGNATURES = {
     "cp_attn_partial": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32, i32,
                               i32, i32, i32, ctypes.c_float, i32, i32, vp, i32, vp, i32, i32,
                               vp, vp]),
+    "cp_attn_partial_restore": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
+                                      i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, vp,
+                                      i32, vp, i32, vp, vp]),
+    "cp_attn_partial_accumulate": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
+                                         i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
+                                         vp, vp, i32, i32, vp, vp]),
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
     "cp_partial_kv_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32,

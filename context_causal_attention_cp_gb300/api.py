@@ -163,6 +163,65 @@ def cp_attn_partial(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tile
     return out, lse
 
 
+def _check_qkv(q, k, v):
+    if k.shape[1] != v.shape[1] or k.shape[0] != v.shape[0]:
+        raise ValueError("k and v disagree on rows or heads")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("q, k and v must be bfloat16")
+    if not q.is_contiguous() or k.stride(2) != 1 or v.stride(2) != 1:
+        raise ValueError("q must be contiguous; k and v need a contiguous last dim")
+
+
+def cp_attn_partial_restore(segs, q, k, v, scale, dst_rows, *, num_out_rows=None,
+                            num_segs=None, tiles=None, num_tiles=None, kv_lo=0, kv_hi=-1,
+                            out=None, lse=None, out_fp32=False, status=None, stream=None):
+    """cp_attn_partial storing query row i at output row dst_rows[i] (restore fused)."""
+    lib = L.load()
+    _check_qkv(q, k, v)
+    rows, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    if dst_rows.dtype != torch.int32 or dst_rows.shape[0] < rows:
+        raise ValueError("dst_rows must be int32 with one entry per query row")
+    n_out = rows if num_out_rows is None else num_out_rows
+    if out is None:
+        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=q.device)
+    if lse is None:
+        lse = torch.empty((n_out, Hq), dtype=torch.float32, device=q.device)
+    ns = segs.shape[0] if num_segs is None else num_segs
+    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
+    L.check(lib.cp_attn_partial_restore(
+        _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
+        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
+        int(kv_hi), _p(dst_rows), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse),
+        out.shape[0], _p(status), _stream(stream)), "cp_attn_partial_restore")
+    return out, lse
+
+
+def cp_attn_partial_accumulate(segs, q, k, v, scale, o_acc, lse_acc, lse_out, *, num_segs=None,
+                               tiles=None, num_tiles=None, kv_lo=0, kv_hi=-1, out_row_base=0,
+                               status=None, stream=None):
+    """One pass-Q hop: merge this window's partial into (o_acc, lse_acc) -> (o_acc, lse_out)."""
+    lib = L.load()
+    _check_qkv(q, k, v)
+    rows, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    if o_acc.dtype != torch.float32 or lse_acc.dtype != torch.float32 or \
+            lse_out.dtype != torch.float32:
+        raise TypeError("the accumulator is float32")
+    if o_acc.shape[1:] != (Hq, dv) or not o_acc.is_contiguous() or \
+            lse_acc.shape != (o_acc.shape[0], Hq) or lse_out.shape != lse_acc.shape:
+        raise ValueError("accumulator shapes disagree with q / v")
+    ns = segs.shape[0] if num_segs is None else num_segs
+    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
+    L.check(lib.cp_attn_partial_accumulate(
+        _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
+        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
+        int(kv_hi), _p(o_acc), _p(lse_acc), _p(lse_out), int(out_row_base), o_acc.shape[0],
+        _p(status), _stream(stream)), "cp_attn_partial_accumulate")
+    return o_acc, lse_out
+
+
 # -------------------------------------------------------------------- merge --
 def cp_lse_merge(o_parts, lse_parts, *, dst_rows=None, out=None, lse_out=None, out_fp32=True,
                  num_out_rows=None, status=None, stream=None):
@@ -201,8 +260,12 @@ def cp_restore(src, idx, *, out=None, status=None, stream=None):
 
 # --------------------------------------------------------------- pipelines --
 def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream=None,
-                         q_is_cat=False, workspace=None):
+                         q_is_cat=False, workspace=None, fuse_restore=False):
     """Full-KV prefill CP on one GPU: shard rows -> attention -> restore.
+
+    ``fuse_restore``: the attention store writes original order directly
+    (cp_attn_partial_restore with the plan's gather index) instead of a
+    separate cp_restore pass over O and LSE.
 
     q: bf16 [N, Hq, d] in original (flat) order, or already in cat order when
     ``q_is_cat``.  Returns (O [N, Hq, dv] bf16, LSE [N, Hq] fp32) in original order.
@@ -212,6 +275,12 @@ def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream
     ws = workspace or {}
     q_cat = q if q_is_cat else cp_restore(q, plan.gather_idx[:N], out=ws.get("q_cat"),
                                           status=status, stream=stream)
+    if fuse_restore:
+        return cp_attn_partial_restore(plan.segs, q_cat, k, v, scale, plan.gather_idx,
+                                       num_out_rows=N, num_segs=plan.total_segs,
+                                       tiles=plan.tiles, num_tiles=plan.total_tiles,
+                                       out=ws.get("o"), lse=ws.get("lse"), status=status,
+                                       stream=stream)
     o_cat, lse_cat = cp_attn_partial(plan.segs, q_cat, k, v, scale, num_segs=plan.total_segs,
                                      tiles=plan.tiles, num_tiles=plan.total_tiles,
                                      out=ws.get("o_cat"), lse=ws.get("lse_cat"),
@@ -325,3 +394,75 @@ def cp_partial_kv_attention(q_cat, k, v, plan: ShardPlan, scale, kv_block, *, se
         cp_lse_merge(o_parts, l_parts, dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql],
                      out=out, lse_out=lse_out, num_out_rows=N, status=status, stream=stream)
     return out, lse_out
+
+
+def pass_q_kv_blocks(kv_total: int, cp_size: int):
+    """Resident KV shards of the pass-Q ring for one request.
+
+    The request's KV positions 0..kv_total-1 are cut into 2C near-equal blocks
+    (the remainder to the first blocks, as for the zigzag query split) and
+    rank r keeps blocks r and 2C-1-r.  Returns, per rank, its two (lo, hi)
+    position ranges.
+    """
+    nb = 2 * cp_size
+    base, rem = divmod(int(kv_total), nb)
+    starts = [0]
+    for i in range(nb):
+        starts.append(starts[-1] + base + (1 if i < rem else 0))
+    return [[(starts[r], starts[r + 1]), (starts[nb - 1 - r], starts[nb - r])]
+            for r in range(cp_size)]
+
+
+def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, segs_host=None, status=None,
+                        stream=None):
+    """Pass-Q ring CP on one GPU, hop by hop.
+
+    KV stays resident: rank r holds the KV blocks of pass_q_kv_blocks.  Each
+    rank's query shard travels round the ring with an fp32 accumulator
+    (O_acc, L_acc) that starts empty (0, -inf); at hop s rank r merges the
+    partial of the visiting shard (of rank (r - s) mod C) against its own KV
+    blocks into that accumulator (one cp_attn_partial_accumulate per request
+    and block).  After C hops every accumulator is the exact result.
+    Returns (O fp32 [N, Hq, dv], LSE [N, Hq]) in cat order.
+    """
+    C = plan.cp_size
+    N, Hq, _ = q_cat.shape
+    dv = v.shape[2]
+    dev = q_cat.device
+    segs_host = segs_host or segments_host(plan)
+    new_lens = plan.new_lens_dev.cpu().tolist()[: plan.num_reqs]
+    prefix_lens = plan.prefix_lens_dev.cpu().tolist()[: plan.num_reqs]
+    blocks = [pass_q_kv_blocks(p + n, C) for n, p in zip(new_lens, prefix_lens)]
+    first = [0]
+    for c in plan.segs_per_rank:
+        first.append(first[-1] + c)
+    # each rank's segments grouped by request: (req, seg_begin, seg_end, last position)
+    groups = []
+    for qr in range(C):
+        g = []
+        for i in range(first[qr], first[qr + 1]):
+            sg = segs_host[i]
+            last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
+            if g and g[-1][0] == sg["req"]:
+                g[-1][2] = i + 1
+                g[-1][3] = max(g[-1][3], last)
+            else:
+                g.append([sg["req"], i, i + 1, last])
+        groups.append(g)
+    o_acc = torch.zeros((max(N, 1), Hq, dv), dtype=torch.float32, device=dev)
+    lse_a = torch.full((max(N, 1), Hq), float("-inf"), dtype=torch.float32, device=dev)
+    lse_b = lse_a.clone()
+    with torch.cuda.stream(stream):  # the LSE copies run on the launches' stream
+        for hop in range(C):
+            for r in range(C):
+                qr = (r - hop) % C
+                for req, i0, i1, last in groups[qr]:
+                    for lo, hi in blocks[req][r]:
+                        if hi <= lo or lo > last:
+                            continue  # no row of the visiting shard sees this block
+                        cp_attn_partial_accumulate(plan.segs[i0:i1], q_cat, k, v, scale, o_acc,
+                                                   lse_a, lse_b, kv_lo=lo, kv_hi=hi,
+                                                   status=status, stream=stream)
+                        # keep the two LSE buffers equal between calls
+                        lse_a.copy_(lse_b)
+    return o_acc[:N], lse_a[:N]

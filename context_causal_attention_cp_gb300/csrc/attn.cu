@@ -283,6 +283,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
     const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
+    const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_col = s * BN, o_col = NQ * BN + s * DV;
     const float sl2 = p.scale_log2;
@@ -372,42 +373,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else {
       tc_fence_after();
       const int h = head0 + s;
-      const long long out_row = out_row0 + r0 + row;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
-#pragma unroll
-      for (int q = 0; q < DV / 32; ++q) {
-        uint32_t r[32];
-        if (n_kv > 0) {
-          tmem_ld32(lane_addr + o_col + q * 32, r);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = 0u;
-        }
-        if (valid) {
-          float v[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * inv;
-          const long long off = (out_row * p.Hq + h) * DV + q * 32;
-          if (p.o_f32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      MergeCoef mc{0.f, inv, has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY};
+      if (p.lse_acc) {
+        // accumulate mode (fp32 O): merge into the partial already stored
+        if (out_row >= 0) mc = merge_coef(__ldg(p.lse_acc + out_row * p.Hq + h), has, m_use, l_run);
+#pragma unroll 1
+        for (int q = 0; q < DV / 32; ++q) {
+          uint32_t r[32];
+          if (n_kv > 0) {
+            tmem_ld32(lane_addr + o_col + q * 32, r);
+            tmem_wait_ld();
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
-                                  pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                                  pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                                  pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+            for (int c = 0; c < 32; ++c) r[c] = 0u;
+          }
+          if (out_row >= 0) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) +
+                                                    (out_row * p.Hq + h) * DV + q * 32);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float4 a = dst[c];
+              dst[c] = make_float4(mc.c_old * a.x + mc.c_new * __uint_as_float(r[4 * c]),
+                                   mc.c_old * a.y + mc.c_new * __uint_as_float(r[4 * c + 1]),
+                                   mc.c_old * a.z + mc.c_new * __uint_as_float(r[4 * c + 2]),
+                                   mc.c_old * a.w + mc.c_new * __uint_as_float(r[4 * c + 3]));
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < DV / 32; ++q) {
+          uint32_t r[32];
+          if (n_kv > 0) {
+            tmem_ld32(lane_addr + o_col + q * 32, r);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = 0u;
+          }
+          if (out_row >= 0) {
+            float v[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * inv;
+            const long long off = (out_row * p.Hq + h) * DV + q * 32;
+            if (p.o_f32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                    pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                    pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                    pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+            }
           }
         }
       }
-      if (valid)
-        p.lse[out_row * p.Hq + h] = has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      if (out_row >= 0) p.lse[out_row * p.Hq + h] = mc.lse;
     }
   }
 
@@ -553,6 +581,67 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
   prm.o = o;
   prm.o_f32 = o_is_fp32 ? 1 : 0;
   prm.lse = lse;
+  prm.out_row_base = out_row_base;
+  prm.num_out_rows = num_out_rows;
+  prm.status = status_dev;
+  prm.split_block = 0;
+  return attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
+                     k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
+                     scale, prm, stream);
+}
+
+extern "C" int cp_attn_partial_restore(
+    const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
+    const void* q, int num_q_rows, const void* k, int64_t k_row_stride, int64_t k_head_stride,
+    const void* v, int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
+    int d, int dv, float scale, int kv_lo, int kv_hi, const int32_t* dst_rows, void* o,
+    int o_is_fp32, float* lse, int num_out_rows, int32_t* status_dev, cudaStream_t stream) {
+  if (num_out_rows < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_segs > 0 && (!o || !lse || !dst_rows || num_out_rows == 0))
+    return CPATTN_ERR_INVALID_ARG;
+  if (o && (!a16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))) return CPATTN_ERR_ALIGNMENT;
+  AttnParams prm{};
+  prm.kv_lo = kv_lo;
+  prm.kv_hi = kv_hi;
+  prm.o = o;
+  prm.o_f32 = o_is_fp32 ? 1 : 0;
+  prm.lse = lse;
+  prm.out_row_base = 0;
+  prm.num_out_rows = num_q_rows;  // segment rows are checked against the query rows
+  prm.dst_rows = dst_rows;
+  prm.dst_limit = num_out_rows;
+  prm.status = status_dev;
+  prm.split_block = 0;
+  return attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
+                     k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
+                     scale, prm, stream);
+}
+
+extern "C" int cp_attn_partial_accumulate(
+    const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
+    const void* q, int num_q_rows, const void* k, int64_t k_row_stride, int64_t k_head_stride,
+    const void* v, int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
+    int d, int dv, float scale, int kv_lo, int kv_hi, float* o_acc, const float* lse_acc,
+    float* lse_out, int out_row_base, int num_out_rows, int32_t* status_dev, cudaStream_t stream) {
+  if (num_out_rows < 0 || Hq <= 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_segs > 0 && (!o_acc || !lse_acc || !lse_out || num_out_rows == 0))
+    return CPATTN_ERR_INVALID_ARG;
+  if (o_acc && (!a16(o_acc) || (reinterpret_cast<uintptr_t>(lse_acc) & 3u) ||
+                (reinterpret_cast<uintptr_t>(lse_out) & 3u)))
+    return CPATTN_ERR_ALIGNMENT;
+  if (lse_acc && lse_out) {
+    // both LSE buffers span num_out_rows * Hq floats and must not overlap
+    const uintptr_t a = reinterpret_cast<uintptr_t>(lse_acc), b = reinterpret_cast<uintptr_t>(lse_out);
+    const uintptr_t n = (uintptr_t)num_out_rows * (uintptr_t)Hq * sizeof(float);
+    if (a < b + n && b < a + n) return CPATTN_ERR_INVALID_ARG;
+  }
+  AttnParams prm{};
+  prm.kv_lo = kv_lo;
+  prm.kv_hi = kv_hi;
+  prm.o = o_acc;
+  prm.o_f32 = 1;
+  prm.lse = lse_out;
+  prm.lse_acc = lse_acc;
   prm.out_row_base = out_row_base;
   prm.num_out_rows = num_out_rows;
   prm.status = status_dev;

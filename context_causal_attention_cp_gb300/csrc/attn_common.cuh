@@ -40,6 +40,17 @@ struct AttnParams {
   const long long* ws_slot;
   long long ws_rows;  // capacity of the partial buffers, rows
   const void* q;      // query rows (read directly by kernels that stage part of Q in TMEM)
+  // Output placement and mode of the normal (non-split) path:
+  //   dst_rows: when set, query row i writes output row dst_rows[i] (the
+  //     restore scatter done by the store), which must lie in [0, dst_limit);
+  //     then out_row_base = 0 and num_out_rows = num_q_rows.  Otherwise row i
+  //     writes row i - out_row_base.
+  //   lse_acc: when set, the store merges this call's partial into the fp32 O
+  //     already at the output row, whose LSE is lse_acc[row], by the pairwise
+  //     log-sum-exp rule: merged O in place, merged LSE to lse.
+  const int32_t* dst_rows;
+  long long dst_limit;
+  const float* lse_acc;
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).
@@ -189,6 +200,47 @@ __device__ __forceinline__ bool split_window(const AttnParams& p, const cp_segme
     return false;
   }
   return true;
+}
+
+// Output row of row `row` of query tile r0 of segment sg (normal mode), or -1
+// with CPATTN_ERR_RANGE when the destination index is out of range.
+__device__ __forceinline__ long long output_row(const AttnParams& p, const cp_segment_t& sg,
+                                                int r0, int row, long long out_row0) {
+  if (!p.dst_rows) return out_row0 + r0 + row;
+  const long long d = __ldg(p.dst_rows + sg.q_row0 + r0 + row);
+  if (d < 0 || d >= p.dst_limit) {
+    set_status(p.status, CPATTN_ERR_RANGE);
+    return -1;
+  }
+  return d;
+}
+
+// Pairwise log-sum-exp merge of the store in accumulate mode.  This call's
+// partial for a row is (acc / l_run, n) with n = m_use + log2(l_run) in log2
+// units (no visible key: n = -inf); the accumulator holds (O_old, L_old) with
+// L_old a natural log.  With m = max, w_old = 2^(L_old*log2e - m) and
+// w_new = 2^(n - m): O = (w_old O_old + w_new acc / l_run) / (w_old + w_new),
+// L = (m + log2(w_old + w_new)) ln 2.  Both sides empty: O = 0, L = -inf.
+struct MergeCoef {
+  float c_old, c_new, lse;  // O = c_old * O_old + c_new * acc
+};
+__device__ __forceinline__ MergeCoef merge_coef(float l_old, bool has, float m_use, float l_run) {
+  const float n2 = has ? m_use + lg2_approx(l_run) : -INFINITY;
+  const float o2 = l_old * kLog2e;
+  const float m = fmaxf(n2, o2);
+  MergeCoef c;
+  if (m == -INFINITY) {
+    c.c_old = 0.f;
+    c.c_new = 0.f;
+    c.lse = -INFINITY;
+    return c;
+  }
+  const float wo = ex2_approx(o2 - m), wn = ex2_approx(n2 - m);
+  const float iw = 1.f / (wo + wn);
+  c.c_old = wo * iw;
+  c.c_new = has ? wn * iw * (1.f / l_run) : 0.f;
+  c.lse = (m + lg2_approx(wo + wn)) * kLn2;
+  return c;
 }
 
 // ------------------------------------------------------------------- host --

@@ -255,6 +255,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
     const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
+    const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
@@ -364,9 +365,12 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else {
       tc_fence_after();
-      const long long out_row = out_row0 + r0 + row;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
+      const bool acc_mode = p.lse_acc != nullptr;
+      MergeCoef mc{0.f, inv, has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY};
+      if (acc_mode && out_row >= 0)
+        mc = merge_coef(__ldg(p.lse_acc + out_row * p.Hq + h), has, m_use, l_run);
 #pragma unroll 1
       for (int q = 0; q < kDVH / 32; ++q) {
         uint32_t r[32];
@@ -377,29 +381,40 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int c = 0; c < 32; ++c) r[c] = 0u;
         }
-        if (valid) {
+        if (out_row >= 0) {
           const long long off = (out_row * p.Hq + h) * kDV + half * kDVH + q * 32;
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * mc.c_new;
           if (p.o_f32) {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
+            if (acc_mode) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float4 a = dst[c];
+                v[4 * c] += mc.c_old * a.x;
+                v[4 * c + 1] += mc.c_old * a.y;
+                v[4 * c + 2] += mc.c_old * a.z;
+                v[4 * c + 3] += mc.c_old * a.w;
+              }
+            }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              dst[c] = make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
-                                   __uint_as_float(r[4 * c + 2]) * inv,
-                                   __uint_as_float(r[4 * c + 3]) * inv);
+              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(
-                  pack_bf16x2(__uint_as_float(r[8 * c]) * inv, __uint_as_float(r[8 * c + 1]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv));
+              dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                  pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                  pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                  pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
           }
         }
       }
-      if (valid && half == 0)
-        p.lse[out_row * p.Hq + h] = has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY;
+      // both halves read lse_acc; only half 0 writes the LSE (the accumulate
+      // entry point requires lse_acc and lse not to overlap)
+      if (out_row >= 0 && half == 0) p.lse[out_row * p.Hq + h] = mc.lse;
     }
   }
 

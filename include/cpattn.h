@@ -16,6 +16,9 @@
  *             (all-gather KV; restore index after the all-gather)
  *   [CPB-3.3] same blog, sections 3.1 and 3.3 (per-shard partial O_j and LSE L_j)
  *   [CPB-3.6] same blog, section 3.6 (merging partials: online-softmax / LSE rule)
+ *   [CPB-PQ]  same blog, section 3.3.2 "Pass Q" (ring pass-Q: the query block
+ *             carries a partial accumulator (O_acc, L_acc) from rank to rank
+ *             and every hop merges its local partial into it)
  *
  * Conventions for every call:
  *   - Return value: CPATTN_OK (0) or a negative CPATTN_ERR_* code.  Argument
@@ -160,6 +163,56 @@ int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* t
                     int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
                     int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
                     int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* cp_attn_partial with the restore fused into the store.  [CPB-2.1] (the
+ * restore index after the all-gather), [SGL-BE]
+ *
+ * Same computation and arguments as cp_attn_partial, except that the output
+ * row of query (cat) row i is dst_rows[i] instead of i - out_row_base.  With
+ * dst_rows = the plan's gather index (cat row -> flat index) the shard outputs
+ * land directly in causal token order, so no cp_restore pass is needed.
+ *   dst_rows: device int32 [num_q_rows]; every entry used must lie in
+ *     [0, num_out_rows) (an entry outside sets CPATTN_ERR_RANGE and that row
+ *     is not written).  Rows are written once each if dst_rows is injective on
+ *     the segments' rows; otherwise the last writer wins (unspecified).
+ *   o: [num_out_rows, Hq, dv] bf16 or fp32; lse: fp32 [num_out_rows, Hq]. */
+int cp_attn_partial_restore(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                            int num_tiles, const void* q, int num_q_rows, const void* k,
+                            int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                            int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                            int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi,
+                            const int32_t* dst_rows, void* o, int o_is_fp32, float* lse,
+                            int num_out_rows, int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* One pass-Q hop: cp_attn_partial whose store merges the new partial into a
+ * running accumulator.  [CPB-PQ], [CPB-3.6]
+ *
+ * For every segment row (output row R = cat row - out_row_base) and head h,
+ * with (O_new, L_new) = cp_attn_partial's result for the key window
+ * [kv_lo, kv_hi) and (O_acc, L_acc) = o_acc[R, h, :], lse_acc[R, h]:
+ *     m = max(L_acc, L_new);  w_a = exp(L_acc - m);  w_n = exp(L_new - m)
+ *     o_acc[R, h, :]  <- (w_a O_acc + w_n O_new) / (w_a + w_n)
+ *     lse_out[R, h]   <- m + ln(w_a + w_n)
+ * and both empty (L = -inf) gives O = 0, L = -inf.  An accumulator that starts
+ * at O = 0, L = -inf (the identity) and goes through hops whose windows
+ * partition the keys ends equal to cp_attn_partial over all keys.
+ *   Arguments shared with cp_attn_partial keep its meaning.
+ *   o_acc: fp32 [num_out_rows, Hq, dv], read and overwritten in place.
+ *   lse_acc: fp32 [num_out_rows, Hq] read; lse_out: fp32 [num_out_rows, Hq]
+ *     written.  The two must not overlap (CPATTN_ERR_INVALID_ARG): a hop
+ *     reads the old LSE of a row from more than one thread block (the MLA
+ *     shape splits dv over two), so the caller alternates two LSE buffers.
+ *   Rows outside the segments are not touched. */
+int cp_attn_partial_accumulate(const cp_segment_t* segs_dev, int num_segs,
+                               const int32_t* tiles_dev, int num_tiles, const void* q,
+                               int num_q_rows, const void* k, int64_t k_row_stride,
+                               int64_t k_head_stride, const void* v, int64_t v_row_stride,
+                               int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
+                               int dv, float scale, int kv_lo, int kv_hi, float* o_acc,
+                               const float* lse_acc, float* lse_out, int out_row_base,
+                               int num_out_rows, int32_t* status_dev, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Partial-KV (ring-style) decomposition in one call.  [CPB-2.1] item 2,

@@ -25,6 +25,7 @@ def test_library_exports_every_declared_symbol():
     lib = L.load()
     names = header_functions()
     assert {"cp_shard_plan_sizes", "cp_shard_plan", "cp_attn_partial", "cp_lse_merge",
+            "cp_attn_partial_restore", "cp_attn_partial_accumulate",
             "cp_restore"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
@@ -101,6 +102,53 @@ def test_invalid_arguments_are_rejected_on_host():
     # misaligned pointers are refused before any launch
     assert lib.cp_restore(ctypes.c_void_p(0x1002), 4, ctypes.c_void_p(0x2000), 4, 32,
                           ctypes.c_void_p(0x3000), nul, nul) == L.ERR_ALIGNMENT
+
+
+def test_restore_and_accumulate_calls_validate_on_host():
+    """Argument checks of the fused-restore and pass-Q accumulate entry points
+    (every call fails validation before any launch; pointers are never used)."""
+    lib = L.load()
+    nul = None
+    fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    args = [fake[0], 1, nul, 0, fake[1], 128, fake[2], 1024, 128, fake[3], 1024, 128, 256]
+    o, lse, dst = fake[4], fake[5], fake[6]
+    # restore: the destination index is required, shapes checked as for cp_attn_partial
+    assert lib.cp_attn_partial_restore(*args, 8, 4, 128, 128, 0.1, 0, -1, nul, o, 0, lse, 128,
+                                       nul, nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial_restore(*args, 6, 4, 128, 128, 0.1, 0, -1, dst, o, 0, lse, 128,
+                                       nul, nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial_restore(*args, 8, 4, 96, 96, 0.1, 0, -1, dst, o, 0, lse, 128,
+                                       nul, nul) == L.ERR_UNSUPPORTED
+    assert lib.cp_attn_partial_restore(*args, 8, 4, 128, 128, 0.1, 0, -1, dst,
+                                       ctypes.c_void_p(0x40008), 0, lse, 128, nul,
+                                       nul) == L.ERR_ALIGNMENT
+    # accumulate: the two LSE buffers (128 rows x 8 heads x 4 B = 4096 B) must not overlap
+    la = 0x80000
+    for lb in (la, la + 16, la + 4092, la - 4092):
+        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, o,
+                                              ctypes.c_void_p(la), ctypes.c_void_p(lb), 0, 128,
+                                              nul, nul) == L.ERR_INVALID_ARG, hex(lb)
+    # adjacent buffers are fine (the call then fails on the unsupported shape)
+    for lb in (la + 4096, la - 4096):
+        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 96, 96, 0.1, 0, -1, o,
+                                              ctypes.c_void_p(la), ctypes.c_void_p(lb), 0, 128,
+                                              nul, nul) == L.ERR_UNSUPPORTED, hex(lb)
+    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, nul,
+                                          ctypes.c_void_p(la), ctypes.c_void_p(la + 8192), 0,
+                                          128, nul, nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1,
+                                          ctypes.c_void_p(0x40004), ctypes.c_void_p(la),
+                                          ctypes.c_void_p(la + 8192), 0, 128, nul,
+                                          nul) == L.ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("total", [0, 1, 5, 16, 333, 131072])
+@pytest.mark.parametrize("C", [1, 2, 4, 8])
+def test_pass_q_blocks_match_oracle(total, C):
+    """Host logic of the pass-Q ring: resident KV windows as the oracle's."""
+    from oracle import pipeline as opipe
+    assert api.pass_q_kv_blocks(total, C) == [[tuple(w) for w in ws]
+                                              for ws in opipe.resident_kv_windows(total, C)]
 
 
 def test_status_strings():

@@ -320,6 +320,38 @@ def test_sharded_pipeline_equals_dense(strategy, C):
     np.testing.assert_allclose(Lp, L_ref, atol=1e-12)
 
 
+def test_pass_q_resident_kv_matches_zigzag_example(golden):
+    """With no prefix, the resident KV blocks of the pass-Q ring are the zigzag
+    blocks of the page's CP=4 / 16-token example (rank r keeps blocks r and
+    2C-1-r)."""
+    g = golden("zigzag_cp4_16tokens.txt")
+    wins = opipe.resident_kv_windows(16, 4)
+    for r in range(4):
+        owned = sorted(t for lo, hi in wins[r] for t in range(lo, hi))
+        assert owned == [int(x) for x in g[f"rank {r}"]]
+
+
+@pytest.mark.parametrize("total", [0, 1, 7, 16, 37, 1000])
+@pytest.mark.parametrize("C", [1, 2, 3, 8])
+def test_pass_q_resident_kv_partitions_positions(total, C):
+    wins = opipe.resident_kv_windows(total, C)
+    cover = sorted(t for r in range(C) for lo, hi in wins[r] for t in range(lo, hi))
+    assert cover == list(range(total))
+    sizes = [hi - lo for r in range(C) for lo, hi in wins[r]]
+    assert max(sizes) - min(sizes) <= 1
+
+
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+@pytest.mark.parametrize("C", [1, 2, 3, 4])
+def test_pass_q_ring_equals_dense(strategy, C):
+    """Blog §3.3.2: after C hops the carried accumulator is the exact output."""
+    new, pre, q, k, v = _tiny(60 + C, B=3, Hq=4, Hkv=2, d=6, dv=5)
+    O_ref, L_ref = oatt.dense_causal_attention(q, k, v, new, pre, 0.45)
+    O, L, _ = opipe.pass_q_attention(q, k, v, new, pre, C, strategy, 0.45)
+    np.testing.assert_allclose(O, O_ref, atol=1e-12)
+    np.testing.assert_allclose(L, L_ref, atol=1e-12)
+
+
 # ------------------------------------------------------ planted mistakes ----
 
 def test_planted_mistakes_are_caught(monkeypatch):
@@ -358,3 +390,28 @@ def test_planted_mistakes_are_caught(monkeypatch):
         return list(reversed(oplan.zigzag_block_sizes(n, C)))
     sizes = late_rem(13, 4)
     assert sizes != sorted(sizes, reverse=True)
+
+
+def test_planted_pass_q_mistakes_are_caught(monkeypatch):
+    """A ring that forgets a rank's second resident block, or merges with the
+    wrong weight, must break the pass-Q pin."""
+    new, pre, q, k, v = _tiny(63, B=3, Hq=4, Hkv=2, d=6, dv=5)
+    O_ref, L_ref = oatt.dense_causal_attention(q, k, v, new, pre, 0.45)
+    good = opipe.resident_kv_windows
+    monkeypatch.setattr(opipe, "resident_kv_windows", lambda t, c: [w[:1] for w in good(t, c)])
+    O, L, _ = opipe.pass_q_attention(q, k, v, new, pre, 3, "zigzag", 0.45)
+    assert not np.allclose(L, L_ref, atol=1e-6)
+    monkeypatch.setattr(opipe, "resident_kv_windows", good)
+
+    real_merge = opipe.lse_merge
+
+    def merge_without_max_weight(o_parts, l_parts):
+        # plain mean of the non-empty partials instead of the LSE weights
+        O, L = real_merge(o_parts, l_parts)
+        w = np.where(np.isneginf(l_parts), 0.0, 1.0)
+        n = np.maximum(w.sum(axis=0), 1.0)
+        return (w[..., None] * o_parts).sum(axis=0) / n[..., None], L
+
+    monkeypatch.setattr(opipe, "lse_merge", merge_without_max_weight)
+    O, L, _ = opipe.pass_q_attention(q, k, v, new, pre, 3, "zigzag", 0.45)
+    assert not np.allclose(O, O_ref, atol=1e-6)
