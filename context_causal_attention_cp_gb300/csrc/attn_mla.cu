@@ -48,6 +48,132 @@ constexpr int kSmemM = kBarOffM + kNumBarsM * 8 + 16 + 1024;
 static_assert(kSmemM <= 232448, "MLA tile exceeds shared memory");
 constexpr uint32_t kSCol = 0, kQtCol = 128, kOCol = 256;  // TMEM column map
 
+// Chunk c of a K tile is one of output half HALF's four V chunks iff
+// 4*HALF <= c < 4*HALF+4; the other five are the non-V chunks, numbered
+// 0..4 in increasing c.  Both lists are compile-time so that every MMA of a
+// tile is issued with immediate descriptor offsets.
+template <int HALF>
+__device__ __forceinline__ constexpr bool mla_is_v(int c) {
+  return c >= kVChunks * HALF && c < kVChunks * (HALF + 1);
+}
+template <int HALF>
+__device__ __forceinline__ constexpr int mla_n_slot(int c) {
+  return c < kVChunks * HALF ? c : c - kVChunks;
+}
+
+// Q K^T over chunk C of the tile whose non-V / V chunks start at descriptors
+// dn / dkv (this stage), into S at s_tm.
+template <int HALF, int C>
+__device__ __forceinline__ void mla_qk_chunk(uint32_t s_tm, uint32_t qt_base, uint64_t dq0,
+                                             uint64_t dn, uint64_t dkv, bool first) {
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, kBNm, 0, 0);
+  uint64_t kd;
+  if constexpr (mla_is_v<HALF>(C))
+    kd = dkv + (uint64_t)(((C - kVChunks * HALF) * kKChunkBytes) >> 4);
+  else
+    kd = dn + (uint64_t)((mla_n_slot<HALF>(C) * kKChunkBytes) >> 4);
+  if constexpr (C < kQSmemChunks) {
+    const uint64_t qd = dq0 + (uint64_t)((C * kQChunkBytes) >> 4);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
+  } else {
+    const uint32_t qt = qt_base + (C - kQSmemChunks) * 32;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ts(s_tm, qt + kk * 8, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
+  }
+}
+
+// Q K^T over the non-V chunks (PART 0) or the V chunks (PART 1) of a tile.
+template <int HALF, int PART, int C = 0>
+__device__ __forceinline__ void mla_qk_part(uint32_t s_tm, uint32_t qt_base, uint64_t dq0,
+                                            uint64_t dn, uint64_t dkv, bool first) {
+  if constexpr (C < kChunks) {
+    constexpr bool mine = (PART == 1) == mla_is_v<HALF>(C);
+    if constexpr (mine) mla_qk_chunk<HALF, C>(s_tm, qt_base, dq0, dn, dkv, first);
+    mla_qk_part<HALF, PART, C + 1>(s_tm, qt_base, dq0, dn, dkv, first && !mine);
+  }
+}
+
+// The MMA issuer of one CTA (one thread).  Per tile j: Q K_j^T on the non-V
+// chunks (their stage is released right after), then P_{j-1} V_{j-1} (frees
+// the V chunks of tile j-1), then Q K_j^T on the V chunks; the V reload of a
+// stage has a whole tile of MMAs to land.
+template <int HALF>
+__device__ __noinline__ void mla_mma_issue(const AttnParams& p, uint8_t* smem, uint32_t q_base,
+                                           uint32_t tmem_base, int n_kv, uint64_t* bars,
+                                           volatile int* abort_flag) {
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kDVH, 0, 1);
+  uint64_t* bar_q = bars;
+  uint64_t* qt_full = bars + 1;
+  uint64_t* n_full = bars + 2;
+  uint64_t* n_empty = bars + 4;
+  uint64_t* v_full = bars + 6;
+  uint64_t* v_empty = bars + 8;
+  uint64_t* s_full = bars + 10;
+  uint64_t* p_full = bars + 12;
+  uint64_t* o_ready = bars + 14;
+  uint64_t* o_full = bars + 15;
+  uint64_t* bar_drain = bars + 16;
+  const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
+  const uint64_t dn0 = smem_desc_sw128(smem_u32(smem + kNOff), 16, 1024);
+  const uint64_t dkv0 = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kVOff), kKChunkBytes, 1024);
+  constexpr uint64_t kNStage = (kNChunks * kKChunkBytes) >> 4;  // descriptor step per stage
+  constexpr uint64_t kVStage = (kVChunks * kKChunkBytes) >> 4;
+  const uint32_t qt_base = tmem_base + kQtCol;
+  auto pv = [&](int j) {
+    const uint32_t p_tm = tmem_base + kSCol + (j & 1) * kBNm;
+    const uint64_t vd = dv0 + (j & 1) * kVStage;
+#pragma unroll
+    for (int kk = 0; kk < kBNm / 16; ++kk)
+      mma_ts(tmem_base + kOCol, p_tm + kk * 8, vd + (uint64_t)(kk * ((16 * 128) >> 4)),
+             kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+  };
+  bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
+  if (ok) ok = mbar_wait(qt_full, 0, abort_flag, p.timeout_ns);
+  for (int j = 0; j < n_kv && ok; ++j) {
+    const int st = j & 1;
+    const uint32_t s_tm = tmem_base + kSCol + st * kBNm;
+    const uint64_t dn = dn0 + st * kNStage, dkv = dkv0 + st * kVStage;
+    ok = mbar_wait(n_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
+    if (!ok) break;
+    tc_fence_after();
+    mla_qk_part<HALF, 0>(s_tm, qt_base, dq0, dn, dkv, true);
+    mma_commit(n_empty + st);
+    if (j > 0) {
+      const int jp = j - 1;
+      ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
+      if (!ok) break;
+      tc_fence_after();
+      pv(jp);
+      mma_commit(o_ready);
+      mma_commit(v_empty + (jp & 1));
+    }
+    ok = mbar_wait(v_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
+    if (!ok) break;
+    tc_fence_after();
+    mla_qk_part<HALF, 1>(s_tm, qt_base, dq0, dn, dkv, false);
+    mma_commit(s_full + st);
+  }
+  if (ok) {
+    const int jp = n_kv - 1;
+    ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      pv(jp);
+      mma_commit(o_full);
+    }
+  }
+  if (!ok) {
+    set_status(p.status, CPATTN_ERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  mma_commit(bar_drain);
+  mbar_wait(bar_drain, 0, nullptr, p.timeout_ns);
+}
+
 __global__ void __launch_bounds__(kThreadsM, 1)
 attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const AttnParams p) {
@@ -166,88 +292,10 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else if (warp == 5) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, kBNm, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kDVH, 0, 1);
-      // descriptors built once; per MMA only a constant offset is added
-      const uint64_t dq0 = smem_desc_sw128(q_base, 16, 1024);
-      const uint64_t dn0 = smem_desc_sw128(smem_u32(smem + kNOff), 16, 1024);
-      const uint64_t dkv0 = smem_desc_sw128(smem_u32(smem + kVOff), 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kVOff), kKChunkBytes, 1024);
-      // Q K^T over chunk c of tile j (Q chunk from shared or tensor memory,
-      // K chunk from the ring that holds it)
-      auto qk_chunk = [&](int j, int c, bool first) {
-        const uint32_t s_tm = tmem_base + kSCol + (j & 1) * kBNm;
-        const int st = j & 1;
-        const uint64_t kd = is_v(c)
-            ? dkv0 + (uint64_t)(((st * kVChunks + c - kVChunks * half) * kKChunkBytes) >> 4)
-            : dn0 + (uint64_t)(((st * kNChunks + n_slot(c)) * kKChunkBytes) >> 4);
-        if (c < kQSmemChunks) {
-          const uint64_t qd = dq0 + (uint64_t)((c * kQChunkBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
-        } else {
-          const uint32_t qt = tmem_base + kQtCol + (c - kQSmemChunks) * 32;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(s_tm, qt + kk * 8, kd + kk * 2, kIdescQK, (first && kk == 0) ? 0u : 1u);
-        }
-      };
-      auto pv = [&](int j) {
-        const uint32_t p_tm = tmem_base + kSCol + (j & 1) * kBNm;
-        const uint64_t vd = dv0 + (uint64_t)((((j & 1) * kVChunks) * kKChunkBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kBNm / 16; ++kk)
-          mma_ts(tmem_base + kOCol, p_tm + kk * 8, vd + (uint64_t)(kk * ((16 * 128) >> 4)),
-                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      // Per tile j: Q K_j^T on the non-V chunks (released right after), then
-      // P_{j-1} V_{j-1} (frees the V chunks of tile j-1), then Q K_j^T on the
-      // V chunks; the V reload of a stage has a whole tile of MMAs to land.
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.timeout_ns);
-      if (ok) ok = mbar_wait(qt_full, 0, abort_flag, p.timeout_ns);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j & 1;
-        ok = mbar_wait(n_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-        bool first = true;
-        for (int c = 0; c < kChunks; ++c)
-          if (!is_v(c)) {
-            qk_chunk(j, c, first);
-            first = false;
-          }
-        mma_commit(n_empty + st);
-        if (j > 0) {
-          const int jp = j - 1;
-          ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
-          if (!ok) break;
-          tc_fence_after();
-          pv(jp);
-          mma_commit(o_ready);
-          mma_commit(v_empty + (jp & 1));
-        }
-        ok = mbar_wait(v_full + st, (j >> 1) & 1, abort_flag, p.timeout_ns);
-        if (!ok) break;
-        tc_fence_after();
-        for (int c = kVChunks * half; c < kVChunks * (half + 1); ++c) qk_chunk(j, c, false);
-        mma_commit(s_full + st);
-      }
-      if (ok) {
-        const int jp = n_kv - 1;
-        ok = mbar_wait(p_full + (jp & 1), (jp >> 1) & 1, abort_flag, p.timeout_ns);
-        if (ok) {
-          tc_fence_after();
-          pv(jp);
-          mma_commit(o_full);
-        }
-      }
-      if (!ok) {
-        set_status(p.status, CPATTN_ERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      mma_commit(bar_drain);
-      mbar_wait(bar_drain, 0, nullptr, p.timeout_ns);
+      if (half == 0)
+        mla_mma_issue<0>(p, smem, q_base, tmem_base, n_kv, bars, abort_flag);
+      else
+        mla_mma_issue<1>(p, smem, q_base, tmem_base, n_kv, bars, abort_flag);
     }
   } else {
     // ------------------------------------------------------------- softmax --
