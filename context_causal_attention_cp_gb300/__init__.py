@@ -20,6 +20,7 @@ from .api import (  # noqa: F401
     cp_pass_q_attention,
     cp_prefill_attention,
     cp_restore,
+    cp_select_pass,
     cp_shard_plan,
     cp_shard_plan_sizes,
     make_plan,

@@ -18,6 +18,10 @@ ERR_ALIGNMENT = -5
 ERR_RANGE = -6
 ERR_TOO_LARGE = -7
 NOALLOC_SCRATCH_BYTES = 64 << 20
+PASS_KV = 0
+PASS_Q = 1
+SELECT_MESSAGE = 0
+SELECT_FITTED = 1
 
 DEBUG_WAIT_LIMIT_NS = 1
 DEBUG_WITHHOLD_Q = 2
@@ -45,6 +49,8 @@ SIGNATURES = {
     "cp_attn_partial_accumulate": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
                                          i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
                                          vp, vp, i32, i32, vp, vp]),
+    "cp_select_pass": (i32, [ctypes.c_int64, ctypes.c_int64, i32, i32, i32,
+                             ctypes.POINTER(ctypes.c_double)]),
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
     "cp_partial_kv_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32,

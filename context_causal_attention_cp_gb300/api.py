@@ -466,3 +466,19 @@ def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, segs_host=None, 
                         # keep the two LSE buffers equal between calls
                         lse_a.copy_(lse_b)
     return o_acc[:N], lse_a[:N]
+
+
+def cp_select_pass(new_tokens: int, cached_tokens: int, Hq: int, Hkv: int, rule="message"):
+    """Pass-KV or pass-Q for a step (see cp_select_pass in cpattn.h).
+
+    rule: "message" (miss rate against 2*Hkv/Hq) or "fitted" (the fitted
+    heuristic h(T, P)).  Returns ("pass_kv" | "pass_q", score).
+    """
+    lib = L.load()
+    rules = {"message": L.SELECT_MESSAGE, "fitted": L.SELECT_FITTED}
+    score = ctypes.c_double()
+    r = lib.cp_select_pass(int(new_tokens), int(cached_tokens), int(Hq), int(Hkv), rules[rule],
+                           ctypes.byref(score))
+    if r < 0:
+        L.check(r, "cp_select_pass")
+    return ("pass_q" if r == L.PASS_Q else "pass_kv"), score.value

@@ -16,6 +16,8 @@
  *             (all-gather KV; restore index after the all-gather)
  *   [CPB-3.3] same blog, sections 3.1 and 3.3 (per-shard partial O_j and LSE L_j)
  *   [CPB-3.6] same blog, section 3.6 (merging partials: online-softmax / LSE rule)
+ *   [CPB-3.5] same blog, section 3.5, the pass-KV / pass-Q switch (miss-rate
+ *             rule and fitted heuristic)
  *   [CPB-PQ]  same blog, section 3.3.2 "Pass Q" (ring pass-Q: the query block
  *             carries a partial accumulator (O_acc, L_acc) from rank to rank
  *             and every hop merges its local partial into it)
@@ -213,6 +215,30 @@ int cp_attn_partial_accumulate(const cp_segment_t* segs_dev, int num_segs,
                                int dv, float scale, int kv_lo, int kv_hi, float* o_acc,
                                const float* lse_acc, float* lse_out, int out_row_base,
                                int num_out_rows, int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Pass-KV or pass-Q for one step.  [CPB-3.5]  Host only; no device work.
+ *
+ * new_tokens T > 0 (uncached tokens of the step), cached_tokens P >= 0
+ * (persistent KV length), both at most 2^40; Hq / Hkv query / KV heads
+ * (Hq % Hkv == 0, Hq <= 2^20).
+ *   rule CP_SELECT_MESSAGE: pass-Q iff the miss rate T/(T+P) <= 2*Hkv/Hq,
+ *     i.e. iff the query block (T x Hq heads) is no larger than the K and V
+ *     block (T+P rows x Hkv heads each) that pass-KV would send (decided
+ *     exactly in integers: T*Hq <= 2*(T+P)*Hkv); *score =
+ *     T/(T+P) - 2*Hkv/Hq (> 0: pass-KV).
+ *   rule CP_SELECT_FITTED: the blog's fitted heuristic
+ *     h(T,P) = -1.059 log T + 1.145 log(T/(T+P)) + 12.112, pass-KV iff h > 0,
+ *     read with natural logarithms of token counts (the page gives no base
+ *     or unit); *score = h.
+ *   score: nullable.
+ * Returns CP_PASS_KV or CP_PASS_Q, or CPATTN_ERR_INVALID_ARG. */
+#define CP_PASS_KV 0
+#define CP_PASS_Q 1
+#define CP_SELECT_MESSAGE 0
+#define CP_SELECT_FITTED 1
+int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, int rule,
+                   double* score);
 
 /* ------------------------------------------------------------------------ */
 /* Partial-KV (ring-style) decomposition in one call.  [CPB-2.1] item 2,

@@ -172,3 +172,23 @@ def test_partial_kv_workspace_matches_oracle_segments(seed, strategy):
     r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     expect = r256((2 * len(segs) + 2) * 8) + r256(rows * Hq * dv * 4) + r256(rows * Hq * 4) + 256
     assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv) == (expect, mb)
+
+
+def test_select_pass_matches_oracle():
+    """Host logic of cp_select_pass against the oracle on a grid, both rules."""
+    from oracle import select as osel
+    for Hq, Hkv in ((32, 8), (128, 8), (64, 64), (12, 1)):
+        for T in (1, 2, 3, 100, 1500, 16384, 131072):
+            for P in (0, 1, 5, 999, 16384, 114688, 10 ** 7):
+                got, score = api.cp_select_pass(T, P, Hq, Hkv, "message")
+                assert got == osel.select_by_messages(T, P, Hq, Hkv), (T, P, Hq, Hkv)
+                got, score = api.cp_select_pass(T, P, Hq, Hkv, "fitted")
+                assert got == osel.select_fitted(T, P)
+                assert score == pytest.approx(osel.fitted_score(T, P), rel=1e-12, abs=1e-12)
+
+
+def test_select_pass_rejects_bad_arguments():
+    lib = L.load()
+    for args in ((0, 5, 8, 8, 0), (5, -1, 8, 8, 0), (5, 5, 6, 4, 0), (5, 5, 8, 8, 2),
+                 (1 << 41, 0, 8, 8, 0)):
+        assert lib.cp_select_pass(*args, None) == L.ERR_INVALID_ARG

@@ -415,3 +415,39 @@ def test_planted_pass_q_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(opipe, "lse_merge", merge_without_max_weight)
     O, L, _ = opipe.pass_q_attention(q, k, v, new, pre, 3, "zigzag", 0.45)
     assert not np.allclose(O, O_ref, atol=1e-6)
+
+
+# ---------------------------------------------------- pass-KV / pass-Q ----
+
+def test_select_threshold_page_value(golden):
+    """§3.5: with N_h/N_kv = 16 the switch is at a miss rate of 12.5 %."""
+    from oracle import select as osel
+    g = golden("pass_switch_threshold.txt")
+    ratio = int(g["heads_ratio"][0])
+    thr = float(g["threshold_percent"][0]) / 100.0
+    Hkv = 8
+    Hq = ratio * Hkv
+    for total in (8, 1024, 131072):
+        T = int(total * thr)
+        assert T / total == thr
+        assert osel.select_by_messages(T, total - T, Hq, Hkv) == "pass_q"
+        assert osel.select_by_messages(T + 1, total - T - 1, Hq, Hkv) == "pass_kv"
+
+
+@pytest.mark.parametrize("ratio", [4, 8, 16])
+def test_select_page_statements(ratio):
+    """Decode (T = 1) picks pass-Q; full prefill (P = 0) picks pass-KV (GQA)."""
+    from oracle import select as osel
+    for P in (1000, 131071, 10 ** 6):
+        assert osel.select_by_messages(1, P, 8 * ratio, 8) == "pass_q"
+    for T in (1, 4096, 131072):
+        assert osel.select_by_messages(T, 0, 8 * ratio, 8) == "pass_kv"
+
+
+def test_select_fitted_reading():
+    """The fitted rule with natural logs: h is decreasing in T at fixed miss
+    rate, and pass-Q at decode over a long cache (page: decode uses pass-Q)."""
+    from oracle import select as osel
+    assert osel.select_fitted(1, 131071) == "pass_q"
+    assert osel.fitted_score(1000, 1000) > osel.fitted_score(2000, 2000)
+    assert osel.fitted_score(1, 0) == pytest.approx(12.112)
