@@ -5,13 +5,16 @@ Default workload: one 32768-token prompt, Llama-3-8B-shaped attention (32
 query / 8 KV heads, head dim 128), CP = 8 zigzag (16 blocks of 2048), bf16
 N(0,1) synthetic inputs.  One step is the whole hot path on the device:
 shard plan -> gather of each shard's query rows -> causal attention of all 8
-shards against the gathered KV in one launch -> restore of O and LSE to
-causal order.  ``value`` is causal attention TFLOP/s over the step
-(2*Hq*(d+dv) flops per visible (query, key) pair), L2 flushed between steps.
+shards against the gathered KV in one launch, whose store writes O and LSE
+straight to causal order (the restore fused through the plan's gather
+index).  ``value`` is causal attention TFLOP/s over the step (2*Hq*(d+dv)
+flops per visible (query, key) pair), L2 flushed between steps.
 
 The line also carries the LSE-merge GB/s of the 131072-token partial-KV
 decomposition (16 KV blocks of 8192, 136 visible fp32 partials merged and
-scattered to causal order), the restore GB/s, the attention kernel's
+scattered to causal order), that decomposition end to end as one call
+(pass-KV) and through the pass-Q ring, the GB/s of the standalone restore kernel (the
+two-pass path's cp_restore of O and LSE), the attention kernel's
 roofline, clocks under load, an end-to-end figure through the public API with
 host buffers, and the CPU oracle timed on a bounded sample of the same
 workload.
@@ -267,8 +270,6 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, device=dev)
     ws = {"q_cat": torch.empty_like(q),
-          "o_cat": torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev),
-          "lse_cat": torch.empty((N, Hq), dtype=torch.float32, device=dev),
           "o": torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev),
           "lse": torch.empty((N, Hq), dtype=torch.float32, device=dev)}
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -282,25 +283,21 @@ def run_ours(args):
                             stream=stream)
         if ev:
             ev[1].record(stream)
-        cpa.cp_attn_partial(plan.segs, qc, k, v, w.scale, num_segs=plan.total_segs,
-                            tiles=plan.tiles, num_tiles=plan.total_tiles, out=ws["o_cat"],
-                            lse=ws["lse_cat"], status=status, stream=stream)
+        # attention of every shard; the store puts O and LSE in causal order
+        cpa.cp_attn_partial_restore(plan.segs, qc, k, v, w.scale, plan.gather_idx,
+                                    num_out_rows=N, num_segs=plan.total_segs, tiles=plan.tiles,
+                                    num_tiles=plan.total_tiles, out=ws["o"], lse=ws["lse"],
+                                    status=status, stream=stream)
         if ev:
             ev[2].record(stream)
-        cpa.cp_restore(ws["o_cat"], plan.restore_idx[:N], out=ws["o"], status=status,
-                       stream=stream)
-        cpa.cp_restore(ws["lse_cat"], plan.restore_idx[:N], out=ws["lse"], status=status,
-                       stream=stream)
-        if ev:
-            ev[3].record(stream)
 
-    launches_per_step = 3 + 1 + 1 + 2   # plan (3 kernels), gather, attention, 2 restores
+    launches_per_step = 3 + 1 + 1   # plan (3 kernels), Q gather, attention (+ restore store)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     cpa.check_status(status, "warmup")
 
-    evs = [[E() for _ in range(4)] for _ in range(args.steps)]
+    evs = [[E() for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -314,17 +311,15 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     cpa.check_status(status, "timed steps")
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    rest_ms = [e[2].elapsed_time(e[3]) for e in evs]
     total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
     flops = attention_flops(w)
     value = job_throughput(flops, world, args.steps, total_ms)
     pk = peaks()
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = flops / (attn_avg_ms * 1e-3) / 1e12
-    restore_bytes = 2 * (N * Hq * dv * 2) + 2 * (N * Hq * 4)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -332,8 +327,7 @@ def run_ours(args):
             "data": "synthetic", "config": config_of(w, {"parallelism": f"replicas{world}"}),
             "wall_ms_per_step": t_wall * 1e3 / args.steps,
             "breakdown_ms": {"plan_and_q_gather": sum(prep_ms) / len(prep_ms),
-                             "attention": attn_avg_ms,
-                             "restore_o_lse": sum(rest_ms) / len(rest_ms)},
+                             "attention_with_restore_store": attn_avg_ms},
             "roofline": {"kernel": kernel_label(w),
                          "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
@@ -341,11 +335,10 @@ def run_ours(args):
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "algorithmic_bytes": algorithmic_bytes(w),
                          "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
-            "restore": {"gbs": restore_bytes / (sum(rest_ms) / len(rest_ms) * 1e-3) / 1e9,
-                        "bytes_per_step": restore_bytes},
+            "restore": bench_restore(args, w, plan, ws, flush, dev, stream, pk, status),
             "clocks": clk.summary(),
             "gpu_launches": launches_per_step * args.steps}
-    line["restore"]["frac_of_hbm"] = line["restore"]["gbs"] / pk["hbm_gbs"]
+    line["gpu_launches"] += line["restore"].pop("launches")
 
     if not args.skip_merge:
         line["merge"] = bench_merge(args, dev, stream, pk)
@@ -353,6 +346,8 @@ def run_ours(args):
     if not args.skip_merge:
         line["partial_kv"] = bench_partial_kv(args, dev, stream, pk)
         line["gpu_launches"] += line["partial_kv"].pop("launches")
+        line["pass_q"] = bench_pass_q(args, dev, stream, pk)
+        line["gpu_launches"] += line["pass_q"].pop("launches")
     if not args.skip_e2e:
         line["e2e"] = bench_e2e(args, w, inputs, dev, stream)
     del q, k, v, ws, flush
@@ -369,6 +364,44 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_restore(args, w, plan, ws, flush, dev, stream, pk, status):
+    """The standalone restore kernel (cp_restore of O and LSE, the two-pass
+    path), on the step's outputs taken in cat order; L2 flushed between reps."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    o_cat = ws["o"]          # any [N, Hq, dv] rows will do: the kernel is a row gather
+    lse_cat = ws["lse"]
+    o = torch.empty_like(o_cat)
+    lse = torch.empty_like(lse_cat)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def run():
+        cpa.cp_restore(o_cat, plan.restore_idx[:N], out=o, status=status, stream=stream)
+        cpa.cp_restore(lse_cat, plan.restore_idx[:N], out=lse, status=status, stream=stream)
+
+    for _ in range(3):
+        run()
+    reps = max(3, args.steps // 2)
+    evs = [(E(), E()) for _ in range(reps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, "restore")
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    nbytes = 2 * (N * Hq * dv * 2) + 2 * (N * Hq * 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_per_call": nbytes,
+            "ms": ms, "launches": 2 * (3 + reps),
+            "path": "cp_restore of O then LSE (the step itself fuses the restore into the "
+                    "attention store)"}
 
 
 def bench_merge(args, dev, stream, pk):
@@ -483,6 +516,71 @@ def bench_partial_kv(args, dev, stream, pk):
                     "split-KV attention, merge + restore)"}
 
 
+def bench_pass_q(args, dev, stream, pk):
+    """The same 128K workload through the pass-Q ring (KV resident in 2C
+    blocks per rank, each query shard carried round the ring with an fp32
+    accumulator, one accumulate launch per (hop, rank, KV block)); the
+    pass-KV figure is the partial_kv entry.  Step = plan + query gather + the
+    ring + restore of O and LSE to causal order."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    torch.cuda.empty_cache()
+    w = W.WORKLOADS[MERGE_WORKLOAD]
+    inputs = W.make_inputs(w)
+    q = inputs["q"].to(dev)
+    k = inputs["k"].to(dev)
+    v = inputs["v"].to(dev)
+    del inputs
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    status = cpa.new_status(dev)
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
+                         status=status)
+    sched = cpa.pass_q_schedule(plan)
+    q_cat = torch.empty_like(q)
+    acc = (torch.empty((N, Hq, dv), dtype=torch.float32, device=dev),
+           torch.empty((N, Hq), dtype=torch.float32, device=dev),
+           torch.empty((N, Hq), dtype=torch.float32, device=dev))
+    o = torch.empty((N, Hq, dv), dtype=torch.float32, device=dev)
+    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+
+    def step():
+        cpa.cp_shard_plan(plan, status=status, stream=stream)
+        cpa.cp_restore(q, plan.gather_idx[:N], out=q_cat, status=status, stream=stream)
+        o_cat, l_cat = cpa.cp_pass_q_attention(q_cat, k, v, plan, w.scale, schedule=sched,
+                                               status=status, stream=stream, out=acc)
+        cpa.cp_restore(o_cat, plan.restore_idx[:N], out=o, status=status, stream=stream)
+        cpa.cp_restore(l_cat, plan.restore_idx[:N], out=lse, status=status, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    reps = 3
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    cpa.check_status(status, "pass q")
+    ms = sorted(times)[len(times) // 2]
+    tf = attention_flops(w) / (ms * 1e-3) / 1e12
+    choice, score = cpa.cp_select_pass(N, 0, Hq, w.Hkv, "message")
+    del q, k, v, q_cat, acc, o, lse
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: {w.description}", "ms_per_step": ms, "tflops": tf,
+            "frac_of_bf16_peak": tf / pk["bf16_tflops"], "accumulate_launches": len(sched),
+            "launches": (3 + 1 + len(sched) + 2) * (reps + 3),
+            "selector_message_rule": choice,
+            "path": "cp_shard_plan + cp_restore + cp_pass_q_attention (one "
+                    "cp_attn_partial_accumulate per hop, rank and resident KV block) + "
+                    "cp_restore of O and LSE"}
+
+
 def bench_e2e(args, w, inputs, dev, stream):
     """Same step through the public API with pinned host inputs and outputs."""
     import torch
@@ -506,7 +604,8 @@ def bench_e2e(args, w, inputs, dev, stream):
         k.copy_(hk, non_blocking=True)
         vv = k[:, :, : w.dv] if v is None else v.copy_(hv, non_blocking=True)
         cpa.cp_shard_plan(plan, status=status, stream=stream)
-        o, lse = cpa.cp_prefill_attention(q, k, vv, plan, w.scale, status=status, stream=stream)
+        o, lse = cpa.cp_prefill_attention(q, k, vv, plan, w.scale, status=status, stream=stream,
+                                          fuse_restore=True)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -526,13 +625,15 @@ def bench_e2e(args, w, inputs, dev, stream):
     d2h = ho.numel() * 2 + hl.numel() * 4
     return {"value": attention_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "path": "cp_prefill_attention via the C ABI, pinned host q/k/v in, O and LSE out"}
+            "path": "cp_prefill_attention (restore fused into the attention store) via the C "
+                    "ABI, pinned host q/k/v in, O and LSE out"}
 
 
 def run_profile_case(args):
     """One kernel, small case, for ncu: 3 warm-up launches then one launch.
 
-    attention: the default workload's attention launch (all 8 shards).
+    attention: the default workload's attention launch (all 8 shards, restore
+               fused into the store, as in the bench step).
     merge:     the heaviest query block of the 128K partial-KV workload
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
     restore:   the O restore of the default workload (268 MB each way)."""
@@ -564,9 +665,10 @@ def run_profile_case(args):
         o, l = cpa.cp_attn_partial(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
                                    tiles=plan.tiles, num_tiles=plan.total_tiles)
         if args.profile_case == "attention":
-            run = lambda: cpa.cp_attn_partial(  # noqa: E731
-                plan.segs, q, k, v, w.scale, num_segs=plan.total_segs, tiles=plan.tiles,
-                num_tiles=plan.total_tiles, out=o, lse=l, status=status)
+            run = lambda: cpa.cp_attn_partial_restore(  # noqa: E731
+                plan.segs, q, k, v, w.scale, plan.gather_idx, num_out_rows=w.total_new,
+                num_segs=plan.total_segs, tiles=plan.tiles, num_tiles=plan.total_tiles, out=o,
+                lse=l, status=status)
         else:
             out = torch.empty_like(o)
             run = lambda: cpa.cp_restore(o, plan.restore_idx[: w.total_new], out=out,  # noqa: E731

@@ -26,5 +26,6 @@ from .api import (  # noqa: F401
     make_plan,
     new_status,
     pass_q_kv_blocks,
+    pass_q_schedule,
     segments_host,
 )

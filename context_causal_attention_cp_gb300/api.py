@@ -413,22 +413,17 @@ def pass_q_kv_blocks(kv_total: int, cp_size: int):
             for r in range(cp_size)]
 
 
-def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, segs_host=None, status=None,
-                        stream=None):
-    """Pass-Q ring CP on one GPU, hop by hop.
+def pass_q_schedule(plan: ShardPlan, segs_host=None):
+    """Host schedule of the pass-Q ring: one entry per accumulate call.
 
-    KV stays resident: rank r holds the KV blocks of pass_q_kv_blocks.  Each
-    rank's query shard travels round the ring with an fp32 accumulator
-    (O_acc, L_acc) that starts empty (0, -inf); at hop s rank r merges the
-    partial of the visiting shard (of rank (r - s) mod C) against its own KV
-    blocks into that accumulator (one cp_attn_partial_accumulate per request
-    and block).  After C hops every accumulator is the exact result.
-    Returns (O fp32 [N, Hq, dv], LSE [N, Hq]) in cat order.
+    Entry (hop, rank, seg_begin, seg_end, lo, hi, row_begin, row_end): at
+    ring hop ``hop`` rank ``rank`` merges the visiting query shard's segments
+    [seg_begin, seg_end) (one request's segments of the shard of rank
+    (rank - hop) mod C, cat rows [row_begin, row_end)) against its resident
+    KV block [lo, hi) (key positions, see pass_q_kv_blocks).  Blocks that no
+    row of the visiting segments can see are left out.
     """
     C = plan.cp_size
-    N, Hq, _ = q_cat.shape
-    dv = v.shape[2]
-    dev = q_cat.device
     segs_host = segs_host or segments_host(plan)
     new_lens = plan.new_lens_dev.cpu().tolist()[: plan.num_reqs]
     prefix_lens = plan.prefix_lens_dev.cpu().tolist()[: plan.num_reqs]
@@ -436,35 +431,61 @@ def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, segs_host=None, 
     first = [0]
     for c in plan.segs_per_rank:
         first.append(first[-1] + c)
-    # each rank's segments grouped by request: (req, seg_begin, seg_end, last position)
-    groups = []
+    groups = []   # per rank: [req, seg_begin, seg_end, last position, row_begin, row_end]
     for qr in range(C):
         g = []
         for i in range(first[qr], first[qr + 1]):
             sg = segs_host[i]
             last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
+            end = sg["q_row0"] + sg["q_len"]
             if g and g[-1][0] == sg["req"]:
                 g[-1][2] = i + 1
                 g[-1][3] = max(g[-1][3], last)
+                g[-1][5] = end
             else:
-                g.append([sg["req"], i, i + 1, last])
+                g.append([sg["req"], i, i + 1, last, sg["q_row0"], end])
         groups.append(g)
-    o_acc = torch.zeros((max(N, 1), Hq, dv), dtype=torch.float32, device=dev)
-    lse_a = torch.full((max(N, 1), Hq), float("-inf"), dtype=torch.float32, device=dev)
-    lse_b = lse_a.clone()
-    with torch.cuda.stream(stream):  # the LSE copies run on the launches' stream
-        for hop in range(C):
-            for r in range(C):
-                qr = (r - hop) % C
-                for req, i0, i1, last in groups[qr]:
-                    for lo, hi in blocks[req][r]:
-                        if hi <= lo or lo > last:
-                            continue  # no row of the visiting shard sees this block
-                        cp_attn_partial_accumulate(plan.segs[i0:i1], q_cat, k, v, scale, o_acc,
-                                                   lse_a, lse_b, kv_lo=lo, kv_hi=hi,
-                                                   status=status, stream=stream)
-                        # keep the two LSE buffers equal between calls
-                        lse_a.copy_(lse_b)
+    sched = []
+    for hop in range(C):
+        for r in range(C):
+            for req, i0, i1, last, r0, r1 in groups[(r - hop) % C]:
+                for lo, hi in blocks[req][r]:
+                    if hi > lo and lo <= last:
+                        sched.append((hop, r, i0, i1, lo, hi, r0, r1))
+    return sched
+
+
+def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, schedule=None, status=None,
+                        stream=None, out=None):
+    """Pass-Q ring CP on one GPU, hop by hop.
+
+    KV stays resident: rank r holds the KV blocks of pass_q_kv_blocks.  Each
+    rank's query shard travels round the ring with an fp32 accumulator
+    (O_acc, L_acc) that starts empty (0, -inf); at hop s rank r merges the
+    partial of the visiting shard (of rank (r - s) mod C) against its own KV
+    blocks into that accumulator (one cp_attn_partial_accumulate per entry of
+    pass_q_schedule).  After C hops every accumulator is the exact result.
+    ``out``: optional (O_acc fp32 [N, Hq, dv], LSE [N, Hq], LSE scratch [N, Hq]).
+    Returns (O fp32 [N, Hq, dv], LSE [N, Hq]) in cat order.
+    """
+    N, Hq, _ = q_cat.shape
+    dv = v.shape[2]
+    dev = q_cat.device
+    sched = pass_q_schedule(plan) if schedule is None else schedule
+    with torch.cuda.stream(stream):  # the fills and LSE copies run on the launches' stream
+        if out is None:
+            o_acc = torch.empty((max(N, 1), Hq, dv), dtype=torch.float32, device=dev)
+            lse_a = torch.empty((max(N, 1), Hq), dtype=torch.float32, device=dev)
+            lse_b = torch.empty_like(lse_a)
+        else:
+            o_acc, lse_a, lse_b = out
+        o_acc.zero_()
+        lse_a.fill_(float("-inf"))
+        lse_b.fill_(float("-inf"))
+        for _, _, i0, i1, lo, hi, r0, r1 in sched:
+            cp_attn_partial_accumulate(plan.segs[i0:i1], q_cat, k, v, scale, o_acc, lse_a, lse_b,
+                                       kv_lo=lo, kv_hi=hi, status=status, stream=stream)
+            lse_a[r0:r1].copy_(lse_b[r0:r1])  # the rows this call wrote; buffers stay equal
     return o_acc[:N], lse_a[:N]
 
 
