@@ -291,6 +291,82 @@ def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream
     return o, lse
 
 
+class PrefillPipeline:
+    """Full-KV CP prefill over a stream of same-shaped batches held in host memory.
+
+    Every ``submit`` copies one batch's q, k (and v) from pinned host memory,
+    runs plan -> query gather -> attention with the restore fused into its
+    store, and copies O and LSE back to pinned host memory.  Two device
+    buffer sets and three CUDA streams (upload, compute, download) let batch
+    n's attention overlap batch n+1's upload and batch n-1's download; events
+    order every reuse of a buffer set.  ``synchronize`` waits for all
+    submitted batches; host outputs of a batch are valid after it.
+    """
+
+    def __init__(self, new_lens, prefix_lens, cp_size, strategy, Hq, Hkv, d, dv, scale, *,
+                 v_is_k_prefix=False, device="cuda"):
+        dev = torch.device(device)
+        self.N = int(sum(new_lens))
+        kv_rows = int(sum(new_lens) + sum(prefix_lens))
+        self.scale = scale
+        self.dv = dv
+        self.v_is_k_prefix = v_is_k_prefix
+        self.plan = alloc_plan(new_lens, prefix_lens, cp_size, strategy, device=dev)
+        self.status = new_status(dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        self.bufs = []
+        for _ in range(2):
+            b = {"q": torch.empty((self.N, Hq, d), **bf), "k": torch.empty((kv_rows, Hkv, d), **bf),
+                 "q_cat": torch.empty((self.N, Hq, d), **bf),
+                 "o": torch.empty((self.N, Hq, dv), **bf),
+                 "lse": torch.empty((self.N, Hq), dtype=torch.float32, device=dev)}
+            b["v"] = None if v_is_k_prefix else torch.empty((kv_rows, Hkv, dv), **bf)
+            self.bufs.append(b)
+        self.s_up = torch.cuda.Stream(dev)
+        self.s_comp = torch.cuda.Stream(dev)
+        self.s_down = torch.cuda.Stream(dev)
+        self.ev_up = [torch.cuda.Event() for _ in range(2)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
+        self.ev_down = [torch.cuda.Event() for _ in range(2)]
+        self.n = 0
+
+    def submit(self, hq, hk, hv, ho, hlse):
+        """Queue one batch: host q, k, v (v ignored when it is a view of k) in,
+        host O [N, Hq, dv] bf16 and LSE [N, Hq] fp32 out (all pinned)."""
+        i = self.n % 2
+        b = self.bufs[i]
+        reuse = self.n >= 2
+        if reuse:
+            self.s_up.wait_event(self.ev_comp[i])     # batch n-2 is done reading set i
+        with torch.cuda.stream(self.s_up):
+            b["q"].copy_(hq, non_blocking=True)
+            b["k"].copy_(hk, non_blocking=True)
+            if b["v"] is not None:
+                b["v"].copy_(hv, non_blocking=True)
+            self.ev_up[i].record(self.s_up)
+        self.s_comp.wait_event(self.ev_up[i])
+        if reuse:
+            self.s_comp.wait_event(self.ev_down[i])   # batch n-2's outputs are downloaded
+        with torch.cuda.stream(self.s_comp):
+            v = b["k"][:, :, : self.dv] if b["v"] is None else b["v"]
+            cp_shard_plan(self.plan, status=self.status, stream=self.s_comp)
+            cp_prefill_attention(b["q"], b["k"], v, self.plan, self.scale, status=self.status,
+                                 stream=self.s_comp, fuse_restore=True,
+                                 workspace={"q_cat": b["q_cat"], "o": b["o"], "lse": b["lse"]})
+            self.ev_comp[i].record(self.s_comp)
+        self.s_down.wait_event(self.ev_comp[i])
+        with torch.cuda.stream(self.s_down):
+            ho.copy_(b["o"], non_blocking=True)
+            hlse.copy_(b["lse"], non_blocking=True)
+            self.ev_down[i].record(self.s_down)
+        self.n += 1
+
+    def synchronize(self):
+        for s in (self.s_up, self.s_comp, self.s_down):
+            s.synchronize()
+        check_status(self.status, "prefill pipeline")
+
+
 def segments_host(plan: ShardPlan):
     """Copy the plan's segment table to the host (list of dicts)."""
     s = plan.segs[: plan.total_segs].cpu().tolist()

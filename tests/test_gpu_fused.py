@@ -218,3 +218,42 @@ def test_pass_q_ring_128k_sampled():
     O_ref, L_ref = oracle_dense_rows(inputs, w.new_lens, w.prefix_lens, w.scale, rows)
     idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
     assert_attn_close(o[idx], lse[idx], O_ref, L_ref, "128k/pass-q")
+
+
+# ------------------------------------------------------ host pipeline ----
+
+@pytest.mark.parametrize("name", ["varlen6_gqa", "single1k_d64"])
+def test_prefill_pipeline_matches_single_calls(name):
+    """Batches submitted through the overlapped host pipeline (two buffer sets,
+    three streams) give exactly what one cp_prefill_attention call gives."""
+    w = W.WORKLOADS[name]
+    batches = [W.make_inputs(w, seed_offset=i) for i in range(5)]
+    pipe = cpa.PrefillPipeline(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], w.Hq,
+                               w.Hkv, w.d, w.dv, w.scale)
+    outs = []
+    for b in batches:
+        ho = torch.empty((w.total_new, w.Hq, w.dv), dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty((w.total_new, w.Hq), dtype=torch.float32).pin_memory()
+        pipe.submit(b["q"].pin_memory(), b["k"].pin_memory(), b["v"].pin_memory(), ho, hl)
+        outs.append((ho, hl))
+    pipe.synchronize()
+    for b, (ho, hl) in zip(batches, outs):
+        status, plan, _, q, k, v = setup(w, w.strategies[0], b)
+        o, lse = cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=status,
+                                          fuse_restore=True)
+        torch.cuda.synchronize()
+        assert torch.equal(ho, o.cpu())
+        assert torch.equal(hl, lse.cpu())
+
+
+def test_prefill_pipeline_mla_latent_view():
+    w = mla_case([300, 77], [0, 40], 4, 3, 951)
+    b = W.make_inputs(w)
+    pipe = cpa.PrefillPipeline(w.new_lens, w.prefix_lens, w.cp_size, "interleave", w.Hq, w.Hkv,
+                               w.d, w.dv, w.scale, v_is_k_prefix=True)
+    ho = torch.empty((w.total_new, w.Hq, w.dv), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.total_new, w.Hq), dtype=torch.float32).pin_memory()
+    pipe.submit(b["q"].pin_memory(), b["k"].pin_memory(), None, ho, hl)
+    pipe.synchronize()
+    O_ref, L_ref = dense_ref(w, b)
+    assert_attn_close(ho, hl, O_ref, L_ref, "mla/pipeline")
