@@ -634,6 +634,8 @@ def run_profile_case(args):
                fused into the store, as in the bench step).
     merge:     the heaviest query block of the 128K partial-KV workload
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
+    merge4:    query block 3 of that workload (4 partials, 0.54 GB read; the
+               few-partial kernel).
     restore:   the O restore of the default workload (268 MB each way)."""
     import torch
 
@@ -642,9 +644,10 @@ def run_profile_case(args):
 
     dev = torch.device("cuda", 0)
     status = cpa.new_status(dev)
-    if args.profile_case == "merge":
+    if args.profile_case in ("merge", "merge4"):
         w = W.WORKLOADS[MERGE_WORKLOAD]
-        rows, Hq, dv, nb = w.total_new // 16, w.Hq, w.dv, 16
+        rows, Hq, dv = w.total_new // 16, w.Hq, w.dv
+        nb = 16 if args.profile_case == "merge" else 4
         g = torch.Generator(device=dev).manual_seed(5)
         po = torch.randn((nb, rows, Hq, dv), device=dev, generator=g)
         pl = torch.randn((nb, rows, Hq), device=dev, generator=g)
@@ -691,7 +694,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-merge", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--profile-case", choices=["attention", "merge", "restore"], default=None,
+    ap.add_argument("--profile-case", choices=["attention", "merge", "merge4", "restore"],
+                    default=None,
                     help="run one kernel on a small case (for ncu) instead of the bench")
     args = ap.parse_args()
     if args.warmup < 3:
