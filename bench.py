@@ -37,6 +37,8 @@ METRIC = "causal CP-prefill attention TFLOPS & % of GB300 bf16 peak; LSE-merge G
 UNIT = "TFLOP/s"
 WORKLOAD = "llama8b_32k"
 MERGE_WORKLOAD = "partialkv_128k"
+# ncu summary under profiles/ holding the attention kernel's DRAM bytes per launch
+PROFILE_MD = {"llama8b_32k": "attn_fwd_llama8b_32k.md", "mla_16k": "attn_mla_mla_16k.md"}
 
 
 def peaks():
@@ -59,6 +61,8 @@ def profiled_traffic(kernel_md="attn_fwd_llama8b_32k.md"):
     import hashlib
     import re
 
+    if not kernel_md:
+        return None
     path = os.path.join(ROOT, "profiles", kernel_md)
     try:
         text = open(path).read()
@@ -331,7 +335,7 @@ def run_ours(args):
             "roofline": {"kernel": kernel_label(w),
                          "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                         "traffic": profiled_traffic() if w.name == WORKLOAD else None,
+                         "traffic": profiled_traffic(PROFILE_MD.get(w.name, "")),
                          "traffic_unit": "bytes per launch (ncu dram read + write)",
                          "algorithmic_bytes": algorithmic_bytes(w),
                          "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
