@@ -192,3 +192,13 @@ def test_select_pass_rejects_bad_arguments():
     for args in ((0, 5, 8, 8, 0), (5, -1, 8, 8, 0), (5, 5, 6, 4, 0), (5, 5, 8, 8, 2),
                  (1 << 41, 0, 8, 8, 0)):
         assert lib.cp_select_pass(*args, None) == L.ERR_INVALID_ARG
+
+
+def test_plan_limits_refused_on_host():
+    """cp_size above CPATTN_MAX_CP and more than CPATTN_MAX_REQS requests."""
+    with pytest.raises(L.CpAttnError):
+        api.cp_shard_plan_sizes([5], [0], 1025, "zigzag")
+    with pytest.raises(L.CpAttnError):
+        api.cp_shard_plan_sizes([1] * 65537, [0] * 65537, 2, "zigzag")
+    rows, _, _ = api.cp_shard_plan_sizes([2100, 5, 4096], [0, 3, 100], 1024, "zigzag")
+    assert sum(rows) == 2100 + 5 + 4096 and len(rows) == 1024

@@ -432,3 +432,20 @@ def test_partial_kv_workspace_too_small_is_reported():
                            workspace=small, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) in (cpa.api.L.ERR_INVALID_ARG, cpa.api.L.ERR_RANGE)
+
+
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+@pytest.mark.parametrize("C", [4, 8])
+def test_many_tiny_requests_all_rows(strategy, C):
+    """400 requests of 0..20 new tokens after 0..10 cached ones: hundreds of
+    one-tile segments, many with a single row, and empty requests."""
+    new = [(i * 13) % 21 for i in range(400)]
+    pre = [(i * 7) % 11 for i in range(400)]
+    w = W.Workload(name=f"tiny{C}", new_lens=new, prefix_lens=pre, Hq=4, Hkv=2, d=64, dv=64,
+                   scale=0.125, std=1.0, cp_size=C, strategies=[strategy], seed=7100 + C)
+    inputs = W.make_inputs(w)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    o, lse = run_full_kv(w, strategy, inputs)
+    assert_attn_close(o, lse, O_ref, L_ref, f"tiny/{strategy}/C{C}")

@@ -91,3 +91,20 @@ def test_size_mismatch_sets_status():
     cpa.cp_shard_plan(plan, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == -1
+
+
+def test_maximum_cp_size():
+    """C = CPATTN_MAX_CP (1024): 2048 zigzag blocks per request, most of them
+    empty or single-token."""
+    check_plan([2100, 5, 4096], [0, 3, 100], 1024, "zigzag")
+    check_plan([2100, 5, 4096], [0, 3, 100], 1024, "interleave")
+
+
+def test_maximum_request_count():
+    """num_reqs = CPATTN_MAX_REQS (65536) tiny requests, including empty ones."""
+    n = 65536
+    new = [(i * 7) % 5 for i in range(n)]
+    pre = [(i * 3) % 4 for i in range(n)]
+    check_plan(new, pre, 2, "zigzag")
+    check_plan(new, pre, 3, "interleave")
+
