@@ -134,6 +134,10 @@ def config_of(w, extra=None):
 
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms; entering
+    waits (up to 3 s) for the first sample so that the samples kept, those
+    read between entering and leaving, fall inside the timed region."""
+
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -141,26 +145,41 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
+        self.keep = False
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if self.keep:
+                self.lines.append(line)
+            self.first.set()
 
     def __enter__(self):
+        import threading
+        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except Exception:  # noqa: BLE001
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        self.first.wait(timeout=3.0)
+        self.keep = True
         return self
 
     def __exit__(self, *a):
-        self.out = ""
+        self.keep = False
+        self.out = "".join(self.lines)
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:  # noqa: BLE001
                 self.proc.kill()
-                self.out = ""
 
     def summary(self):
         sms, mx, reasons = [], None, set()
