@@ -36,6 +36,51 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+def _dev(t, name, dtype=None, ref=None, contiguous=True):
+    """Check a device argument before its pointer reaches a kernel: a CUDA
+    tensor (on ref's device), of dtype, contiguous.  None passes through."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if ref is not None and t.device != ref.device:
+        raise ValueError(f"{name} is on {t.device}, the call runs on {ref.device}")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _segments(segs, num_segs, tiles, num_tiles, ref):
+    _dev(segs, "segs", torch.int32, ref)
+    if segs.dim() != 2 or segs.shape[1] != 8:
+        raise ValueError("segs must be int32 [S, 8] (cp_segment_t rows)")
+    ns = segs.shape[0] if num_segs is None else int(num_segs)
+    if ns < 0 or ns > segs.shape[0]:
+        raise ValueError("num_segs exceeds the segment table")
+    nt = 0
+    if tiles is not None:
+        _dev(tiles, "tiles", torch.int32, ref)
+        if tiles.dim() != 2 or tiles.shape[1] != 2:
+            raise ValueError("tiles must be int32 [T, 2]")
+        nt = tiles.shape[0] if num_tiles is None else int(num_tiles)
+        if nt < 0 or nt > tiles.shape[0]:
+            raise ValueError("num_tiles exceeds the tile list")
+    return ns, nt
+
+
+def _status(status, ref):
+    if status is not None:
+        _dev(status, "status", torch.int32, ref)
+        if status.numel() < 1:
+            raise ValueError("status needs one int32")
+
+
 def _i32_array(xs):
     xs = [int(x) for x in xs]
     return (ctypes.c_int32 * max(1, len(xs)))(*xs), len(xs)
@@ -119,6 +164,10 @@ def alloc_plan(new_lens, prefix_lens, cp_size, strategy, device="cuda") -> Shard
 def cp_shard_plan(plan: ShardPlan, status=None, stream=None) -> ShardPlan:
     """Fill ``plan``'s device buffers (kernel launches on ``stream``)."""
     lib = L.load()
+    for name in ("new_lens_dev", "prefix_lens_dev", "segs", "seg_offsets", "row_offsets",
+                 "gather_idx", "positions", "restore_idx", "tiles"):
+        _dev(getattr(plan, name), "plan." + name, torch.int32, plan.segs)
+    _status(status, plan.segs)
     L.check(lib.cp_shard_plan(
         _p(plan.new_lens_dev), _p(plan.prefix_lens_dev), plan.num_reqs, plan.cp_size, plan.strategy,
         plan.total_rows, plan.total_segs, plan.total_tiles, _p(plan.segs), _p(plan.seg_offsets),
@@ -134,42 +183,53 @@ def make_plan(new_lens, prefix_lens, cp_size, strategy, device="cuda", status=No
 
 
 # ---------------------------------------------------------------- attention --
-def cp_attn_partial(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tiles=None,
-                    kv_lo=0, kv_hi=-1, out=None, lse=None, out_fp32=False, out_row_base=0,
-                    num_out_rows=None, status=None, stream=None):
-    """Partial causal attention of every segment row (see cp_attn_partial in cpattn.h)."""
-    lib = L.load()
-    rows, Hq, d = q.shape
-    Hkv, dv = v.shape[1], v.shape[2]
-    if k.shape[1] != Hkv or k.shape[0] != v.shape[0]:
-        raise ValueError("k and v disagree on rows or heads")
-    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-        raise TypeError("q, k and v must be bfloat16")
-    if not q.is_contiguous() or k.stride(2) != 1 or v.stride(2) != 1:
-        raise ValueError("q must be contiguous; k and v need a contiguous last dim")
-    n_out = rows if num_out_rows is None else num_out_rows
-    if out is None:
-        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
-                          device=q.device)
-    if lse is None:
-        lse = torch.empty((n_out, Hq), dtype=torch.float32, device=q.device)
-    ns = segs.shape[0] if num_segs is None else num_segs
-    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
-    L.check(lib.cp_attn_partial(
-        _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
-        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
-        int(kv_hi), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse), int(out_row_base),
-        out.shape[0], _p(status), _stream(stream)), "cp_attn_partial")
-    return out, lse
-
-
 def _check_qkv(q, k, v):
+    _dev(q, "q", torch.bfloat16)
+    _dev(k, "k", torch.bfloat16, q, contiguous=False)
+    _dev(v, "v", torch.bfloat16, q, contiguous=False)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k and v are [rows, heads, dim]")
     if k.shape[1] != v.shape[1] or k.shape[0] != v.shape[0]:
         raise ValueError("k and v disagree on rows or heads")
     if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
         raise TypeError("q, k and v must be bfloat16")
     if not q.is_contiguous() or k.stride(2) != 1 or v.stride(2) != 1:
         raise ValueError("q must be contiguous; k and v need a contiguous last dim")
+
+
+def _attn_outputs(out, lse, n_out, Hq, dv, out_fp32, ref):
+    """Allocate or check the O [n, Hq, dv] (bf16 / fp32) and LSE [n, Hq] outputs."""
+    if out is None:
+        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=ref.device)
+    _dev(out, "out", (torch.bfloat16, torch.float32), ref)
+    if out.dim() != 3 or tuple(out.shape[1:]) != (Hq, dv):
+        raise ValueError(f"out must be [rows, {Hq}, {dv}], got {tuple(out.shape)}")
+    if lse is None:
+        lse = torch.empty((out.shape[0], Hq), dtype=torch.float32, device=ref.device)
+    _dev(lse, "lse", torch.float32, ref)
+    _shape(lse, "lse", (out.shape[0], Hq))
+    return out, lse
+
+
+def cp_attn_partial(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tiles=None,
+                    kv_lo=0, kv_hi=-1, out=None, lse=None, out_fp32=False, out_row_base=0,
+                    num_out_rows=None, status=None, stream=None):
+    """Partial causal attention of every segment row (see cp_attn_partial in cpattn.h)."""
+    lib = L.load()
+    _check_qkv(q, k, v)
+    rows, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    n_out = rows if num_out_rows is None else num_out_rows
+    out, lse = _attn_outputs(out, lse, n_out, Hq, dv, out_fp32, q)
+    ns, nt = _segments(segs, num_segs, tiles, num_tiles, q)
+    _status(status, q)
+    L.check(lib.cp_attn_partial(
+        _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
+        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
+        int(kv_hi), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse), int(out_row_base),
+        out.shape[0], _p(status), _stream(stream)), "cp_attn_partial")
+    return out, lse
 
 
 def cp_attn_partial_restore(segs, q, k, v, scale, dst_rows, *, num_out_rows=None,
@@ -180,16 +240,13 @@ def cp_attn_partial_restore(segs, q, k, v, scale, dst_rows, *, num_out_rows=None
     _check_qkv(q, k, v)
     rows, Hq, d = q.shape
     Hkv, dv = v.shape[1], v.shape[2]
-    if dst_rows.dtype != torch.int32 or dst_rows.shape[0] < rows:
+    _dev(dst_rows, "dst_rows", torch.int32, q)
+    if dst_rows.dim() != 1 or dst_rows.shape[0] < rows:
         raise ValueError("dst_rows must be int32 with one entry per query row")
     n_out = rows if num_out_rows is None else num_out_rows
-    if out is None:
-        out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
-                          device=q.device)
-    if lse is None:
-        lse = torch.empty((n_out, Hq), dtype=torch.float32, device=q.device)
-    ns = segs.shape[0] if num_segs is None else num_segs
-    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
+    out, lse = _attn_outputs(out, lse, n_out, Hq, dv, out_fp32, q)
+    ns, nt = _segments(segs, num_segs, tiles, num_tiles, q)
+    _status(status, q)
     L.check(lib.cp_attn_partial_restore(
         _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
         v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
@@ -206,14 +263,15 @@ def cp_attn_partial_accumulate(segs, q, k, v, scale, o_acc, lse_acc, lse_out, *,
     _check_qkv(q, k, v)
     rows, Hq, d = q.shape
     Hkv, dv = v.shape[1], v.shape[2]
-    if o_acc.dtype != torch.float32 or lse_acc.dtype != torch.float32 or \
-            lse_out.dtype != torch.float32:
-        raise TypeError("the accumulator is float32")
-    if o_acc.shape[1:] != (Hq, dv) or not o_acc.is_contiguous() or \
-            lse_acc.shape != (o_acc.shape[0], Hq) or lse_out.shape != lse_acc.shape:
-        raise ValueError("accumulator shapes disagree with q / v")
-    ns = segs.shape[0] if num_segs is None else num_segs
-    nt = 0 if tiles is None else (tiles.shape[0] if num_tiles is None else num_tiles)
+    _dev(o_acc, "o_acc", torch.float32, q)
+    _dev(lse_acc, "lse_acc", torch.float32, q)
+    _dev(lse_out, "lse_out", torch.float32, q)
+    if o_acc.dim() != 3 or tuple(o_acc.shape[1:]) != (Hq, dv):
+        raise ValueError("o_acc must be [rows, Hq, dv]")
+    _shape(lse_acc, "lse_acc", (o_acc.shape[0], Hq))
+    _shape(lse_out, "lse_out", (o_acc.shape[0], Hq))
+    ns, nt = _segments(segs, num_segs, tiles, num_tiles, q)
+    _status(status, q)
     L.check(lib.cp_attn_partial_accumulate(
         _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
         v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
@@ -227,15 +285,30 @@ def cp_lse_merge(o_parts, lse_parts, *, dst_rows=None, out=None, lse_out=None, o
                  num_out_rows=None, status=None, stream=None):
     """LSE merge over axis 0 of o_parts [n, rows, Hq, dv] / lse_parts [n, rows, Hq]."""
     lib = L.load()
+    _dev(o_parts, "o_parts", torch.float32, contiguous=False)
+    _dev(lse_parts, "lse_parts", torch.float32, o_parts, contiguous=False)
+    if o_parts.dim() != 4 or lse_parts.dim() != 3:
+        raise ValueError("o_parts is [n, rows, Hq, dv] and lse_parts [n, rows, Hq]")
     n, rows, Hq, dv = o_parts.shape
-    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
-        raise TypeError("partials must be float32")
+    if tuple(lse_parts.shape) != (n, rows, Hq):
+        raise ValueError("lse_parts disagrees with o_parts")
     if o_parts[0].stride() != (Hq * dv, dv, 1) or lse_parts[0].stride() != (Hq, 1):
         raise ValueError("each partial must be contiguous")
-    n_out = (rows if dst_rows is None else rows) if num_out_rows is None else num_out_rows
+    if dst_rows is not None:
+        _dev(dst_rows, "dst_rows", torch.int32, o_parts)
+        if dst_rows.dim() != 1 or dst_rows.shape[0] < rows:
+            raise ValueError("dst_rows needs one int32 per row")
+    n_out = rows if num_out_rows is None else num_out_rows
     if out is None:
         out = torch.empty((n_out, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
                           device=o_parts.device)
+    _dev(out, "out", (torch.bfloat16, torch.float32), o_parts)
+    if out.dim() != 3 or tuple(out.shape[1:]) != (Hq, dv):
+        raise ValueError("out must be [rows, Hq, dv]")
+    if lse_out is not None:
+        _dev(lse_out, "lse_out", torch.float32, o_parts)
+        _shape(lse_out, "lse_out", (out.shape[0], Hq))
+    _status(status, o_parts)
     L.check(lib.cp_lse_merge(
         _p(o_parts), _p(lse_parts), n, o_parts.stride(0), lse_parts.stride(0), rows, Hq, dv,
         _p(dst_rows), _p(out), 1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0],
@@ -247,12 +320,17 @@ def cp_lse_merge(o_parts, lse_parts, *, dst_rows=None, out=None, lse_out=None, o
 def cp_restore(src, idx, *, out=None, status=None, stream=None):
     """out[i] = src[idx[i]] (rows along dim 0)."""
     lib = L.load()
+    _dev(src, "src")
+    _dev(idx, "idx", torch.int32, src)
+    if idx.dim() != 1:
+        raise ValueError("idx must be a 1-D int32 index")
     rows = idx.shape[0]
     row_bytes = src[0].numel() * src.element_size() if src.shape[0] > 0 else 0
-    if not src.is_contiguous():
-        raise ValueError("src must be contiguous")
     if out is None:
         out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    _dev(out, "out", src.dtype, src)
+    _shape(out, "out", (rows,) + tuple(src.shape[1:]))
+    _status(status, src)
     L.check(lib.cp_restore(_p(src), src.shape[0], _p(idx), rows, row_bytes, _p(out), _p(status),
                            _stream(stream)), "cp_restore")
     return out
@@ -410,14 +488,18 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
     Hkv, dv = v.shape[1], v.shape[2]
     nbytes, max_blocks = cp_partial_kv_workspace_size(new_lens, prefix_lens, plan.cp_size,
                                                       plan.strategy, kv_block, Hq, dv)
+    _check_qkv(q_cat, k, v)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_cat.device)
+    _dev(workspace, "workspace", torch.uint8, q_cat)
     idx = plan.gather_idx[:N] if isinstance(dst_rows, str) else dst_rows
-    if out is None:
-        out = torch.empty((N, Hq, dv), dtype=torch.float32 if out_fp32 else torch.bfloat16,
-                          device=q_cat.device)
-    if lse_out is None:
-        lse_out = torch.empty((N, Hq), dtype=torch.float32, device=q_cat.device)
+    if idx is not None:
+        _dev(idx, "dst_rows", torch.int32, q_cat)
+        if idx.dim() != 1 or idx.shape[0] < N:
+            raise ValueError("dst_rows needs one int32 per query row")
+    out, lse_out = _attn_outputs(out, lse_out, N, Hq, dv, out_fp32, q_cat)
+    _segments(plan.segs, plan.total_segs, plan.tiles, plan.total_tiles, q_cat)
+    _status(status, q_cat)
     L.check(lib.cp_attn_partial_kv(
         _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
         k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,

@@ -202,3 +202,26 @@ def test_plan_limits_refused_on_host():
         api.cp_shard_plan_sizes([1] * 65537, [0] * 65537, 2, "zigzag")
     rows, _, _ = api.cp_shard_plan_sizes([2100, 5, 4096], [0, 3, 100], 1024, "zigzag")
     assert sum(rows) == 2100 + 5 + 4096 and len(rows) == 1024
+
+
+def test_binding_refuses_host_tensors_before_any_launch():
+    """A host tensor (or wrong dtype / shape) never reaches a kernel as a
+    device pointer: the binding raises first."""
+    import torch
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
+    segs = torch.zeros(1, 8, dtype=torch.int32)
+    idx = torch.zeros(8, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_attn_partial(segs, q, q, q, 0.1)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_attn_partial_restore(segs, q, q, q, 0.1, idx)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_attn_partial_accumulate(segs, q, q, q, 0.1, torch.zeros(8, 2, 64),
+                                       torch.zeros(8, 2), torch.zeros(8, 2))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_lse_merge(torch.zeros(2, 8, 2, 64), torch.zeros(2, 8, 2))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_restore(q, idx)
+    plan = api.alloc_plan([16], [0], 4, "zigzag", device="cpu")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        api.cp_shard_plan(plan)
