@@ -371,6 +371,8 @@ def run_ours(args):
         line["gpu_launches"] += line["partial_kv"].pop("launches")
         line["pass_q"] = bench_pass_q(args, dev, stream, pk)
         line["gpu_launches"] += line["pass_q"].pop("launches")
+        line["merge_sweep"] = bench_merge_sweep(args, dev, stream, pk)
+        line["gpu_launches"] += line["merge_sweep"].pop("launches")
     if not args.skip_e2e:
         line["e2e"] = bench_e2e(args, w, inputs, dev, stream)
     del q, k, v, ws, flush
@@ -602,6 +604,95 @@ def bench_pass_q(args, dev, stream, pk):
             "path": "cp_shard_plan + cp_restore + cp_pass_q_attention (one "
                     "cp_attn_partial_accumulate per hop, rank and resident KV block) + "
                     "cp_restore of O and LSE"}
+
+
+def bench_merge_sweep(args, dev, stream, pk):
+    """Decode-style merge sweep: 64 single-token queries x 32 heads over 65536
+    keys, key i resident on shard i mod 8 (a strided view of the KV, no copy).
+    The decode step is, per shard, a split-KV partial (cp_attn_split_kv: keys
+    in blocks of 512 over separate CTAs, merged in the library) and then one
+    LSE merge of the 8 shard partials; the merge alone (8 partials, 9.5 MB,
+    L2-sized) is reported both warm (launches queued behind a GPU sleep, run
+    back to back) and with L2 flushed before each call."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+    from context_causal_attention_cp_gb300 import workloads as W
+
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q = inputs["q"].to(dev)
+    k = inputs["k"].to(dev)
+    v = inputs["v"].to(dev)
+    S, nq, Hq, dv = m["shards"], m["queries"], m["Hq"], m["dv"]
+    n_kv = m["kv_tokens"] // S
+    seg = torch.tensor([[0, nq, n_kv - 1, 0, 0, n_kv, 0, 0]], dtype=torch.int32, device=dev)
+    po = torch.empty(S, nq, Hq, dv, device=dev)
+    pl = torch.empty(S, nq, Hq, device=dev)
+    out = torch.empty(nq, Hq, dv, device=dev)
+    lse = torch.empty(nq, Hq, device=dev)
+    status = cpa.new_status(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def merge():
+        cpa.cp_lse_merge(po, pl, out=out, lse_out=lse, status=status, stream=stream)
+
+    seg_host = seg.cpu()
+    ws = cpa.cp_attn_split_kv(seg, q, k[0::S], v[0::S], m["scale"], 512, segs_host=seg_host,
+                              out=po[0], lse_out=pl[0], status=status, stream=stream)[2]
+
+    def decode_step():
+        for j in range(S):
+            cpa.cp_attn_split_kv(seg, q, k[j::S], v[j::S], m["scale"], 512, segs_host=seg_host,
+                                 out=po[j], lse_out=pl[j], workspace=ws, status=status,
+                                 stream=stream)
+        merge()
+
+    for _ in range(5):
+        decode_step()
+    torch.cuda.synchronize(dev)
+    reps = 50
+    e0, e1 = E(), E()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(300_000_000)  # let the host queue the launches ahead of the GPU
+    e0.record(stream)
+    for _ in range(reps):
+        decode_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    step_us = e0.elapsed_time(e1) * 1e3 / reps
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)
+    e0.record(stream)
+    for _ in range(reps):
+        merge()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_us = e0.elapsed_time(e1) * 1e3 / reps
+    cold = []
+    for _ in range(20):
+        flush.zero_()
+        a, b = E(), E()
+        a.record(stream)
+        merge()
+        b.record(stream)
+        cold.append((a, b))
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, "merge sweep")
+    cold_us = sorted(x.elapsed_time(y) for x, y in cold)[len(cold) // 2] * 1e3
+    nbytes = S * nq * Hq * (dv + 1) * 4 + nq * Hq * (dv + 1) * 4
+    launches = (3 * S + 1) * (reps + 6) + reps + 20
+    del q, k, v, po, pl, flush
+    torch.cuda.empty_cache()
+    return {"queries": nq, "heads": Hq, "kv_tokens": m["kv_tokens"], "shards": S,
+            "decode_step_us": step_us, "merge_bytes": nbytes,
+            "merge_warm_us": warm_us, "merge_warm_gbs": nbytes / (warm_us * 1e-6) / 1e9,
+            "merge_flushed_us": cold_us, "merge_flushed_gbs": nbytes / (cold_us * 1e-6) / 1e9,
+            "merge_flushed_frac_of_hbm": nbytes / (cold_us * 1e-6) / 1e9 / pk["hbm_gbs"],
+            "launches": launches,
+            "path": "8 x cp_attn_split_kv (kv blocks of 512) over strided KV views + "
+                    "cp_lse_merge (8 partials)"}
 
 
 def bench_e2e(args, w, inputs, dev, stream):

@@ -55,6 +55,8 @@ SIGNATURES = {
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
     "cp_partial_kv_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32,
                                            ctypes.POINTER(ctypes.c_int64), c_i32p]),
+    "cp_partial_kv_workspace_size_segs": (i32, [vp, i32, i32, i32, i32,
+                                                ctypes.POINTER(ctypes.c_int64), c_i32p]),
     "cp_attn_partial_kv": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32,
                                  i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, vp, i32, vp,
                                  i32, vp, i64, vp, vp]),

@@ -509,6 +509,47 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
     return out, lse_out, workspace
 
 
+def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_rows=None,
+                     dst_rows=None, out=None, lse_out=None, out_fp32=True, workspace=None,
+                     status=None, stream=None):
+    """cp_attn_partial over any segment table with every segment's keys split
+    into blocks of ``kv_block`` attended by separate CTAs, then merged by the
+    LSE rule inside the library (cp_attn_partial_kv without a plan).  Meant for
+    few query rows over many keys, e.g. a decode step against one KV shard.
+    ``dst_rows`` (int32, one per query row) scatters the output; otherwise row
+    i of the output is query row i.  Returns (O, LSE, workspace).
+    """
+    lib = L.load()
+    _check_qkv(q, k, v)
+    rows, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    ns, _ = _segments(segs, None, None, None, q)
+    if segs_host is None:
+        segs_host = segs.cpu()
+    sh = segs_host.to(torch.int32).contiguous()
+    nbytes, max_blocks = ctypes.c_int64(), ctypes.c_int32()
+    L.check(lib.cp_partial_kv_workspace_size_segs(
+        ctypes.c_void_p(sh.data_ptr()), ns, int(kv_block), Hq, dv, ctypes.byref(nbytes),
+        ctypes.byref(max_blocks)), "cp_partial_kv_workspace_size_segs")
+    if workspace is None:
+        workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=q.device)
+    _dev(workspace, "workspace", torch.uint8, q)
+    if dst_rows is not None:
+        _dev(dst_rows, "dst_rows", torch.int32, q)
+        if dst_rows.dim() != 1 or dst_rows.shape[0] < rows:
+            raise ValueError("dst_rows needs one int32 per query row")
+    n_out = rows if num_out_rows is None else num_out_rows
+    out, lse_out = _attn_outputs(out, lse_out, n_out, Hq, dv, out_fp32, q)
+    _status(status, q)
+    L.check(lib.cp_attn_partial_kv(
+        _p(segs), ns, None, 0, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v), v.stride(0),
+        v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_block),
+        max(1, int(max_blocks.value)), _p(dst_rows), _p(out),
+        1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
+        workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
+    return out, lse_out, workspace
+
+
 def cp_partial_kv_attention(q_cat, k, v, plan: ShardPlan, scale, kv_block, *, segs_host=None,
                             parts_o=None, parts_lse=None, out=None, lse_out=None, status=None,
                             stream=None):

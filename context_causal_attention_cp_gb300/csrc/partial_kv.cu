@@ -287,6 +287,28 @@ extern "C" int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32
   return CPATTN_OK;
 }
 
+extern "C" int cp_partial_kv_workspace_size_segs(const cp_segment_t* segs_host, int num_segs,
+                                                 int kv_block, int Hq, int dv, int64_t* bytes,
+                                                 int32_t* max_blocks) {
+  if (num_segs < 0 || kv_block < 1 || Hq < 1 || dv < 4 || (dv % 4) != 0 || !bytes)
+    return CPATTN_ERR_INVALID_ARG;
+  if (num_segs > 0 && !segs_host) return CPATTN_ERR_INVALID_ARG;
+  long long rows = 0, mb = 0;
+  for (int i = 0; i < num_segs; ++i) {
+    const cp_segment_t& sg = segs_host[i];
+    if (sg.q_len < 0 || sg.q_pos0 < 0 || sg.q_pos_step < 0) return CPATTN_ERR_INVALID_ARG;
+    if (sg.q_len == 0) continue;
+    const long long last = (long long)sg.q_pos0 + (long long)(sg.q_len - 1) * sg.q_pos_step;
+    const long long nb = last / kv_block + 1;
+    rows += nb * sg.q_len;
+    mb = std::max(mb, nb);
+  }
+  const long long header = round256((2LL * num_segs + 2) * 8);
+  *bytes = header + round256(rows * Hq * dv * 4) + round256(rows * Hq * 4) + 256;
+  if (max_blocks) *max_blocks = (int32_t)std::min<long long>(mb, 0x7fffffff);
+  return CPATTN_OK;
+}
+
 extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                                   const int32_t* tiles_dev, int num_tiles, const void* q,
                                   int num_q_rows, const void* k, int64_t k_row_stride,

@@ -269,6 +269,11 @@ int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, i
 int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
                                  int num_reqs, int cp_size, int strategy, int kv_block, int Hq,
                                  int dv, int64_t* bytes, int32_t* max_blocks);
+/* The same sizing for an explicit segment table on the host (for segments
+ * that no plan made, e.g. a decode step's few queries over a KV shard):
+ * bytes and the largest block count over segs_host[0 .. num_segs). */
+int cp_partial_kv_workspace_size_segs(const cp_segment_t* segs_host, int num_segs, int kv_block,
+                                      int Hq, int dv, int64_t* bytes, int32_t* max_blocks);
 int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
                        int num_tiles, const void* q, int num_q_rows, const void* k,
                        int64_t k_row_stride, int64_t k_head_stride, const void* v,

@@ -225,3 +225,36 @@ def test_binding_refuses_host_tensors_before_any_launch():
     plan = api.alloc_plan([16], [0], 4, "zigzag", device="cpu")
     with pytest.raises(ValueError, match="CUDA tensor"):
         api.cp_shard_plan(plan)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_workspace_size_from_segments_matches_plan_sizing(seed, strategy):
+    """cp_partial_kv_workspace_size_segs over a plan's own segments gives the
+    plan-based sizing, and decode-style segments (step 0) size by hand."""
+    import torch
+    new, pre = W.random_batch(400 + seed, max_reqs=5, max_new=700, max_prefix=300)
+    C, kv_block, Hq, dv = [2, 3, 4, 8, 1, 5][seed], [64, 100, 256, 512, 7, 1000][seed], 8, 64
+    op = oplan.make_plan(new, pre, C, strategy)
+    rows = [[s.q_row0, s.q_len, s.q_pos0, s.q_pos_step, s.kv_row0, s.kv_len,
+             op.gather_idx[s.q_row0], s.req] for r in range(C) for s in op.segments[r]]
+    lib = L.load()
+    seg = torch.tensor(rows or [[0] * 8], dtype=torch.int32)
+    b1, m1 = ctypes.c_int64(), ctypes.c_int32()
+    assert lib.cp_partial_kv_workspace_size_segs(ctypes.c_void_p(seg.data_ptr()), len(rows),
+                                                 kv_block, Hq, dv, ctypes.byref(b1),
+                                                 ctypes.byref(m1)) == L.OK
+    b2, m2 = api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv)
+    assert (b1.value, m1.value) == (b2, m2)
+
+
+def test_workspace_size_for_decode_segment():
+    import torch
+    lib = L.load()
+    seg = torch.tensor([[0, 64, 8191, 0, 0, 8192, 0, 0]], dtype=torch.int32)
+    b, m = ctypes.c_int64(), ctypes.c_int32()
+    assert lib.cp_partial_kv_workspace_size_segs(ctypes.c_void_p(seg.data_ptr()), 1, 512, 32, 128,
+                                                 ctypes.byref(b), ctypes.byref(m)) == L.OK
+    rows = 16 * 64                       # 16 blocks of 512 keys, 64 rows each
+    expect = 256 + ((rows * 32 * 128 * 4 + 255) // 256) * 256 + ((rows * 32 * 4 + 255) // 256) * 256 + 256
+    assert (b.value, m.value) == (expect, 16)

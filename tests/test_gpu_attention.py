@@ -449,3 +449,51 @@ def test_many_tiny_requests_all_rows(strategy, C):
                                                w.scale)
     o, lse = run_full_kv(w, strategy, inputs)
     assert_attn_close(o, lse, O_ref, L_ref, f"tiny/{strategy}/C{C}")
+
+
+def test_merge_sweep_strided_kv_views_match_copies():
+    """A shard's interleaved keys passed as a strided view of the KV buffer
+    (row stride 8 rows) give exactly the partial of a gathered copy."""
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q, k, v = inputs["q"].cuda(), inputs["k"].cuda(), inputs["v"].cuda()
+    S, n_kv = m["shards"], m["kv_tokens"] // m["shards"]
+    seg = torch.tensor([[0, m["queries"], n_kv - 1, 0, 0, n_kv, 0, 0]], dtype=torch.int32,
+                       device="cuda")
+    status = cpa.new_status()
+    for j in (0, 3, 7):
+        idx = torch.arange(j, m["kv_tokens"], S, dtype=torch.int32, device="cuda")
+        o1, l1 = cpa.cp_attn_partial(seg, q, cpa.cp_restore(k, idx), cpa.cp_restore(v, idx),
+                                     m["scale"], out_fp32=True, status=status)
+        o2, l2 = cpa.cp_attn_partial(seg, q, k[j::S], v[j::S], m["scale"], out_fp32=True,
+                                     status=status)
+        torch.cuda.synchronize()
+        cpa.check_status(status, "strided views")
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("kv_block", [512, 1024, 8192])
+def test_decode_sweep_split_kv(kv_block):
+    """The decode path: each shard's partial through cp_attn_split_kv (keys in
+    blocks of kv_block over separate CTAs, merged in the library), then the
+    8 shard partials merged; equals attention over all 65536 keys."""
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q, k, v = inputs["q"].cuda(), inputs["k"].cuda(), inputs["v"].cuda()
+    S, n_kv = m["shards"], m["kv_tokens"] // m["shards"]
+    seg = torch.tensor([[0, m["queries"], n_kv - 1, 0, 0, n_kv, 0, 0]], dtype=torch.int32,
+                       device="cuda")
+    po = torch.empty(S, m["queries"], m["Hq"], m["dv"], device="cuda")
+    pl = torch.empty(S, m["queries"], m["Hq"], device="cuda")
+    status = cpa.new_status()
+    ws = None
+    for j in range(S):
+        _, _, ws = cpa.cp_attn_split_kv(seg, q, k[j::S], v[j::S], m["scale"], kv_block,
+                                        out=po[j], lse_out=pl[j], workspace=ws, status=status)
+    out, lse = cpa.cp_lse_merge(po, pl, lse_out=torch.empty(m["queries"], m["Hq"], device="cuda"),
+                                status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "decode split")
+    O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
+                                         m["scale"], np.arange(m["kv_tokens"]))
+    assert_attn_close(out, lse, O_ref, L_ref, f"decode split {kv_block}")
