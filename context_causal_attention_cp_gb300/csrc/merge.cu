@@ -7,9 +7,10 @@
 // Restore (same blog, §2.1): a restore index puts the all-gathered shard rows
 // back into causal token order.
 //
-// Both kernels are HBM-bound streams: one warp per (row, head) merge unit with
-// groups of 16-byte partial loads issued before any use, and a flat
-// grid-stride 16-byte copy for the gather.
+// Both are HBM-bound streams: a warp merges one (row, head) unit per step
+// (or, with at most 8 partials, 16 / n units so that every lane still has 16
+// loads in flight), with groups of 16-byte partial loads issued before any
+// use; the gather is a flat grid-stride 16-byte copy.
 #include <algorithm>
 #include <cstdint>
 
