@@ -117,6 +117,7 @@ pkv_layout_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_bl
 
 constexpr int kMergeThreadsP = 256;
 constexpr int kGroupP = 16;
+constexpr int kFewLoads = 8;  // partial loads per lane per step with few partials
 
 __device__ __forceinline__ float4 ld_stream4(const float* p) {
   float4 v;
@@ -126,55 +127,93 @@ __device__ __forceinline__ float4 ld_stream4(const float* p) {
   return v;
 }
 
-// One warp per (segment row, head): find the segment (binary search on
-// rows_before), merge its nb partials (lane j holds L_j), write the result.
-template <bool OUT_F32>
-__global__ void __launch_bounds__(kMergeThreadsP, 2)
-pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_block,
-                 const long long* __restrict__ slot, const long long* __restrict__ rows_before,
-                 const float* __restrict__ ws_o, const float* __restrict__ ws_l, long long cap_rows,
-                 int Hq, int dv, int num_q_rows, const int32_t* __restrict__ dst_rows,
-                 void* __restrict__ o_out, float* __restrict__ lse_out, int num_out_rows,
-                 int32_t* status) {
-  const int lane = threadIdx.x & 31;
-  const long long total_rows = rows_before[num_segs];
-  const long long units = total_rows * Hq;
-  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long u = warp0; u < units; u += nwarps) {
-    const long long gr = u / Hq;
-    const int h = (int)(u - gr * Hq);
-    int lo = 0, hi = num_segs;  // last segment with rows_before <= gr
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (rows_before[mid] <= gr) lo = mid; else hi = mid;
-    }
-    const cp_segment_t sg = segs[lo];
-    const int i = (int)(gr - rows_before[lo]);
-    if (i < 0 || i >= sg.q_len) {
-      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
-      continue;
-    }
-    const int nb = segment_blocks(sg, kv_block);
-    const long long first = slot[lo] + i;          // partial 0 of this row
-    const long long cat_row = (long long)sg.q_row0 + i;
-    if (cat_row < 0 || cat_row >= num_q_rows) {
-      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
-      continue;
-    }
-    const long long out_row = dst_rows ? (long long)__ldg(dst_rows + cat_row) : cat_row;
-    if (nb > 32 || first + (long long)(nb - 1) * sg.q_len >= cap_rows || out_row < 0 ||
-        out_row >= num_out_rows) {
-      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
-      continue;
-    }
-    const long long stride_rows = sg.q_len;
-    const long long part_stride = stride_rows * Hq * dv;
-    const float* base = ws_o + (first * Hq + h) * dv;
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    // the L_j load and the first group of partial loads go out together
+// Merge of one segment row's partials for all heads, NP <= 8 partials: a
+// warp step merges U = 8 / NP heads (at least one) so that each lane has
+// about 8 partial loads in flight.  Lane L < U*NP owns L_j of (head h0 + L / NP,
+// partial L % NP); the normalised weights are broadcast by shuffles.
+//   o_row: partial 0 of the row, all heads ([Hq, dv] fp32); part_stride /
+//   l_stride: distance between a row's consecutive partials.
+template <bool OUT_F32, int NP>
+__device__ __forceinline__ void pkv_merge_row_few(const float* __restrict__ o_row,
+                                                  const float* __restrict__ l_row,
+                                                  long long part_stride, long long l_stride,
+                                                  int Hq, int hb, int he, int dv,
+                                                  long long out_row, void* __restrict__ o_out,
+                                                  float* __restrict__ lse_out, int lane) {
+  constexpr int U = kFewLoads / NP > 0 ? kFewLoads / NP : 1;
+  const int ui_l = lane / NP, j_l = lane - ui_l * NP;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int h0 = hb; h0 < he; h0 += U) {
+    const int h_l = h0 + ui_l;
     float lj = -INFINITY;
-    if (lane < nb) lj = __ldg(ws_l + (first + lane * stride_rows) * Hq + h);
+    if (lane < U * NP && h_l < he) lj = __ldg(l_row + j_l * l_stride + h_l);
+    float v4[U * NP][4];
+    for (int c0 = 0; c0 < dv; c0 += 128) {
+      const int c = c0 + lane * 4;
+      const bool act = c < dv;
+#pragma unroll
+      for (int sl = 0; sl < U * NP; ++sl) {
+        const int ui = sl / NP, j = sl - ui * NP;
+        const float4 v = (act && h0 + ui < he)
+                             ? ld_stream4(o_row + j * part_stride + (long long)(h0 + ui) * dv + c)
+                             : zero;
+        v4[sl][0] = v.x; v4[sl][1] = v.y; v4[sl][2] = v.z; v4[sl][3] = v.w;
+      }
+      if (c0 == 0) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) m = fmaxf(m, __shfl_sync(0xffffffffu, lj, (ui_l * NP + j) & 31));
+        const bool empty = (m == -INFINITY);
+        const float w = empty ? 0.f : __expf(lj - m);
+        float sw = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) sw += __shfl_sync(0xffffffffu, w, (ui_l * NP + j) & 31);
+        lj = empty ? 0.f : w / sw;  // now the normalised weight
+        if (lse_out && lane < U * NP && j_l == 0 && h_l < he)
+          lse_out[out_row * Hq + h_l] = empty ? -INFINITY : m + __logf(sw);
+      }
+#pragma unroll
+      for (int ui = 0; ui < U; ++ui) {
+        float ax = 0.f, ay = 0.f, az = 0.f, aw = 0.f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          const float w = __shfl_sync(0xffffffffu, lj, ui * NP + j);
+          ax = fmaf(w, v4[ui * NP + j][0], ax);
+          ay = fmaf(w, v4[ui * NP + j][1], ay);
+          az = fmaf(w, v4[ui * NP + j][2], az);
+          aw = fmaf(w, v4[ui * NP + j][3], aw);
+        }
+        if (!act || h0 + ui >= he) continue;
+        const long long oo = (out_row * Hq + h0 + ui) * dv + c;
+        if (OUT_F32) {
+          __stcs(reinterpret_cast<float4*>(static_cast<float*>(o_out) + oo),
+                 make_float4(ax, ay, az, aw));
+        } else {
+          uint2 pk;
+          pk.x = pack_bf16x2(ax, ay);
+          pk.y = pack_bf16x2(az, aw);
+          __stcs(reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + oo), pk);
+        }
+      }
+    }
+  }
+}
+
+// Merge of one segment row's nb (> 8, <= 32) partials, one head per warp
+// step: lane j holds L_j; partial loads in groups of kGroupP per lane, the
+// first group issued with the L_j load.
+template <bool OUT_F32>
+__device__ __forceinline__ void pkv_merge_row_many(const float* __restrict__ o_row,
+                                                   const float* __restrict__ l_row, int nb,
+                                                   long long part_stride, long long l_stride,
+                                                   int Hq, int hb, int he, int dv,
+                                                   long long out_row, void* __restrict__ o_out,
+                                                   float* __restrict__ lse_out, int lane) {
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int h = hb; h < he; ++h) {
+    const float* base = o_row + (long long)h * dv;
+    float lj = -INFINITY;
+    if (lane < nb) lj = __ldg(l_row + lane * l_stride + h);
     float4 v[kGroupP];
     {
       const int c = lane * 4;
@@ -224,6 +263,66 @@ pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_blo
       }
     }
     if (lse_out && lane == 0) lse_out[out_row * Hq + h] = empty ? -INFINITY : m + __logf(ws);
+  }
+}
+
+// One warp per (segment row, slice of hs heads): find the row's segment once
+// (binary search on rows_before), check the row's partials and destination,
+// then merge its nb partials for the slice's heads.  hs = Hq when there are
+// rows enough to fill the GPU, smaller for a few rows (e.g. decode).
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kMergeThreadsP, 2)
+pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_block,
+                 const long long* __restrict__ slot, const long long* __restrict__ rows_before,
+                 const float* __restrict__ ws_o, const float* __restrict__ ws_l, long long cap_rows,
+                 int Hq, int dv, int num_q_rows, const int32_t* __restrict__ dst_rows,
+                 void* __restrict__ o_out, float* __restrict__ lse_out, int num_out_rows,
+                 int hs, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int nslices = (Hq + hs - 1) / hs;
+  const long long total_tasks = rows_before[num_segs] * nslices;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long task = warp0; task < total_tasks; task += nwarps) {
+    const long long gr = task / nslices;
+    const int hb = (int)(task - gr * nslices) * hs, he = min(Hq, hb + hs);
+    int lo = 0, hi = num_segs;  // last segment with rows_before <= gr
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (rows_before[mid] <= gr) lo = mid; else hi = mid;
+    }
+    const cp_segment_t sg = segs[lo];
+    const int i = (int)(gr - rows_before[lo]);
+    const long long cat_row = (long long)sg.q_row0 + i;
+    if (i < 0 || i >= sg.q_len || cat_row < 0 || cat_row >= num_q_rows) {
+      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const int nb = segment_blocks(sg, kv_block);
+    const long long first = slot[lo] + i;  // partial 0 of this row
+    const long long out_row = dst_rows ? (long long)__ldg(dst_rows + cat_row) : cat_row;
+    if (nb < 1 || nb > 32 || first + (long long)(nb - 1) * sg.q_len >= cap_rows || out_row < 0 ||
+        out_row >= num_out_rows) {
+      if (lane == 0) set_status(status, CPATTN_ERR_RANGE);
+      continue;
+    }
+    const float* o_row = ws_o + first * Hq * dv;
+    const float* l_row = ws_l + first * Hq;
+    const long long part_stride = (long long)sg.q_len * Hq * dv;
+    const long long l_stride = (long long)sg.q_len * Hq;
+    switch (nb) {
+#define CPATTN_PKV_FEW(NPV)                                                                    \
+  case NPV:                                                                                    \
+    pkv_merge_row_few<OUT_F32, NPV>(o_row, l_row, part_stride, l_stride, Hq, hb, he, dv,      \
+                                    out_row, o_out, lse_out, lane);                            \
+    break;
+      CPATTN_PKV_FEW(1) CPATTN_PKV_FEW(2) CPATTN_PKV_FEW(3) CPATTN_PKV_FEW(4)
+      CPATTN_PKV_FEW(5) CPATTN_PKV_FEW(6) CPATTN_PKV_FEW(7) CPATTN_PKV_FEW(8)
+#undef CPATTN_PKV_FEW
+      default:
+        pkv_merge_row_many<OUT_F32>(o_row, l_row, nb, part_stride, l_stride, Hq, hb, he, dv,
+                                    out_row, o_out, lse_out, lane);
+    }
   }
 }
 
@@ -359,13 +458,18 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
   if (rc != CPATTN_OK) return rc;
 
   const int grid = num_sms() * 2 * 8;
+  // heads per merge task: all of a row's heads, unless the rows (at most
+  // num_q_rows) are too few to give every resident warp a few tasks
+  const long long warps = (long long)grid * (kMergeThreadsP / 32);
+  int hs = Hq;
+  while (hs > 1 && (long long)num_q_rows * ((Hq + hs - 1) / hs) < 4 * warps) hs = (hs + 1) / 2;
   if (o_is_fp32)
     pkv_merge_kernel<true><<<grid, kMergeThreadsP, 0, stream>>>(
         segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
-        o_out, lse_out, num_out_rows, status_dev);
+        o_out, lse_out, num_out_rows, hs, status_dev);
   else
     pkv_merge_kernel<false><<<grid, kMergeThreadsP, 0, stream>>>(
         segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
-        o_out, lse_out, num_out_rows, status_dev);
+        o_out, lse_out, num_out_rows, hs, status_dev);
   return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
