@@ -750,6 +750,8 @@ def run_profile_case(args):
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
     merge4:    query block 3 of that workload (4 partials, 0.54 GB read; the
                few-partial kernel).
+    partial_kv: the whole 128K partial-KV call (layout, split-KV attention,
+               fused merge + restore), as in the partial_kv entry.
     restore:   the O restore of the default workload (268 MB each way)."""
     import torch
 
@@ -758,7 +760,20 @@ def run_profile_case(args):
 
     dev = torch.device("cuda", 0)
     status = cpa.new_status(dev)
-    if args.profile_case in ("merge", "merge4"):
+    if args.profile_case == "partial_kv":
+        w = W.WORKLOADS[MERGE_WORKLOAD]
+        inputs = W.make_inputs(w)
+        plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
+                             status=status)
+        q = cpa.cp_restore(inputs["q"].to(dev), plan.gather_idx[: w.total_new], status=status)
+        k, v = inputs["k"].to(dev), inputs["v"].to(dev)
+        del inputs
+        ws = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
+                                    prefix_lens=w.prefix_lens, status=status)[2]
+        run = lambda: cpa.cp_attn_partial_kv(  # noqa: E731
+            plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens, prefix_lens=w.prefix_lens,
+            workspace=ws, status=status)
+    elif args.profile_case in ("merge", "merge4"):
         w = W.WORKLOADS[MERGE_WORKLOAD]
         rows, Hq, dv = w.total_new // 16, w.Hq, w.dv
         nb = 16 if args.profile_case == "merge" else 4
@@ -808,7 +823,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-merge", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
-    ap.add_argument("--profile-case", choices=["attention", "merge", "merge4", "restore"],
+    ap.add_argument("--profile-case",
+                    choices=["attention", "merge", "merge4", "partial_kv", "restore"],
                     default=None,
                     help="run one kernel on a small case (for ncu) instead of the bench")
     args = ap.parse_args()
