@@ -4,10 +4,10 @@
 Default workload: one 32768-token prompt, Llama-3-8B-shaped attention (32
 query / 8 KV heads, head dim 128), CP = 8 zigzag (16 blocks of 2048), bf16
 N(0,1) synthetic inputs.  One step is the whole hot path on the device:
-shard plan -> gather of each shard's query rows -> causal attention of all 8
-shards against the gathered KV in one launch, whose store writes O and LSE
-straight to causal order (the restore fused through the plan's gather
-index).  ``value`` is causal attention TFLOP/s over the step (2*Hq*(d+dv)
+shard plan -> causal attention of all 8 shards against the gathered KV in
+one launch that reads each shard's query rows and writes O and LSE by token
+index (zigzag shards are runs of consecutive tokens: the query gather and the
+restore happen in the kernel's own loads and stores).  ``value`` is causal attention TFLOP/s over the step (2*Hq*(d+dv)
 flops per visible (query, key) pair), L2 flushed between steps.
 
 The line also carries the LSE-merge GB/s of the 131072-token partial-KV
@@ -298,23 +298,34 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
+    token_rows = strategy == "zigzag"   # zigzag shards are runs of consecutive tokens
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
         cpa.cp_shard_plan(plan, status=status, stream=stream)
-        qc = cpa.cp_restore(q, plan.gather_idx[:N], out=ws["q_cat"], status=status,
-                            stream=stream)
+        if not token_rows:
+            qc = cpa.cp_restore(q, plan.gather_idx[:N], out=ws["q_cat"], status=status,
+                                stream=stream)
         if ev:
             ev[1].record(stream)
-        # attention of every shard; the store puts O and LSE in causal order
-        cpa.cp_attn_partial_restore(plan.segs, qc, k, v, w.scale, plan.gather_idx,
-                                    num_out_rows=N, num_segs=plan.total_segs, tiles=plan.tiles,
-                                    num_tiles=plan.total_tiles, out=ws["o"], lse=ws["lse"],
-                                    status=status, stream=stream)
+        if token_rows:
+            # zigzag: each shard's rows are token runs; the kernel reads its
+            # queries and writes O and LSE by token index (no gather, no restore)
+            cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
+                                tiles=plan.tiles, num_tiles=plan.total_tiles, out=ws["o"],
+                                lse=ws["lse"], status=status, stream=stream)
+        else:
+            # attention of every shard; the store puts O and LSE in causal order
+            cpa.cp_attn_partial_restore(plan.segs, qc, k, v, w.scale, plan.gather_idx,
+                                        num_out_rows=N, num_segs=plan.total_segs,
+                                        tiles=plan.tiles, num_tiles=plan.total_tiles,
+                                        out=ws["o"], lse=ws["lse"], status=status,
+                                        stream=stream)
         if ev:
             ev[2].record(stream)
 
-    launches_per_step = 3 + 1 + 1   # plan (3 kernels), Q gather, attention (+ restore store)
+    launches_per_step = 3 + (0 if token_rows else 1) + 1  # plan, [Q gather], attention
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -349,8 +360,10 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config_of(w, {"parallelism": f"replicas{world}"}),
             "wall_ms_per_step": t_wall * 1e3 / args.steps,
-            "breakdown_ms": {"plan_and_q_gather": sum(prep_ms) / len(prep_ms),
-                             "attention_with_restore_store": attn_avg_ms},
+            "breakdown_ms": {("plan" if token_rows else "plan_and_q_gather"):
+                             sum(prep_ms) / len(prep_ms),
+                             ("attention_token_rows" if token_rows else
+                              "attention_with_restore_store"): attn_avg_ms},
             "roofline": {"kernel": kernel_label(w),
                          "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
@@ -744,8 +757,8 @@ def bench_e2e(args, w, inputs, dev, stream):
 def run_profile_case(args):
     """One kernel, small case, for ncu: 3 warm-up launches then one launch.
 
-    attention: the default workload's attention launch (all 8 shards, restore
-               fused into the store, as in the bench step).
+    attention: the workload's attention launch as in the bench step (zigzag:
+               queries and outputs by token index; else restore store).
     merge:     the heaviest query block of the 128K partial-KV workload
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
     merge4:    query block 3 of that workload (4 partials, 0.54 GB read; the
@@ -794,7 +807,12 @@ def run_profile_case(args):
         v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].to(dev)
         o, l = cpa.cp_attn_partial(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
                                    tiles=plan.tiles, num_tiles=plan.total_tiles)
-        if args.profile_case == "attention":
+        if args.profile_case == "attention" and w.strategies[0] == "zigzag":
+            q_tok = inputs["q"].to(dev)   # original order, read by token index
+            run = lambda: cpa.cp_attn_prefill(  # noqa: E731
+                plan.segs, q_tok, k, v, w.scale, num_segs=plan.total_segs, tiles=plan.tiles,
+                num_tiles=plan.total_tiles, out=o, lse=l, status=status)
+        elif args.profile_case == "attention":
             run = lambda: cpa.cp_attn_partial_restore(  # noqa: E731
                 plan.segs, q, k, v, w.scale, plan.gather_idx, num_out_rows=w.total_new,
                 num_segs=plan.total_segs, tiles=plan.tiles, num_tiles=plan.total_tiles, out=o,

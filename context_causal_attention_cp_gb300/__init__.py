@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     cp_attn_partial_accumulate,
     cp_attn_partial_kv,
     cp_attn_partial_restore,
+    cp_attn_prefill,
     cp_attn_split_kv,
     cp_lse_merge,
     cp_partial_kv_workspace_size,

@@ -43,6 +43,8 @@ SIGNATURES = {
     "cp_attn_partial": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32, i32,
                               i32, i32, i32, ctypes.c_float, i32, i32, vp, i32, vp, i32, i32,
                               vp, vp]),
+    "cp_attn_prefill": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32, i32,
+                              i32, i32, i32, ctypes.c_float, vp, i32, vp, vp, vp]),
     "cp_attn_partial_restore": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
                                       i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, vp,
                                       i32, vp, i32, vp, vp]),

@@ -232,6 +232,29 @@ def cp_attn_partial(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tile
     return out, lse
 
 
+def cp_attn_prefill(segs, q, k, v, scale, *, num_segs=None, tiles=None, num_tiles=None,
+                    out=None, lse=None, out_fp32=False, status=None, stream=None):
+    """Full-KV attention with q, O and LSE in original token order (segment
+    rows addressed by token index; every segment a consecutive token run,
+    e.g. a zigzag plan): the shard gather and the restore happen in the
+    kernel.  See cp_attn_prefill in cpattn.h."""
+    lib = L.load()
+    _check_qkv(q, k, v)
+    n, Hq, d = q.shape
+    Hkv, dv = v.shape[1], v.shape[2]
+    out, lse = _attn_outputs(out, lse, n, Hq, dv, out_fp32, q)
+    if out.shape[0] != n:
+        raise ValueError("out needs one row per token")
+    ns, nt = _segments(segs, num_segs, tiles, num_tiles, q)
+    _status(status, q)
+    L.check(lib.cp_attn_prefill(
+        _p(segs), ns, _p(tiles), nt, _p(q), n, _p(k), k.stride(0), k.stride(1), _p(v),
+        v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), _p(out),
+        1 if out.dtype == torch.float32 else 0, _p(lse), _p(status), _stream(stream)),
+        "cp_attn_prefill")
+    return out, lse
+
+
 def cp_attn_partial_restore(segs, q, k, v, scale, dst_rows, *, num_out_rows=None,
                             num_segs=None, tiles=None, num_tiles=None, kv_lo=0, kv_hi=-1,
                             out=None, lse=None, out_fp32=False, status=None, stream=None):
@@ -343,7 +366,9 @@ def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream
 
     ``fuse_restore``: the attention store writes original order directly
     (cp_attn_partial_restore with the plan's gather index) instead of a
-    separate cp_restore pass over O and LSE.
+    separate cp_restore pass over O and LSE; with a zigzag plan and q in
+    original order the kernel also reads the queries by token index
+    (cp_attn_prefill), so no gather runs either.
 
     q: bf16 [N, Hq, d] in original (flat) order, or already in cat order when
     ``q_is_cat``.  Returns (O [N, Hq, dv] bf16, LSE [N, Hq] fp32) in original order.
@@ -351,6 +376,11 @@ def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream
     N, Hq, _ = q.shape
     dv = v.shape[2]
     ws = workspace or {}
+    if fuse_restore and not q_is_cat and plan.strategy == L.ZIGZAG:
+        # zigzag segments are consecutive token runs: no gather, no restore pass
+        return cp_attn_prefill(plan.segs, q, k, v, scale, num_segs=plan.total_segs,
+                               tiles=plan.tiles, num_tiles=plan.total_tiles, out=ws.get("o"),
+                               lse=ws.get("lse"), status=status, stream=stream)
     q_cat = q if q_is_cat else cp_restore(q, plan.gather_idx[:N], out=ws.get("q_cat"),
                                           status=status, stream=stream)
     if fuse_restore:

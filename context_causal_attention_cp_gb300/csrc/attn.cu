@@ -590,6 +590,32 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
                      scale, prm, stream);
 }
 
+extern "C" int cp_attn_prefill(const cp_segment_t* segs_dev, int num_segs,
+                               const int32_t* tiles_dev, int num_tiles, const void* q,
+                               int num_tokens, const void* k, int64_t k_row_stride,
+                               int64_t k_head_stride, const void* v, int64_t v_row_stride,
+                               int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
+                               int dv, float scale, void* o, int o_is_fp32, float* lse,
+                               int32_t* status_dev, cudaStream_t stream) {
+  if (num_tokens < 0) return CPATTN_ERR_INVALID_ARG;
+  if (num_segs > 0 && (!o || !lse || num_tokens == 0)) return CPATTN_ERR_INVALID_ARG;
+  if (o && (!a16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))) return CPATTN_ERR_ALIGNMENT;
+  AttnParams prm{};
+  prm.kv_lo = 0;
+  prm.kv_hi = -1;
+  prm.o = o;
+  prm.o_f32 = o_is_fp32 ? 1 : 0;
+  prm.lse = lse;
+  prm.out_row_base = 0;
+  prm.num_out_rows = num_tokens;
+  prm.q_token_rows = 1;
+  prm.status = status_dev;
+  prm.split_block = 0;
+  return attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_tokens, k, k_row_stride,
+                     k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
+                     scale, prm, stream);
+}
+
 extern "C" int cp_attn_partial_restore(
     const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
     const void* q, int num_q_rows, const void* k, int64_t k_row_stride, int64_t k_head_stride,

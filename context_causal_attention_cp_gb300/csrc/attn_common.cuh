@@ -51,6 +51,11 @@ struct AttnParams {
   const int32_t* dst_rows;
   long long dst_limit;
   const float* lse_acc;
+  // q_token_rows: query and output rows are token (flat) indices: segment row
+  // i reads query row tok0 + i and writes output row tok0 + i (the shard
+  // gather and the restore both done by the kernel's own loads and stores);
+  // every segment must be a run of consecutive tokens (q_pos_step == 1).
+  int q_token_rows;
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).
@@ -159,8 +164,13 @@ __device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, 
     if (seg_id < 0) return false;
   }
   sg = p.segs[seg_id];
+  bool not_run = false;
+  if (p.q_token_rows) {  // rows of a consecutive token run, addressed by token index
+    not_run = sg.q_pos_step != 1;
+    sg.q_row0 = sg.tok0;
+  }
   const long long last_pos = (long long)sg.q_pos0 + (long long)(sg.q_len - 1) * sg.q_pos_step;
-  const bool bad = sg.q_len <= 0 || sg.q_row0 < 0 ||
+  const bool bad = not_run || sg.q_len <= 0 || sg.q_row0 < 0 ||
                    (long long)sg.q_row0 + sg.q_len > p.num_q_rows || sg.q_pos0 < 0 ||
                    sg.q_pos_step < 0 || sg.kv_row0 < 0 ||
                    (long long)sg.kv_row0 + sg.kv_len > p.num_kv_rows ||

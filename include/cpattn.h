@@ -167,6 +167,27 @@ int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const int32_t* t
                     int32_t* status_dev, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Full-KV CP attention in original token order.  [SGL-ZZ], [SGL-BE],
+ * [CPB-2.1]
+ *
+ * cp_attn_partial over the whole key range, with every segment row addressed
+ * by its token (flat) index: segment row i reads query row tok0 + i of q and
+ * writes output row tok0 + i of o and lse.  The shard gather of the queries
+ * and the restore of the outputs are thus done by the kernel's own loads and
+ * stores.  Every segment must be a run of consecutive tokens (q_pos_step == 1:
+ * the segments of a zigzag plan, or of any plan with cp_size 1); another one
+ * sets CPATTN_ERR_RANGE and is skipped.
+ *   q: bf16 [num_tokens, Hq, d] in original order; o: [num_tokens, Hq, dv]
+ *   bf16 or fp32; lse: fp32 [num_tokens, Hq].  Other arguments as in
+ *   cp_attn_partial. */
+int cp_attn_prefill(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
+                    int num_tiles, const void* q, int num_tokens, const void* k,
+                    int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                    int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
+                    int Hkv, int d, int dv, float scale, void* o, int o_is_fp32, float* lse,
+                    int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* cp_attn_partial with the restore fused into the store.  [CPB-2.1] (the
  * restore index after the all-gather), [SGL-BE]
  *

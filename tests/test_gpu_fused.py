@@ -257,3 +257,50 @@ def test_prefill_pipeline_mla_latent_view():
     pipe.synchronize()
     O_ref, L_ref = dense_ref(w, b)
     assert_attn_close(ho, hl, O_ref, L_ref, "mla/pipeline")
+
+
+# -------------------------------------------------- token-order prefill ----
+
+@pytest.mark.parametrize("name", ["single1k_d64", "varlen6_gqa", "llama8b_32k"])
+def test_token_rows_prefill_matches_gather_path(name):
+    """cp_attn_prefill (queries read and outputs written by token index, zigzag
+    plan) equals, bit for bit, the gather + attention with the restore store."""
+    w = W.WORKLOADS[name]
+    status, plan, inputs, q, k, v = setup(w, "zigzag")
+    N = w.total_new
+    o1, l1 = cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
+                                 tiles=plan.tiles, num_tiles=plan.total_tiles, status=status)
+    q_cat = cpa.cp_restore(q, plan.gather_idx[:N], status=status)
+    o2, l2 = cpa.cp_attn_partial_restore(plan.segs, q_cat, k, v, w.scale, plan.gather_idx,
+                                         num_out_rows=N, num_segs=plan.total_segs,
+                                         tiles=plan.tiles, num_tiles=plan.total_tiles,
+                                         status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, name)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_token_rows_prefill_mla_small():
+    w = mla_case([300, 77], [0, 40], 4, 3, 961)
+    status, plan, inputs, q, k, v = setup(w, "zigzag")
+    o, lse = cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
+                                 status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "mla token rows")
+    O_ref, L_ref = dense_ref(w, inputs)
+    assert_attn_close(o, lse, O_ref, L_ref, "mla token rows")
+
+
+def test_token_rows_prefill_refuses_strided_segments():
+    """Interleave segments (position step C > 1) are not token runs: their
+    tiles set CPATTN_ERR_RANGE and are skipped."""
+    w = W.WORKLOADS["varlen6_gqa"]
+    status, plan, inputs, q, k, v = setup(w, "interleave")
+    status.zero_()
+    out = torch.full((w.total_new, w.Hq, w.dv), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")
+    cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs, out=out,
+                        status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    assert torch.isnan(out).all()
