@@ -54,7 +54,10 @@ struct Cfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + NQ * kQTileBytes;
   static constexpr int kVOff = kKOff + KST * kKTileBytes;
-  static constexpr int kBarOff = kVOff + VST * kVTileBytes;
+  // epilogue staging: 32 rows x 128 bytes per softmax warp
+  static constexpr int kStageOff = kVOff + VST * kVTileBytes;
+  static constexpr int kStageBytes = 4 * NQ * 32 * 128;
+  static constexpr int kBarOff = kStageOff + kStageBytes;
   static constexpr int kNumBars = 1 + 2 * KST + 2 * VST + 3 * NQ + 1;
   // barriers, then TMEM slot, abort flag and two issued-load counters
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;  // + align slack
@@ -403,36 +406,60 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       } else {
+        // Plain store, staged per warp through shared memory: each thread
+        // puts 128 bytes of its row in the warp's 32-row buffer (16-byte
+        // chunks XOR-swizzled by row, so neither side has bank conflicts),
+        // then every store instruction writes 4 rows x 128 contiguous bytes.
+        uint8_t* stage = smem + C::kStageOff + warp * (32 * 128);
+        const int row_bytes = DV * (p.o_f32 ? 4 : 2);
+        for (int b0 = 0; b0 < row_bytes; b0 += 128) {
+          uint32_t pk[32];  // 128 bytes of this thread's row
+          if (p.o_f32) {
+            uint32_t r[32];
+            if (n_kv > 0) {
+              tmem_ld32(lane_addr + o_col + b0 / 4, r);
+              tmem_wait_ld();
+            } else {
 #pragma unroll
-        for (int q = 0; q < DV / 32; ++q) {
-          uint32_t r[32];
-          if (n_kv > 0) {
-            tmem_ld32(lane_addr + o_col + q * 32, r);
-            tmem_wait_ld();
+              for (int c = 0; c < 32; ++c) r[c] = 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = __float_as_uint(__uint_as_float(r[c]) * inv);
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = 0u;
-          }
-          if (out_row >= 0) {
-            float v[32];
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t r[32];
+              if (n_kv > 0) {
+                tmem_ld32(lane_addr + o_col + b0 / 2 + hh * 32, r);
+                tmem_wait_ld();
+              } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * inv;
-            const long long off = (out_row * p.Hq + h) * DV + q * 32;
-            if (p.o_f32) {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
+                for (int c = 0; c < 32; ++c) r[c] = 0u;
+              }
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
-                                    pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                                    pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                                    pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+              for (int c = 0; c < 16; ++c)
+                pk[hh * 16 + c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv,
+                                              __uint_as_float(r[2 * c + 1]) * inv);
             }
           }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+            const long long orr = __shfl_sync(0xffffffffu, out_row, rr);
+            const uint4 val =
+                *reinterpret_cast<const uint4*>(stage + rr * 128 + ((ch ^ (rr & 7)) * 16));
+            if (orr >= 0) {
+              uint8_t* dst = reinterpret_cast<uint8_t*>(p.o) + (orr * p.Hq + h) * row_bytes +
+                             b0 + ch * 16;
+              *reinterpret_cast<uint4*>(dst) = val;
+            }
+          }
+          __syncwarp();
         }
       }
       if (out_row >= 0) p.lse[out_row * p.Hq + h] = mc.lse;
