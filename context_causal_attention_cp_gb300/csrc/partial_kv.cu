@@ -418,9 +418,12 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                                   float* lse_out, int num_out_rows, void* workspace,
                                   int64_t workspace_bytes, int32_t* status_dev,
                                   cudaStream_t stream) {
-  if (num_segs < 0 || kv_block < 1 || max_blocks < 1 || max_blocks > 32 || num_out_rows < 0)
+  if (num_segs < 0 || kv_block < 1 || max_blocks < 0 || max_blocks > 32 || num_out_rows < 0)
     return CPATTN_ERR_INVALID_ARG;
+  // no segments (a batch without new tokens): nothing to compute; the sizing
+  // calls report max_blocks = 0 for it
   if (num_segs == 0) return CPATTN_OK;
+  if (max_blocks < 1) return CPATTN_ERR_INVALID_ARG;
   if (!o_out || !workspace || num_out_rows == 0 || Hq < 1 || dv < 4) return CPATTN_ERR_INVALID_ARG;
   if (!a16(o_out) || !a16(workspace) || (reinterpret_cast<uintptr_t>(lse_out) & 3u) ||
       (reinterpret_cast<uintptr_t>(dst_rows) & 3u))

@@ -279,6 +279,9 @@ int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, i
  *   Arguments shared with cp_attn_partial keep its meaning.
  *   kv_block > 0; max_blocks: an upper bound on the blocks any segment sees,
  *     1 <= max_blocks <= 32 (a segment with more sets CPATTN_ERR_INVALID_ARG).
+ *     With num_segs == 0 the call does nothing and returns CPATTN_OK, and
+ *     max_blocks may be 0 (what the sizing calls report for a batch without
+ *     new tokens).
  *   dst_rows: nullable, [num_q_rows] output row of each cat row.
  *   o_out: [num_out_rows, Hq, dv] bf16 or fp32; lse_out fp32 [num_out_rows, Hq]
  *     (nullable).

@@ -90,6 +90,15 @@ def test_invalid_arguments_are_rejected_on_host():
     assert lib.cp_partial_kv_workspace_size(one, zero, 1, 2, 0, 256, 8, 128, ctypes.byref(nbytes),
                                             ctypes.byref(mb)) == L.OK
     assert mb.value == 4
+    # a batch without new tokens: max_blocks 0, and the call is a no-op
+    assert lib.cp_partial_kv_workspace_size(zero, one, 1, 2, 0, 256, 8, 128, ctypes.byref(nbytes),
+                                            ctypes.byref(mb)) == L.OK
+    assert mb.value == 0
+    empty = [fake[0], 0] + args[2:]
+    assert lib.cp_attn_partial_kv(*empty, 8, 4, 128, 128, 0.1, 64, 0, nul, nul, 0, nul, 0,
+                                  nul, 0, nul, nul) == L.OK
+    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 0, nul, o, 0, lse, 128,
+                                  fake[1], 1 << 20, nul, nul) == L.ERR_INVALID_ARG
     # merge: part count and dv limits
     assert lib.cp_lse_merge(nul, nul, 0, 0, 0, 4, 2, 128, nul, nul, 1, nul, 4, nul,
                             nul) == L.ERR_INVALID_ARG

@@ -304,3 +304,27 @@ def test_token_rows_prefill_refuses_strided_segments():
     torch.cuda.synchronize()
     assert int(status.item()) == -6
     assert torch.isnan(out).all()
+
+
+# ------------------------------------------------------------ empty batch ----
+
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_batch_without_new_tokens_is_a_no_op(strategy):
+    """Requests with a cached prefix but no new tokens: every path returns
+    empty outputs and a clean status, and launches nothing that could read
+    the empty query buffer."""
+    w = W.Workload(name="empty", new_lens=[0, 0], prefix_lens=[5, 0], Hq=4, Hkv=2, d=128,
+                   dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=2,
+                   strategies=[strategy], seed=17, kv_block=64)
+    status, plan, _, q, k, v = setup(w, strategy)
+    assert q.shape[0] == 0 and plan.total_segs == 0
+    outs = [cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=status, fuse_restore=f)
+            for f in (False, True)]
+    o, lse, _ = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
+                                       prefix_lens=w.prefix_lens, status=status)
+    outs.append((o, lse))
+    outs.append(cpa.cp_pass_q_attention(q, k, v, plan, w.scale, status=status))
+    torch.cuda.synchronize()
+    cpa.check_status(status, "empty batch")
+    for o, lse in outs:
+        assert tuple(o.shape) == (0, w.Hq, w.dv) and tuple(lse.shape) == (0, w.Hq)
