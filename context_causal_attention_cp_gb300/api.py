@@ -14,6 +14,7 @@ from dataclasses import dataclass
 from typing import List, Optional, Sequence
 
 import ctypes
+import math
 import torch
 
 from . import _lib as L
@@ -348,7 +349,7 @@ def cp_restore(src, idx, *, out=None, status=None, stream=None):
     if idx.dim() != 1:
         raise ValueError("idx must be a 1-D int32 index")
     rows = idx.shape[0]
-    row_bytes = src[0].numel() * src.element_size() if src.shape[0] > 0 else 0
+    row_bytes = math.prod(src.shape[1:]) * src.element_size()
     if out is None:
         out = torch.empty((rows,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
     _dev(out, "out", src.dtype, src)

@@ -227,6 +227,26 @@ def test_restore_is_exact():
     assert torch.equal(out, src[idx.long()])
     lse = torch.randn(1000, 4, generator=g).cuda()
     assert torch.equal(cpa.cp_restore(lse, idx), lse[idx.long()])
+    # row sizes around the warp-per-row path (>= 32 16-byte chunks): ragged
+    # chunk counts, more chunks than one pass of a warp, 4-byte rows
+    for rows, cols, dt in [(37, 264, torch.bfloat16), (1003, 300, torch.float32),
+                           (9, 4800, torch.bfloat16), (77, 31, torch.float32),
+                           (130, 3, torch.float32)]:
+        src = torch.randn(rows, cols, generator=g).to(dt).cuda()
+        idx = torch.randint(0, rows, (rows,), generator=g, dtype=torch.int32).cuda()
+        assert torch.equal(cpa.cp_restore(src, idx), src[idx.long()]), (rows, cols, dt)
+
+
+def test_restore_bad_index_sets_range():
+    src = torch.zeros(64, 256, dtype=torch.float32, device="cuda")
+    idx = torch.arange(64, dtype=torch.int32, device="cuda")
+    idx[5] = 64
+    status = cpa.new_status()
+    out = torch.full_like(src, 7.0)
+    cpa.cp_restore(src, idx, out=out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6
+    assert torch.all(out[5] == 7.0) and torch.all(out[:5] == 0) and torch.all(out[6:] == 0)
 
 
 def test_bad_segment_sets_range_status():
