@@ -557,9 +557,10 @@ def bench_partial_kv(args, dev, stream, pk):
 def bench_pass_q(args, dev, stream, pk):
     """The same 128K workload through the pass-Q ring (KV resident in 2C
     blocks per rank, each query shard carried round the ring with an fp32
-    accumulator, one accumulate launch per (hop, rank, KV block)); the
-    pass-KV figure is the partial_kv entry.  Step = plan + query gather + the
-    ring + restore of O and LSE to causal order."""
+    accumulator; one accumulate launch per (hop, resident block) covers all
+    ranks, each segment with its own key window); the pass-KV figure is the
+    partial_kv entry.  Step = plan + query gather + the ring + restore of O
+    and LSE to causal order."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -615,8 +616,8 @@ def bench_pass_q(args, dev, stream, pk):
             "launches": (3 + 1 + len(sched) + 2) * (reps + 3),
             "selector_message_rule": choice,
             "path": "cp_shard_plan + cp_restore + cp_pass_q_attention (one "
-                    "cp_attn_partial_accumulate per hop, rank and resident KV block) + "
-                    "cp_restore of O and LSE"}
+                    "cp_attn_partial_accumulate per hop and resident KV block, all ranks "
+                    "in one launch with per-segment key windows) + cp_restore of O and LSE"}
 
 
 def bench_merge_sweep(args, dev, stream, pk):

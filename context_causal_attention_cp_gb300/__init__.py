@@ -7,6 +7,7 @@ absence raises: there is no CPU fallback.
 """
 
 from .api import (  # noqa: F401
+    PassQLaunch,
     PrefillPipeline,
     ShardPlan,
     alloc_plan,

@@ -50,7 +50,7 @@ SIGNATURES = {
                                       i32, vp, i32, vp, vp]),
     "cp_attn_partial_accumulate": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
                                          i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
-                                         vp, vp, i32, i32, vp, vp]),
+                                         vp, vp, vp, i32, i32, vp, vp]),
     "cp_select_pass": (i32, [ctypes.c_int64, ctypes.c_int64, i32, i32, i32,
                              ctypes.POINTER(ctypes.c_double)]),
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),

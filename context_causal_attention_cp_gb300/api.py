@@ -280,9 +280,13 @@ def cp_attn_partial_restore(segs, q, k, v, scale, dst_rows, *, num_out_rows=None
 
 
 def cp_attn_partial_accumulate(segs, q, k, v, scale, o_acc, lse_acc, lse_out, *, num_segs=None,
-                               tiles=None, num_tiles=None, kv_lo=0, kv_hi=-1, out_row_base=0,
-                               status=None, stream=None):
-    """One pass-Q hop: merge this window's partial into (o_acc, lse_acc) -> (o_acc, lse_out)."""
+                               tiles=None, num_tiles=None, kv_lo=0, kv_hi=-1, seg_windows=None,
+                               out_row_base=0, status=None, stream=None):
+    """One pass-Q hop: merge this window's partial into (o_acc, lse_acc) -> (o_acc, lse_out).
+
+    ``seg_windows``: optional int32 [num_segs, 2] on the device; segment s
+    then uses key window [lo, hi) = seg_windows[s] in place of (kv_lo, kv_hi).
+    """
     lib = L.load()
     _check_qkv(q, k, v)
     rows, Hq, d = q.shape
@@ -295,12 +299,16 @@ def cp_attn_partial_accumulate(segs, q, k, v, scale, o_acc, lse_acc, lse_out, *,
     _shape(lse_acc, "lse_acc", (o_acc.shape[0], Hq))
     _shape(lse_out, "lse_out", (o_acc.shape[0], Hq))
     ns, nt = _segments(segs, num_segs, tiles, num_tiles, q)
+    if seg_windows is not None:
+        _dev(seg_windows, "seg_windows", torch.int32, q)
+        if seg_windows.dim() != 2 or seg_windows.shape[1] != 2 or seg_windows.shape[0] < ns:
+            raise ValueError("seg_windows must be int32 [num_segs, 2]")
     _status(status, q)
     L.check(lib.cp_attn_partial_accumulate(
         _p(segs), ns, _p(tiles), nt, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v),
         v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_lo),
-        int(kv_hi), _p(o_acc), _p(lse_acc), _p(lse_out), int(out_row_base), o_acc.shape[0],
-        _p(status), _stream(stream)), "cp_attn_partial_accumulate")
+        int(kv_hi), _p(seg_windows), _p(o_acc), _p(lse_acc), _p(lse_out), int(out_row_base),
+        o_acc.shape[0], _p(status), _stream(stream)), "cp_attn_partial_accumulate")
     return o_acc, lse_out
 
 
@@ -643,46 +651,58 @@ def pass_q_kv_blocks(kv_total: int, cp_size: int):
             for r in range(cp_size)]
 
 
-def pass_q_schedule(plan: ShardPlan, segs_host=None):
-    """Host schedule of the pass-Q ring: one entry per accumulate call.
+@dataclass
+class PassQLaunch:
+    """One accumulate launch of the pass-Q ring: at ring hop ``hop`` every
+    rank merges the query shard visiting it against resident block ``block``
+    of its KV (0: block r of the request's 2C, 1: block 2C-1-r; see
+    pass_q_kv_blocks).  ``segs`` holds copies of the plan's segment rows that
+    see that block (int32 [n, 8]), ``windows`` their key windows (int32
+    [n, 2]), ``seg_ids`` their indices in the plan."""
+    hop: int
+    block: int
+    segs: torch.Tensor
+    windows: torch.Tensor
+    seg_ids: List[int]
 
-    Entry (hop, rank, seg_begin, seg_end, lo, hi, row_begin, row_end): at
-    ring hop ``hop`` rank ``rank`` merges the visiting query shard's segments
-    [seg_begin, seg_end) (one request's segments of the shard of rank
-    (rank - hop) mod C, cat rows [row_begin, row_end)) against its resident
-    KV block [lo, hi) (key positions, see pass_q_kv_blocks).  Blocks that no
-    row of the visiting segments can see are left out.
+
+def pass_q_schedule(plan: ShardPlan, segs_host=None) -> List[PassQLaunch]:
+    """Host schedule of the pass-Q ring: one launch per (hop, resident block).
+
+    At hop s the shard of rank q visits rank (q + s) mod C.  Each launch
+    takes every segment of every shard, with the key window of its host
+    rank's block for the segment's request; a segment that cannot see the
+    block (the block is empty or starts after the segment's last position)
+    is left out.  All windows of one launch belong to different rows, so one
+    launch merges every rank's hop at once: at most 2C launches for any
+    batch.  The segment copies are taken from the plan as it is now: build
+    the schedule again after re-planning a different batch.
     """
     C = plan.cp_size
     segs_host = segs_host or segments_host(plan)
     new_lens = plan.new_lens_dev.cpu().tolist()[: plan.num_reqs]
     prefix_lens = plan.prefix_lens_dev.cpu().tolist()[: plan.num_reqs]
     blocks = [pass_q_kv_blocks(p + n, C) for n, p in zip(new_lens, prefix_lens)]
-    first = [0]
-    for c in plan.segs_per_rank:
-        first.append(first[-1] + c)
-    groups = []   # per rank: [req, seg_begin, seg_end, last position, row_begin, row_end]
-    for qr in range(C):
-        g = []
-        for i in range(first[qr], first[qr + 1]):
-            sg = segs_host[i]
-            last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
-            end = sg["q_row0"] + sg["q_len"]
-            if g and g[-1][0] == sg["req"]:
-                g[-1][2] = i + 1
-                g[-1][3] = max(g[-1][3], last)
-                g[-1][5] = end
-            else:
-                g.append([sg["req"], i, i + 1, last, sg["q_row0"], end])
-        groups.append(g)
-    sched = []
+    shard_of = []
+    for r, c in enumerate(plan.segs_per_rank):
+        shard_of += [r] * c
+    raw = plan.segs[: plan.total_segs].cpu()
+    dev = plan.segs.device
+    launches = []
     for hop in range(C):
-        for r in range(C):
-            for req, i0, i1, last, r0, r1 in groups[(r - hop) % C]:
-                for lo, hi in blocks[req][r]:
-                    if hi > lo and lo <= last:
-                        sched.append((hop, r, i0, i1, lo, hi, r0, r1))
-    return sched
+        for b in (0, 1):
+            ids, wins = [], []
+            for i, sg in enumerate(segs_host):
+                lo, hi = blocks[sg["req"]][(shard_of[i] + hop) % C][b]
+                last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
+                if hi > lo and lo <= last:
+                    ids.append(i)
+                    wins.append((lo, hi))
+            if ids:
+                launches.append(PassQLaunch(
+                    hop=hop, block=b, segs=raw[ids].contiguous().to(dev),
+                    windows=torch.tensor(wins, dtype=torch.int32).to(dev), seg_ids=ids))
+    return launches
 
 
 def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, schedule=None, status=None,
@@ -693,8 +713,10 @@ def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, schedule=None, s
     rank's query shard travels round the ring with an fp32 accumulator
     (O_acc, L_acc) that starts empty (0, -inf); at hop s rank r merges the
     partial of the visiting shard (of rank (r - s) mod C) against its own KV
-    blocks into that accumulator (one cp_attn_partial_accumulate per entry of
-    pass_q_schedule).  After C hops every accumulator is the exact result.
+    blocks into that accumulator.  One cp_attn_partial_accumulate per launch
+    of pass_q_schedule covers every rank of a hop for one of its two blocks,
+    each segment with its own key window.  After C hops every accumulator is
+    the exact result.
     ``out``: optional (O_acc fp32 [N, Hq, dv], LSE [N, Hq], LSE scratch [N, Hq]).
     Returns (O fp32 [N, Hq, dv], LSE [N, Hq]) in cat order.
     """
@@ -712,10 +734,11 @@ def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, schedule=None, s
         o_acc.zero_()
         lse_a.fill_(float("-inf"))
         lse_b.fill_(float("-inf"))
-        for _, _, i0, i1, lo, hi, r0, r1 in sched:
-            cp_attn_partial_accumulate(plan.segs[i0:i1], q_cat, k, v, scale, o_acc, lse_a, lse_b,
-                                       kv_lo=lo, kv_hi=hi, status=status, stream=stream)
-            lse_a[r0:r1].copy_(lse_b[r0:r1])  # the rows this call wrote; buffers stay equal
+        for launch in sched:
+            cp_attn_partial_accumulate(launch.segs, q_cat, k, v, scale, o_acc, lse_a, lse_b,
+                                       seg_windows=launch.windows, status=status, stream=stream)
+            # rows outside the launch hold equal values in both buffers
+            lse_a.copy_(lse_b)
     return o_acc[:N], lse_a[:N]
 
 

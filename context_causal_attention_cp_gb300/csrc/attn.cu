@@ -674,9 +674,11 @@ extern "C" int cp_attn_partial_accumulate(
     const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
     const void* q, int num_q_rows, const void* k, int64_t k_row_stride, int64_t k_head_stride,
     const void* v, int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
-    int d, int dv, float scale, int kv_lo, int kv_hi, float* o_acc, const float* lse_acc,
-    float* lse_out, int out_row_base, int num_out_rows, int32_t* status_dev, cudaStream_t stream) {
+    int d, int dv, float scale, int kv_lo, int kv_hi, const int32_t* seg_windows_dev,
+    float* o_acc, const float* lse_acc, float* lse_out, int out_row_base, int num_out_rows,
+    int32_t* status_dev, cudaStream_t stream) {
   if (num_out_rows < 0 || Hq <= 0) return CPATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(seg_windows_dev) & 3u) return CPATTN_ERR_ALIGNMENT;
   if (num_segs > 0 && (!o_acc || !lse_acc || !lse_out || num_out_rows == 0))
     return CPATTN_ERR_INVALID_ARG;
   if (o_acc && (!a16(o_acc) || (reinterpret_cast<uintptr_t>(lse_acc) & 3u) ||
@@ -695,6 +697,7 @@ extern "C" int cp_attn_partial_accumulate(
   prm.o_f32 = 1;
   prm.lse = lse_out;
   prm.lse_acc = lse_acc;
+  prm.seg_windows = seg_windows_dev;
   prm.out_row_base = out_row_base;
   prm.num_out_rows = num_out_rows;
   prm.status = status_dev;

@@ -56,6 +56,11 @@ struct AttnParams {
   // gather and the restore both done by the kernel's own loads and stores);
   // every segment must be a run of consecutive tokens (q_pos_step == 1).
   int q_token_rows;
+  // seg_windows (normal mode): when set, segment s uses the key window
+  // [seg_windows[2s], seg_windows[2s+1]) in place of the call's kv_lo / kv_hi
+  // (an upper end < 0 is unbounded), so that one launch can merge every
+  // segment against its own resident KV block (the pass-Q ring hop).
+  const int32_t* seg_windows;
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).
@@ -185,14 +190,20 @@ __device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, 
 }
 
 // The key window and output placement of this CTA.  Normal mode: the call's
-// window, output row = cat row - out_row_base.  Split-KV mode: block j of the
+// window (or the segment's own, with seg_windows), output row = cat row -
+// out_row_base.  Split-KV mode: block j of the
 // segment's keys, output row = ws_slot[seg] + j * q_len + row-in-segment.
 // Returns false when the CTA has no block to do (or its slot is out of range).
 __device__ __forceinline__ bool split_window(const AttnParams& p, const cp_segment_t& sg, int seg_id,
                                              int j, int& kv_lo, int& kv_hi, long long& out_row0) {
   if (p.split_block <= 0) {
-    kv_lo = p.kv_lo;
-    kv_hi = p.kv_hi;
+    if (p.seg_windows) {
+      kv_lo = __ldg(p.seg_windows + 2 * seg_id);
+      kv_hi = __ldg(p.seg_windows + 2 * seg_id + 1);
+    } else {
+      kv_lo = p.kv_lo;
+      kv_hi = p.kv_hi;
+    }
     out_row0 = (long long)sg.q_row0 - p.out_row_base;  // output row of segment row 0
     return true;
   }

@@ -222,6 +222,12 @@ int cp_attn_partial_restore(const cp_segment_t* segs_dev, int num_segs, const in
  * at O = 0, L = -inf (the identity) and goes through hops whose windows
  * partition the keys ends equal to cp_attn_partial over all keys.
  *   Arguments shared with cp_attn_partial keep its meaning.
+ *   seg_windows_dev: nullable int32 [num_segs][2] on the device, 4-byte
+ *     aligned.  When set, segment s uses its own key window
+ *     [seg_windows_dev[2s], seg_windows_dev[2s+1]) (upper end < 0:
+ *     unbounded) and kv_lo / kv_hi are ignored, so that one launch can
+ *     merge every visiting shard against its own rank's resident KV block
+ *     (one launch per ring hop and block instead of one per rank).
  *   o_acc: fp32 [num_out_rows, Hq, dv], read and overwritten in place.
  *   lse_acc: fp32 [num_out_rows, Hq] read; lse_out: fp32 [num_out_rows, Hq]
  *     written.  The two must not overlap (CPATTN_ERR_INVALID_ARG): a hop
@@ -233,7 +239,8 @@ int cp_attn_partial_accumulate(const cp_segment_t* segs_dev, int num_segs,
                                int num_q_rows, const void* k, int64_t k_row_stride,
                                int64_t k_head_stride, const void* v, int64_t v_row_stride,
                                int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
-                               int dv, float scale, int kv_lo, int kv_hi, float* o_acc,
+                               int dv, float scale, int kv_lo, int kv_hi,
+                               const int32_t* seg_windows_dev, float* o_acc,
                                const float* lse_acc, float* lse_out, int out_row_base,
                                int num_out_rows, int32_t* status_dev, cudaStream_t stream);
 

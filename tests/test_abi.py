@@ -134,19 +134,24 @@ def test_restore_and_accumulate_calls_validate_on_host():
     # accumulate: the two LSE buffers (128 rows x 8 heads x 4 B = 4096 B) must not overlap
     la = 0x80000
     for lb in (la, la + 16, la + 4092, la - 4092):
-        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, o,
+        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, nul, o,
                                               ctypes.c_void_p(la), ctypes.c_void_p(lb), 0, 128,
                                               nul, nul) == L.ERR_INVALID_ARG, hex(lb)
     # adjacent buffers are fine (the call then fails on the unsupported shape)
     for lb in (la + 4096, la - 4096):
-        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 96, 96, 0.1, 0, -1, o,
+        assert lib.cp_attn_partial_accumulate(*args, 8, 4, 96, 96, 0.1, 0, -1, nul, o,
                                               ctypes.c_void_p(la), ctypes.c_void_p(lb), 0, 128,
                                               nul, nul) == L.ERR_UNSUPPORTED, hex(lb)
-    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, nul,
+    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, nul, nul,
                                           ctypes.c_void_p(la), ctypes.c_void_p(la + 8192), 0,
                                           128, nul, nul) == L.ERR_INVALID_ARG
-    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1,
+    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1, nul,
                                           ctypes.c_void_p(0x40004), ctypes.c_void_p(la),
+                                          ctypes.c_void_p(la + 8192), 0, 128, nul,
+                                          nul) == L.ERR_ALIGNMENT
+    # per-segment windows must be int32-aligned
+    assert lib.cp_attn_partial_accumulate(*args, 8, 4, 128, 128, 0.1, 0, -1,
+                                          ctypes.c_void_p(0x50002), o, ctypes.c_void_p(la),
                                           ctypes.c_void_p(la + 8192), 0, 128, nul,
                                           nul) == L.ERR_ALIGNMENT
 

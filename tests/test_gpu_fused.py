@@ -155,6 +155,42 @@ def test_accumulate_merges_into_carried_partial(shape):
     assert torch.equal(la.cpu(), l0)  # the input LSE is only read
 
 
+@pytest.mark.parametrize("shape", [(32, 8, 128), (4, 1, 576)])
+def test_accumulate_per_segment_windows_match_single_calls(shape):
+    """Per-segment key windows (one launch) give bit for bit what one call per
+    segment with that window gives, including empty and unbounded windows."""
+    Hq, Hkv, d = shape
+    mla = d == 576
+    dv = 512 if mla else d
+    w = W.Workload(name=f"win{d}", new_lens=[517, 33, 1000, 3], prefix_lens=[0, 17, 256, 5],
+                   Hq=Hq, Hkv=Hkv, d=d, dv=dv, scale=1 / math.sqrt(192 if mla else d),
+                   std=0.1 if mla else 1.0, cp_size=3, strategies=["zigzag"], seed=1301 + d,
+                   v_is_k_prefix=mla)
+    status, plan, inputs, q, k, v = setup(w, "zigzag")
+    N = w.total_new
+    q_cat = cpa.cp_restore(q, plan.gather_idx[:N])
+    S = plan.total_segs
+    gen = torch.Generator().manual_seed(77 + d)
+    lo = torch.randint(0, 600, (S,), generator=gen, dtype=torch.int32)
+    hi = lo + torch.randint(0, 700, (S,), generator=gen, dtype=torch.int32)
+    hi[::5] = -1                       # unbounded
+    lo[1::7] = 2000                    # past every row: empty window
+    wins = torch.stack([lo, hi], 1).contiguous()
+    o0 = torch.randn((N, Hq, dv), generator=gen, dtype=torch.float32)
+    l0 = torch.randn((N, Hq), generator=gen, dtype=torch.float32)
+    o_a, la, lb = o0.cuda(), l0.cuda(), torch.full((N, Hq), float("nan"), device="cuda")
+    cpa.cp_attn_partial_accumulate(plan.segs, q_cat, k, v, w.scale, o_a, la, lb, num_segs=S,
+                                   seg_windows=wins.cuda(), status=status)
+    o_b, lc, ld = o0.cuda(), l0.cuda(), torch.full((N, Hq), float("nan"), device="cuda")
+    for i in range(S):
+        cpa.cp_attn_partial_accumulate(plan.segs[i:i + 1], q_cat, k, v, w.scale, o_b, lc, ld,
+                                       kv_lo=int(lo[i]), kv_hi=int(hi[i]), status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, w.name)
+    assert torch.equal(o_a, o_b)
+    assert torch.equal(lb, ld)
+
+
 def test_accumulate_refuses_overlapping_lse():
     w = W.WORKLOADS["single1k_d64"]
     status, plan, inputs, q, k, v = setup(w, "zigzag")
