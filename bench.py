@@ -37,6 +37,7 @@ METRIC = "causal CP-prefill attention TFLOPS & % of GB300 bf16 peak; LSE-merge G
 UNIT = "TFLOP/s"
 WORKLOAD = "llama8b_32k"
 MERGE_WORKLOAD = "partialkv_128k"
+DECODE_KV_BLOCK = 4096  # keys per CTA in the decode step (2 blocks per rank)
 # ncu summary under profiles/ holding the attention kernel's DRAM bytes per launch
 PROFILE_MD = {"llama8b_32k": "attn_fwd_llama8b_32k.md", "mla_16k": "attn_mla_mla_16k.md"}
 
@@ -622,12 +623,16 @@ def bench_pass_q(args, dev, stream, pk):
 
 def bench_merge_sweep(args, dev, stream, pk):
     """Decode-style merge sweep: 64 single-token queries x 32 heads over 65536
-    keys, key i resident on shard i mod 8 (a strided view of the KV, no copy).
-    The decode step is, per shard, a split-KV partial (cp_attn_split_kv: keys
-    in blocks of 512 over separate CTAs, merged in the library) and then one
-    LSE merge of the 8 shard partials; the merge alone (8 partials, 9.5 MB,
-    L2-sized) is reported both warm (launches queued behind a GPU sleep, run
-    back to back) and with L2 flushed before each call."""
+    keys, key i resident on shard i mod 8.  Each rank's KV cache holds its
+    tokens contiguously (laid out once before timing, as a KV cache is) and
+    every rank holds all decode queries.  The decode step is one
+    cp_attn_split_kv call over the 8 ranks' segments (each rank's keys in
+    blocks of DECODE_KV_BLOCK over separate CTAs, merged per rank in the
+    library: 8 shard partials) and then one LSE merge of the 8 partials.  The
+    same step with one call per rank on strided views of the original-order
+    KV is reported beside it.  The merge alone (8 partials, 9.5 MB, L2-sized)
+    is reported both warm (launches queued behind a GPU sleep, run back to
+    back) and with L2 flushed before each call."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -656,26 +661,50 @@ def bench_merge_sweep(args, dev, stream, pk):
     ws = cpa.cp_attn_split_kv(seg, q, k[0::S], v[0::S], m["scale"], 512, segs_host=seg_host,
                               out=po[0], lse_out=pl[0], status=status, stream=stream)[2]
 
-    def decode_step():
+    def decode_step_per_rank():
         for j in range(S):
             cpa.cp_attn_split_kv(seg, q, k[j::S], v[j::S], m["scale"], 512, segs_host=seg_host,
                                  out=po[j], lse_out=pl[j], workspace=ws, status=status,
                                  stream=stream)
         merge()
 
-    for _ in range(5):
-        decode_step()
-    torch.cuda.synchronize(dev)
+    # each rank's KV cache: its interleaved tokens, contiguous; every rank
+    # holds all decode queries
+    Hkv, d = k.shape[1], k.shape[2]
+    k_rank = k.view(n_kv, S, Hkv, d).transpose(0, 1).contiguous().view(S * n_kv, Hkv, d)
+    v_rank = v.view(n_kv, S, Hkv, dv).transpose(0, 1).contiguous().view(S * n_kv, Hkv, dv)
+    q_rank = q.repeat(S, 1, 1).contiguous()
+    segs_all_host = torch.tensor([[j * nq, nq, n_kv - 1, 0, j * n_kv, n_kv, j * nq, j]
+                                  for j in range(S)], dtype=torch.int32)
+    segs_all = segs_all_host.to(dev)
+    po_rows, pl_rows = po.view(S * nq, Hq, dv), pl.view(S * nq, Hq)
+    ws_all = cpa.cp_attn_split_kv(segs_all, q_rank, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
+                                  segs_host=segs_all_host, out=po_rows, lse_out=pl_rows,
+                                  status=status, stream=stream)[2]
+
+    def decode_step():
+        cpa.cp_attn_split_kv(segs_all, q_rank, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
+                             segs_host=segs_all_host, out=po_rows, lse_out=pl_rows,
+                             workspace=ws_all, status=status, stream=stream)
+        merge()
+
+    def time_steps(fn, reps=50):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = E(), E()
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(300_000_000)  # let the host queue the launches ahead of the GPU
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    per_rank_us = time_steps(decode_step_per_rank)
+    step_us = time_steps(decode_step)
     reps = 50
-    e0, e1 = E(), E()
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(300_000_000)  # let the host queue the launches ahead of the GPU
-    e0.record(stream)
-    for _ in range(reps):
-        decode_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    step_us = e0.elapsed_time(e1) * 1e3 / reps
     with torch.cuda.stream(stream):
         torch.cuda._sleep(50_000_000)
     e0.record(stream)
@@ -696,17 +725,21 @@ def bench_merge_sweep(args, dev, stream, pk):
     cpa.check_status(status, "merge sweep")
     cold_us = sorted(x.elapsed_time(y) for x, y in cold)[len(cold) // 2] * 1e3
     nbytes = S * nq * Hq * (dv + 1) * 4 + nq * Hq * (dv + 1) * 4
-    launches = (3 * S + 1) * (reps + 6) + reps + 20
+    # both steps: one sizing call + 5 warm-up + 50 timed; then the merge alone
+    launches = 3 + (3 * S + 1) * 55 + 3 + 4 * 55 + reps + 20
     del q, k, v, po, pl, flush
     torch.cuda.empty_cache()
     return {"queries": nq, "heads": Hq, "kv_tokens": m["kv_tokens"], "shards": S,
-            "decode_step_us": step_us, "merge_bytes": nbytes,
+            "decode_step_us": step_us, "decode_kv_block": DECODE_KV_BLOCK,
+            "decode_step_per_rank_calls_us": per_rank_us, "merge_bytes": nbytes,
             "merge_warm_us": warm_us, "merge_warm_gbs": nbytes / (warm_us * 1e-6) / 1e9,
             "merge_flushed_us": cold_us, "merge_flushed_gbs": nbytes / (cold_us * 1e-6) / 1e9,
             "merge_flushed_frac_of_hbm": nbytes / (cold_us * 1e-6) / 1e9 / pk["hbm_gbs"],
             "launches": launches,
-            "path": "8 x cp_attn_split_kv (kv blocks of 512) over strided KV views + "
-                    "cp_lse_merge (8 partials)"}
+            "path": "one cp_attn_split_kv over the 8 ranks' segments (each rank's KV cache "
+                    "contiguous, keys in blocks of DECODE_KV_BLOCK, merged per rank) + "
+                    "cp_lse_merge (8 partials); per_rank_calls: 8 cp_attn_split_kv calls "
+                    "(blocks of 512) on strided views of the original-order KV"}
 
 
 def bench_e2e(args, w, inputs, dev, stream):

@@ -517,3 +517,40 @@ def test_decode_sweep_split_kv(kv_block):
     O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
                                          m["scale"], np.arange(m["kv_tokens"]))
     assert_attn_close(out, lse, O_ref, L_ref, f"decode split {kv_block}")
+
+
+@pytest.mark.parametrize("kv_block", [512, 4096])
+def test_decode_one_call_over_all_ranks(kv_block):
+    """The decode step as the bench times it: each rank's KV cache holds its
+    interleaved tokens contiguously, every rank holds all queries, and one
+    cp_attn_split_kv call over the 8 ranks' segments gives the 8 shard
+    partials, bit-identical to one call per rank on strided views; their
+    merge equals attention over all 65536 keys."""
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q, k, v = inputs["q"].cuda(), inputs["k"].cuda(), inputs["v"].cuda()
+    S, nq, Hq, dv = m["shards"], m["queries"], m["Hq"], m["dv"]
+    n_kv = m["kv_tokens"] // S
+    Hkv, d = k.shape[1], k.shape[2]
+    k_rank = k.view(n_kv, S, Hkv, d).transpose(0, 1).contiguous().view(S * n_kv, Hkv, d)
+    v_rank = v.view(n_kv, S, Hkv, dv).transpose(0, 1).contiguous().view(S * n_kv, Hkv, dv)
+    q_rank = q.repeat(S, 1, 1).contiguous()
+    segs = torch.tensor([[j * nq, nq, n_kv - 1, 0, j * n_kv, n_kv, j * nq, j] for j in range(S)],
+                        dtype=torch.int32)
+    status = cpa.new_status()
+    po, pl, _ = cpa.cp_attn_split_kv(segs.cuda(), q_rank, k_rank, v_rank, m["scale"], kv_block,
+                                     segs_host=segs, status=status)
+    seg1 = torch.tensor([[0, nq, n_kv - 1, 0, 0, n_kv, 0, 0]], dtype=torch.int32)
+    po1 = torch.empty(S, nq, Hq, dv, device="cuda")
+    pl1 = torch.empty(S, nq, Hq, device="cuda")
+    for j in range(S):
+        cpa.cp_attn_split_kv(seg1.cuda(), q, k[j::S], v[j::S], m["scale"], kv_block,
+                             segs_host=seg1, out=po1[j], lse_out=pl1[j], status=status)
+    out, lse = cpa.cp_lse_merge(po.view(S, nq, Hq, dv), pl.view(S, nq, Hq),
+                                lse_out=torch.empty(nq, Hq, device="cuda"), status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "decode one call")
+    assert torch.equal(po.view(S, nq, Hq, dv), po1) and torch.equal(pl.view(S, nq, Hq), pl1)
+    O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
+                                         m["scale"], np.arange(m["kv_tokens"]))
+    assert_attn_close(out, lse, O_ref, L_ref, f"decode one call {kv_block}")
