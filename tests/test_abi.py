@@ -272,3 +272,55 @@ def test_workspace_size_for_decode_segment():
     rows = 16 * 64                       # 16 blocks of 512 keys, 64 rows each
     expect = 256 + ((rows * 32 * 128 * 4 + 255) // 256) * 256 + ((rows * 32 * 4 + 255) // 256) * 256 + 256
     assert (b.value, m.value) == (expect, 16)
+
+
+def _host_plan(new, pre, C, strategy):
+    """A ShardPlan on the CPU built from the oracle's plan (for host logic)."""
+    import torch
+    op = oplan.make_plan(new, pre, C, strategy)
+    rows = []
+    for r in range(C):
+        for s in op.segments[r]:
+            rows.append([s.q_row0, s.q_len, s.q_pos0, s.q_pos_step, s.kv_row0, s.kv_len, 0, s.req])
+    i32 = torch.int32
+    empty = torch.empty(0, dtype=i32)
+    return api.ShardPlan(
+        cp_size=C, strategy=L.ZIGZAG if strategy == "zigzag" else L.INTERLEAVE,
+        rows_per_rank=[len(op.rank_rows[r]) for r in range(C)],
+        segs_per_rank=[len(op.segments[r]) for r in range(C)], tiles_per_rank=[0] * C,
+        segs=torch.tensor(rows or [[0] * 8], dtype=i32), seg_offsets=empty, row_offsets=empty,
+        gather_idx=empty, positions=empty, restore_idx=empty, tiles=empty,
+        new_lens_dev=torch.tensor(list(new) or [0], dtype=i32),
+        prefix_lens_dev=torch.tensor(list(pre) or [0], dtype=i32), num_reqs=len(new))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_pass_q_schedule_covers_every_visible_key_once(seed):
+    """Host logic of the ring schedule: over all launches, each segment meets
+    every key its rows can see exactly once, at hop s from the blocks of rank
+    (its shard + s) mod C, and no launch holds a segment twice."""
+    new, pre = W.random_batch(900 + seed, max_reqs=5, max_new=400, max_prefix=200)
+    C = [1, 2, 3, 4, 8, 5][seed % 6]
+    strategy = "zigzag" if seed % 2 == 0 else "interleave"
+    plan = _host_plan(new, pre, C, strategy)
+    segs = api.segments_host(plan)
+    shard = [r for r, c in enumerate(plan.segs_per_rank) for _ in range(c)]
+    sched = api.pass_q_schedule(plan)
+    assert len(sched) <= 2 * C
+    seen = {i: [] for i in range(len(segs))}
+    for launch in sched:
+        assert len(set(launch.seg_ids)) == len(launch.seg_ids)
+        assert launch.segs.shape[0] == launch.windows.shape[0] == len(launch.seg_ids)
+        for i, row, (lo, hi) in zip(launch.seg_ids, launch.segs.tolist(),
+                                    launch.windows.tolist()):
+            assert row == [segs[i][f] for f in api.SEGMENT_FIELDS]
+            sg = segs[i]
+            host = (shard[i] + launch.hop) % C
+            blocks = api.pass_q_kv_blocks(new[sg["req"]] + pre[sg["req"]], C)
+            assert (lo, hi) == tuple(blocks[host][launch.block]), blocks
+            seen[i].append((lo, hi))
+    for i, sg in enumerate(segs):
+        last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
+        covered = sorted(seen[i])
+        keys = [k for lo, hi in covered for k in range(lo, min(hi, last + 1))]
+        assert keys == list(range(last + 1)), (i, covered)
