@@ -621,6 +621,23 @@ def bench_pass_q(args, dev, stream, pk):
                     "in one launch with per-segment key windows) + cp_restore of O and LSE"}
 
 
+def decode_ranks(q, k, v, shards):
+    """Each rank's resident data for the decode step: its interleaved KV
+    tokens (key i on rank i mod shards) contiguous, as its KV cache holds
+    them, and a copy of every decode query; plus the segment table (one
+    segment per rank, every query at the last position)."""
+    import torch
+
+    nq, n_kv = q.shape[0], k.shape[0] // shards
+    Hkv, d, dv = k.shape[1], k.shape[2], v.shape[2]
+    k_rank = k.view(n_kv, shards, Hkv, d).transpose(0, 1).reshape(shards * n_kv, Hkv, d)
+    v_rank = v.view(n_kv, shards, Hkv, dv).transpose(0, 1).reshape(shards * n_kv, Hkv, dv)
+    q_rank = q.repeat(shards, 1, 1).contiguous()
+    segs_host = torch.tensor([[j * nq, nq, n_kv - 1, 0, j * n_kv, n_kv, j * nq, j]
+                              for j in range(shards)], dtype=torch.int32)
+    return q_rank, k_rank, v_rank, segs_host
+
+
 def bench_merge_sweep(args, dev, stream, pk):
     """Decode-style merge sweep: 64 single-token queries x 32 heads over 65536
     keys, key i resident on shard i mod 8.  Each rank's KV cache holds its
@@ -668,14 +685,7 @@ def bench_merge_sweep(args, dev, stream, pk):
                                  stream=stream)
         merge()
 
-    # each rank's KV cache: its interleaved tokens, contiguous; every rank
-    # holds all decode queries
-    Hkv, d = k.shape[1], k.shape[2]
-    k_rank = k.view(n_kv, S, Hkv, d).transpose(0, 1).contiguous().view(S * n_kv, Hkv, d)
-    v_rank = v.view(n_kv, S, Hkv, dv).transpose(0, 1).contiguous().view(S * n_kv, Hkv, dv)
-    q_rank = q.repeat(S, 1, 1).contiguous()
-    segs_all_host = torch.tensor([[j * nq, nq, n_kv - 1, 0, j * n_kv, n_kv, j * nq, j]
-                                  for j in range(S)], dtype=torch.int32)
+    q_rank, k_rank, v_rank, segs_all_host = decode_ranks(q, k, v, S)
     segs_all = segs_all_host.to(dev)
     po_rows, pl_rows = po.view(S * nq, Hq, dv), pl.view(S * nq, Hq)
     ws_all = cpa.cp_attn_split_kv(segs_all, q_rank, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
@@ -705,6 +715,7 @@ def bench_merge_sweep(args, dev, stream, pk):
     per_rank_us = time_steps(decode_step_per_rank)
     step_us = time_steps(decode_step)
     reps = 50
+    e0, e1 = E(), E()
     with torch.cuda.stream(stream):
         torch.cuda._sleep(50_000_000)
     e0.record(stream)
@@ -799,7 +810,9 @@ def run_profile_case(args):
                few-partial kernel).
     partial_kv: the whole 128K partial-KV call (layout, split-KV attention,
                fused merge + restore), as in the partial_kv entry.
-    restore:   the O restore of the default workload (268 MB each way)."""
+    restore:   the O restore of the default workload (268 MB each way).
+    decode:    the decode step of the merge sweep (one split-KV call over
+               the 8 ranks' KV caches, then the merge of the 8 partials)."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -820,6 +833,24 @@ def run_profile_case(args):
         run = lambda: cpa.cp_attn_partial_kv(  # noqa: E731
             plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens, prefix_lens=w.prefix_lens,
             workspace=ws, status=status)
+    elif args.profile_case == "decode":
+        m = W.MERGE_SWEEP
+        inputs = W.make_merge_sweep_inputs()
+        S, nq, Hq, dv = m["shards"], m["queries"], m["Hq"], m["dv"]
+        q_rank, k_rank, v_rank, segs_host = decode_ranks(inputs["q"].to(dev), inputs["k"].to(dev),
+                                                         inputs["v"].to(dev), S)
+        segs = segs_host.to(dev)
+        po = torch.empty(S, nq, Hq, dv, device=dev)
+        pl = torch.empty(S, nq, Hq, device=dev)
+        ws = cpa.cp_attn_split_kv(segs, q_rank, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
+                                  segs_host=segs_host, out=po.view(S * nq, Hq, dv),
+                                  lse_out=pl.view(S * nq, Hq), status=status)[2]
+
+        def run():
+            cpa.cp_attn_split_kv(segs, q_rank, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
+                                 segs_host=segs_host, out=po.view(S * nq, Hq, dv),
+                                 lse_out=pl.view(S * nq, Hq), workspace=ws, status=status)
+            cpa.cp_lse_merge(po, pl, status=status)
     elif args.profile_case in ("merge", "merge4"):
         w = W.WORKLOADS[MERGE_WORKLOAD]
         rows, Hq, dv = w.total_new // 16, w.Hq, w.dv
@@ -876,7 +907,7 @@ def main():
     ap.add_argument("--skip-merge", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--profile-case",
-                    choices=["attention", "merge", "merge4", "partial_kv", "restore"],
+                    choices=["attention", "merge", "merge4", "partial_kv", "restore", "decode"],
                     default=None,
                     help="run one kernel on a small case (for ncu) instead of the bench")
     args = ap.parse_args()

@@ -60,11 +60,11 @@ SIGNATURES = {
     "cp_partial_kv_workspace_size_segs": (i32, [vp, i32, i32, i32, i32,
                                                 ctypes.POINTER(ctypes.c_int64), c_i32p]),
     "cp_attn_partial_kv": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32,
-                                 i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, vp, i32, vp,
-                                 i32, vp, i64, vp, vp]),
+                                 i32, i32, i32, i32, ctypes.c_float, i32, i32, i32, vp, vp, i32,
+                                 vp, i32, vp, i64, vp, vp]),
     "cp_attn_partial_kv_noalloc": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64,
-                                         i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
-                                         vp, i32, vp, i32, i64, vp, vp]),
+                                         i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, i32,
+                                         vp, vp, i32, vp, i32, i64, vp, vp]),
     "cp_attn_debug": (i32, [i32, ctypes.c_longlong]),
     "cp_status_string": (ctypes.c_char_p, [i32]),
 }

@@ -542,7 +542,7 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
     L.check(lib.cp_attn_partial_kv(
         _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
         k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
-        float(scale), int(kv_block), int(max_blocks), _p(idx), _p(out),
+        float(scale), int(kv_block), int(max_blocks), 0, _p(idx), _p(out),
         1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
         workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
     return out, lse_out, workspace
@@ -550,11 +550,14 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
 
 def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_rows=None,
                      dst_rows=None, out=None, lse_out=None, out_fp32=True, workspace=None,
-                     status=None, stream=None):
+                     max_seg_rows=None, status=None, stream=None):
     """cp_attn_partial over any segment table with every segment's keys split
     into blocks of ``kv_block`` attended by separate CTAs, then merged by the
     LSE rule inside the library (cp_attn_partial_kv without a plan).  Meant for
     few query rows over many keys, e.g. a decode step against one KV shard.
+    ``max_seg_rows`` (default: the longest segment of ``segs_host``) is passed
+    to the library; at most 64 lets it pack two query heads per tile, 0
+    turns packing off.
     ``dst_rows`` (int32, one per query row) scatters the output; otherwise row
     i of the output is query row i.  Returns (O, LSE, workspace).
     """
@@ -566,6 +569,10 @@ def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_
     if segs_host is None:
         segs_host = segs.cpu()
     sh = segs_host.to(torch.int32).contiguous()
+    # the longest segment: decode-sized segments (<= 64 rows) let the kernel
+    # pack two query heads into each 128-row tile
+    max_rows = (int(sh[:ns, 1].max()) if ns > 0 else 0) if max_seg_rows is None \
+        else int(max_seg_rows)
     nbytes, max_blocks = ctypes.c_int64(), ctypes.c_int32()
     L.check(lib.cp_partial_kv_workspace_size_segs(
         ctypes.c_void_p(sh.data_ptr()), ns, int(kv_block), Hq, dv, ctypes.byref(nbytes),
@@ -583,7 +590,7 @@ def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_
     L.check(lib.cp_attn_partial_kv(
         _p(segs), ns, None, 0, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v), v.stride(0),
         v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_block),
-        max(1, int(max_blocks.value)), _p(dst_rows), _p(out),
+        max(1, int(max_blocks.value)), max_rows, _p(dst_rows), _p(out),
         1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
         workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
     return out, lse_out, workspace

@@ -114,15 +114,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   long long out_row0;
   if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
   if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
+  // packed heads: BM / 2 query rows per head, two heads per tile
+  const int HP = p.pack_heads ? 2 : 1;
+  if (p.pack_heads && sg.q_len > BM / 2) {
+    if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+    return;
+  }
   const int r0 = t * BM;
-  const int rows_valid = min(BM, sg.q_len - r0);
+  const int rows_valid = min(BM / HP, sg.q_len - r0);
   const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
   const int win_lo = max(kv_lo, 0);
   const int win_hi_tile = kv_hi < 0 ? pos_max + 1 : min(kv_hi, pos_max + 1);
   const int j0 = win_lo / BN;
   const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + BN - 1) / BN - j0 : 0;
-  const int head0 = hg * NQ;            // query heads head0 .. head0+NQ-1
-  const int kv_head = head0 / p.g;      // shared by all NQ heads (g % NQ == 0)
+  const int head0 = hg * NQ * HP;       // query heads head0 .. head0+NQ*HP-1
+  const int kv_head = head0 / p.g;      // shared by all of them (g % (NQ*HP) == 0)
 
   // ---- setup: barriers, TMEM ----
   if (threadIdx.x == 0) {
@@ -167,10 +173,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int k_issued = 0, v_issued = 0;
       if (!p.withhold_q) {
         mbar_arrive_expect_tx(bar_q, NQ * C::kQTileBytes);
+        // HP boxes of BM / HP rows per 64-column chunk (one per packed head)
         for (int s = 0; s < NQ; ++s)
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + C::kQOff + s * C::kQTileBytes + c * BM * 128, &tm_q, bar_q,
-                        c * 64, head0 + s, sg.q_row0 + r0);
+          for (int hp = 0; hp < HP; ++hp)
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(smem + C::kQOff + s * C::kQTileBytes + c * BM * 128 +
+                              hp * (BM / HP) * 128,
+                          &tm_q, bar_q, c * 64, head0 + s * HP + hp, sg.q_row0 + r0);
       }
       bool ok = true;
       for (int it = 0; it < n_kv && ok; ++it) {
@@ -280,9 +289,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if constexpr (C::kSplitRegs)
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
     // ------------------------------------------------------------- softmax --
-    const int s = warp >> 2;               // query tile / head of this warpgroup
+    const int s = warp >> 2;               // query tile of this warpgroup
     const int wq = warp & 3;               // TMEM lane quarter
-    const int row = wq * 32 + lane;        // row within the tile
+    const int trow = wq * 32 + lane;       // row within the tile
+    // query row and head of this thread (packed: two heads per tile, the
+    // head uniform across a warp)
+    const int row = p.pack_heads ? (trow & (BM / 2 - 1)) : trow;
+    const int h = head0 + s * HP + (p.pack_heads ? trow / (BM / 2) : 0);
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
     const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
@@ -375,7 +388,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else {
       tc_fence_after();
-      const int h = head0 + s;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
       MergeCoef mc{0.f, inv, has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY};
@@ -561,13 +573,16 @@ int cpattn::attn_launch(const cp_segment_t* segs_dev, int num_segs, const int32_
 
   const int g = Hq / Hkv;
   const int nq = (g % 2 == 0) ? 2 : 1;
+  // head packing (segments of at most BM / 2 rows): both tiles of a CTA hold
+  // two heads each, so the head group spans 4 heads of one KV head
+  if (prm.pack_heads && (mla || nq != 2 || g % 4 != 0)) prm.pack_heads = 0;
   prm.segs = segs_dev;
   prm.tiles = tiles_dev;
   prm.num_segs = num_segs;
   prm.num_tiles = tiles_dev ? num_tiles : 0;
   prm.Hq = Hq;
   prm.g = g;
-  prm.n_hgroups = Hq / nq;
+  prm.n_hgroups = Hq / (nq * (prm.pack_heads ? 2 : 1));
   prm.scale_log2 = scale * kLog2e;
   prm.num_q_rows = num_q_rows;
   prm.num_kv_rows = num_kv_rows;
@@ -580,7 +595,7 @@ int cpattn::attn_launch(const cp_segment_t* segs_dev, int num_segs, const int32_
     return launch_attn_mla(q, num_q_rows, k, k_row_stride, k_head_stride, num_kv_rows, Hkv, prm,
                            units, stream);
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, d, Hq, num_q_rows, d, (long long)Hq * d) ||
+  if (!make_map(&mq, q, d, Hq, num_q_rows, d, (long long)Hq * d, prm.pack_heads ? BM / 2 : BM) ||
       !make_map(&mk, k, d, Hkv, num_kv_rows, k_head_stride, k_row_stride) ||
       !make_map(&mv, v, dv, Hkv, num_kv_rows, v_head_stride, v_row_stride))
     return CPATTN_ERR_CUDA;

@@ -61,6 +61,12 @@ struct AttnParams {
   // (an upper end < 0 is unbounded), so that one launch can merge every
   // segment against its own resident KV block (the pass-Q ring hop).
   const int32_t* seg_windows;
+  // pack_heads (d = 64 / 128 kernel, two query tiles per CTA): every segment
+  // has at most BM / 2 rows, and each 128-row tile holds two query heads:
+  // tile row r is query row r % (BM / 2) of head 2 * tile + r / (BM / 2)
+  // within the CTA's head group (which then spans 4 heads).  The Q tensor map
+  // then has boxes of BM / 2 rows.  A longer segment sets CPATTN_ERR_RANGE.
+  int pack_heads;
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).

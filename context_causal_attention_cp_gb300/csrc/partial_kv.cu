@@ -414,11 +414,13 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                                   int64_t k_head_stride, const void* v, int64_t v_row_stride,
                                   int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
                                   int dv, float scale, int kv_block, int max_blocks,
+                                  int max_seg_rows,
                                   const int32_t* dst_rows, void* o_out, int o_is_fp32,
                                   float* lse_out, int num_out_rows, void* workspace,
                                   int64_t workspace_bytes, int32_t* status_dev,
                                   cudaStream_t stream) {
-  if (num_segs < 0 || kv_block < 1 || max_blocks < 0 || max_blocks > 32 || num_out_rows < 0)
+  if (num_segs < 0 || kv_block < 1 || max_blocks < 0 || max_blocks > 32 || num_out_rows < 0 ||
+      max_seg_rows < 0)
     return CPATTN_ERR_INVALID_ARG;
   // no segments (a batch without new tokens): nothing to compute; the sizing
   // calls report max_blocks = 0 for it
@@ -455,6 +457,7 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
   prm.max_blocks = max_blocks;
   prm.ws_slot = slot;
   prm.ws_rows = L.cap_rows;
+  prm.pack_heads = (max_seg_rows >= 1 && max_seg_rows <= BM / 2) ? 1 : 0;
   int rc = attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
                        k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
                        scale, prm, stream);

@@ -46,7 +46,8 @@ extern "C" int cp_attn_partial_kv_noalloc(
     const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev, int num_tiles,
     const void* q, int num_q_rows, const void* k, int64_t k_row_stride, int64_t k_head_stride,
     const void* v, int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
-    int d, int dv, float scale, int kv_block, int max_blocks, const int32_t* dst_rows,
+    int d, int dv, float scale, int kv_block, int max_blocks, int max_seg_rows,
+    const int32_t* dst_rows,
     void* o_out, int o_is_fp32, float* lse_out, int num_out_rows, int64_t workspace_bytes_needed,
     int32_t* status_dev, cudaStream_t stream) {
   if (workspace_bytes_needed < 0) return CPATTN_ERR_INVALID_ARG;
@@ -60,7 +61,8 @@ extern "C" int cp_attn_partial_kv_noalloc(
   // the same call.
   return cp_attn_partial_kv(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k,
                             k_row_stride, k_head_stride, v, v_row_stride, v_head_stride,
-                            num_kv_rows, Hq, Hkv, d, dv, scale, kv_block, max_blocks, dst_rows,
+                            num_kv_rows, Hq, Hkv, d, dv, scale, kv_block, max_blocks,
+                            max_seg_rows, dst_rows,
                             o_out, o_is_fp32, lse_out, num_out_rows, scratch,
                             (int64_t)CPATTN_NOALLOC_SCRATCH_BYTES, status_dev, stream);
 }

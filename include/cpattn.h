@@ -286,6 +286,12 @@ int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, i
  *   Arguments shared with cp_attn_partial keep its meaning.
  *   kv_block > 0; max_blocks: an upper bound on the blocks any segment sees,
  *     1 <= max_blocks <= 32 (a segment with more sets CPATTN_ERR_INVALID_ARG).
+ *   max_seg_rows: an upper bound on every segment's q_len, or 0 when unknown.
+ *     With 1 <= max_seg_rows <= CPATTN_TILE_ROWS / 2 (a decode step's few
+ *     queries) and Hq / Hkv a multiple of 4 (d = 64 or 128), each 128-row
+ *     query tile holds two query heads of the same KV head.  That halves the
+ *     tiles and the MMA work of short segments.  A segment longer than a
+ *     bound that enabled packing sets CPATTN_ERR_RANGE and is skipped.
  *     With num_segs == 0 the call does nothing and returns CPATTN_OK, and
  *     max_blocks may be 0 (what the sizing calls report for a batch without
  *     new tokens).
@@ -310,7 +316,8 @@ int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t
                        int64_t k_row_stride, int64_t k_head_stride, const void* v,
                        int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq,
                        int Hkv, int d, int dv, float scale, int kv_block, int max_blocks,
-                       const int32_t* dst_rows, void* o_out, int o_is_fp32, float* lse_out,
+                       int max_seg_rows, const int32_t* dst_rows, void* o_out, int o_is_fp32,
+                       float* lse_out,
                        int num_out_rows, void* workspace, int64_t workspace_bytes,
                        int32_t* status_dev, cudaStream_t stream);
 
@@ -339,7 +346,8 @@ int cp_attn_partial_kv_noalloc(const cp_segment_t* segs_dev, int num_segs,
                                int64_t k_head_stride, const void* v, int64_t v_row_stride,
                                int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
                                int dv, float scale, int kv_block, int max_blocks,
-                               const int32_t* dst_rows, void* o_out, int o_is_fp32,
+                               int max_seg_rows, const int32_t* dst_rows, void* o_out,
+                               int o_is_fp32,
                                float* lse_out, int num_out_rows, int64_t workspace_bytes_needed,
                                int32_t* status_dev, cudaStream_t stream);
 

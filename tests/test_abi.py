@@ -80,7 +80,9 @@ def test_invalid_arguments_are_rejected_on_host():
     assert lib.cp_attn_partial(*args, 8, 4, 128, 128, 0.1, 0, -1, nul, 0, lse, 0, 128, nul,
                                nul) == L.ERR_INVALID_ARG
     # partial-KV: block count limits and workspace sizing on the host
-    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 33, nul, o, 0, lse, 128,
+    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 33, 0, nul, o, 0, lse, 128,
+                                  fake[1], 1 << 20, nul, nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 4, -1, nul, o, 0, lse, 128,
                                   fake[1], 1 << 20, nul, nul) == L.ERR_INVALID_ARG
     nbytes, mb = ctypes.c_int64(), ctypes.c_int32()
     one = (ctypes.c_int32 * 1)(1000)
@@ -95,9 +97,9 @@ def test_invalid_arguments_are_rejected_on_host():
                                             ctypes.byref(mb)) == L.OK
     assert mb.value == 0
     empty = [fake[0], 0] + args[2:]
-    assert lib.cp_attn_partial_kv(*empty, 8, 4, 128, 128, 0.1, 64, 0, nul, nul, 0, nul, 0,
+    assert lib.cp_attn_partial_kv(*empty, 8, 4, 128, 128, 0.1, 64, 0, 0, nul, nul, 0, nul, 0,
                                   nul, 0, nul, nul) == L.OK
-    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 0, nul, o, 0, lse, 128,
+    assert lib.cp_attn_partial_kv(*args, 8, 4, 128, 128, 0.1, 64, 0, 0, nul, o, 0, lse, 128,
                                   fake[1], 1 << 20, nul, nul) == L.ERR_INVALID_ARG
     # merge: part count and dv limits
     assert lib.cp_lse_merge(nul, nul, 0, 0, 0, 4, 2, 128, nul, nul, 1, nul, 4, nul,

@@ -554,3 +554,51 @@ def test_decode_one_call_over_all_ranks(kv_block):
     O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
                                          m["scale"], np.arange(m["kv_tokens"]))
     assert_attn_close(out, lse, O_ref, L_ref, f"decode one call {kv_block}")
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (64, 16, 2), (128, 8, 8)])
+def test_split_kv_packed_heads_short_segments(d, Hq, Hkv):
+    """Segments of at most 64 rows (decode queries and short causal chunks at
+    several positions, some ragged) through cp_attn_split_kv: with two query
+    heads packed per tile (Hq / Hkv a multiple of 4) the result is
+    bit-identical to unpacked tiles and equals the oracle; with a head ratio
+    that cannot pack, the hint changes nothing."""
+    gen = torch.Generator().manual_seed(4100 + d + Hq)
+    n_kv = 3000
+    k = (torch.randn(n_kv, Hkv, d, generator=gen)).to(torch.bfloat16)
+    v = (torch.randn(n_kv, Hkv, d, generator=gen)).to(torch.bfloat16)
+    # (q_len, q_pos0, q_pos_step, kv_row0, kv_len)
+    spec = [(64, 2999, 0, 0, 3000), (37, 1200, 1, 0, 1237), (1, 5, 0, 0, 6),
+            (50, 700, 1, 1000, 750), (64, 0, 1, 2000, 64), (13, 90, 7, 0, 175)]
+    rows, seg_rows = 0, []
+    for ql, p0, st, kv0, kvl in spec:
+        seg_rows.append([rows, ql, p0, st, kv0, kvl, rows, 0])
+        rows += ql
+    segs = torch.tensor(seg_rows, dtype=torch.int32)
+    q = (torch.randn(rows, Hq, d, generator=gen)).to(torch.bfloat16)
+    scale = 1 / math.sqrt(d)
+    status = cpa.new_status()
+    outs = []
+    for hint in (None, 0):
+        o, l, _ = cpa.cp_attn_split_kv(segs.cuda(), q.cuda(), k.cuda(), v.cuda(), scale, 256,
+                                       segs_host=segs, max_seg_rows=hint, status=status)
+        outs.append((o, l))
+    torch.cuda.synchronize()
+    cpa.check_status(status, "packed heads")
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    pos = np.concatenate([p0 + st * np.arange(ql) for ql, p0, st, _, _ in spec])
+    kv0 = np.concatenate([np.full(ql, kv) for ql, _, _, kv, _ in spec])
+    O_ref, L_ref = oatt.attention_rows(np64(q), np64(k), np64(v), pos, kv0, scale)
+    assert_attn_close(outs[0][0], outs[0][1], O_ref, L_ref, f"packed d={d} Hq={Hq}")
+
+
+def test_packed_heads_reject_a_longer_segment():
+    """A max_seg_rows hint that a segment exceeds: RANGE, the segment skipped."""
+    segs = torch.tensor([[0, 100, 0, 1, 0, 100, 0, 0]], dtype=torch.int32)
+    q = torch.zeros(100, 8, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(100, 2, 128, dtype=torch.bfloat16, device="cuda")
+    status = cpa.new_status()
+    cpa.cp_attn_split_kv(segs.cuda(), q, k, k, 0.1, 64, segs_host=segs, max_seg_rows=64,
+                         status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == -6

@@ -35,7 +35,7 @@ def _noalloc(plan, q_cat, k, v, scale, kv_block, max_blocks, need, out, lse, sta
     return lib.cp_attn_partial_kv_noalloc(
         _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
         k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
-        float(scale), kv_block, max_blocks, _p(plan.gather_idx), _p(out), 0, _p(lse),
+        float(scale), kv_block, max_blocks, 0, _p(plan.gather_idx), _p(out), 0, _p(lse),
         out.shape[0], need, _p(status), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
