@@ -463,12 +463,18 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                        scale, prm, stream);
   if (rc != CPATTN_OK) return rc;
 
-  const int grid = num_sms() * 2 * 8;
   // heads per merge task: all of a row's heads, unless the rows (at most
-  // num_q_rows) are too few to give every resident warp a few tasks
-  const long long warps = (long long)grid * (kMergeThreadsP / 32);
+  // num_q_rows) are too few to give every resident warp (two blocks per SM)
+  // a task.  Each task walks a dependent chain (segment search, slot) before
+  // its loads, so fewer, wider tasks beat one task per head on few rows.
+  const long long resident_warps = (long long)num_sms() * 2 * (kMergeThreadsP / 32);
   int hs = Hq;
-  while (hs > 1 && (long long)num_q_rows * ((Hq + hs - 1) / hs) < 4 * warps) hs = (hs + 1) / 2;
+  while (hs > 1 && (long long)num_q_rows * ((Hq + hs - 1) / hs) < resident_warps)
+    hs = (hs + 1) / 2;
+  const long long tasks = (long long)num_q_rows * ((Hq + hs - 1) / hs);
+  const int grid = (int)std::max<long long>(
+      1, std::min<long long>((long long)num_sms() * 2 * 8,
+                             (tasks + kMergeThreadsP / 32 - 1) / (kMergeThreadsP / 32)));
   if (o_is_fp32)
     pkv_merge_kernel<true><<<grid, kMergeThreadsP, 0, stream>>>(
         segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
