@@ -38,6 +38,16 @@ def _run(cmd):
     return res.stdout
 
 
+def is_stale() -> bool:
+    """True when the library is missing or older than any source or the header."""
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    deps.append(os.path.join(ROOT, "include", "cpattn.h"))
+    return any(os.path.getmtime(f) > t for f in deps)
+
+
 def build(verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -56,7 +66,7 @@ def build(verbose: bool = False, extra_flags=()) -> str:
         for o in outs:
             sys.stdout.write(o)
     tmp = LIB + ".tmp"
-    _run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"] * 0)
+    _run([nvcc()] + ARCH + ["-shared", "-o", tmp] + objs)
     os.replace(tmp, LIB)
     return LIB
 
