@@ -326,3 +326,38 @@ def test_pass_q_schedule_covers_every_visible_key_once(seed):
         covered = sorted(seen[i])
         keys = [k for lo, hi in covered for k in range(lo, min(hi, last + 1))]
         assert keys == list(range(last + 1)), (i, covered)
+
+
+def _c_param_kind(decl):
+    """ctypes kind of one C parameter declaration of the header."""
+    d = " ".join(decl.split())
+    if "*" in d or d.startswith("cudaStream_t"):
+        return "ptr"
+    base = d.rsplit(" ", 1)[0].replace("const ", "")
+    return {"int": "i32", "int32_t": "i32", "cp_strategy_t": "i32", "int64_t": "i64",
+            "long long": "i64", "float": "f32", "double": "f64"}[base]
+
+
+def _ctypes_kind(t):
+    import ctypes
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and \
+            isinstance(getattr(t, "_type_"), type):
+        return "ptr"
+    return {ctypes.c_int32: "i32", ctypes.c_int64: "i64", ctypes.c_longlong: "i64",
+            ctypes.c_float: "f32", ctypes.c_double: "f64"}.get(t, repr(t))
+
+
+def test_binding_signatures_match_the_header():
+    """Every prototype in include/cpattn.h has a binding entry with the same
+    number of arguments and the same kind (pointer, 32 / 64-bit integer,
+    float) at each position, so no ctypes call can shift its arguments."""
+    src = open(os.path.join(ROOT, "include", "cpattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    protos = re.findall(r"\b(?:int|const\s+char\s*\*)\s*(cp_\w+)\s*\(([^;{]*?)\)\s*;", src,
+                        flags=re.S)
+    assert len(protos) == len(header_functions())
+    for name, params in protos:
+        decls = [p.strip() for p in params.split(",")] if params.strip() not in ("", "void") else []
+        want = [_c_param_kind(p) for p in decls]
+        got = [_ctypes_kind(t) for t in L.SIGNATURES[name][1]]
+        assert got == want, (name, got, want)
