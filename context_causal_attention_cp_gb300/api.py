@@ -514,13 +514,24 @@ def cp_partial_kv_workspace_size(new_lens, prefix_lens, cp_size, strategy, kv_bl
     return nbytes.value, mb.value
 
 
+def plan_max_segment_rows(new_lens, cp_size, strategy) -> int:
+    """Upper bound on the rows of any segment a plan makes: a zigzag block
+    holds at most ceil(n / 2C) tokens of its request, an interleave run at
+    most ceil(n / C)."""
+    per = 2 * cp_size if _strategy(strategy) == L.ZIGZAG else cp_size
+    return max([(int(n) + per - 1) // per for n in new_lens] or [0])
+
+
 def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_lens, prefix_lens,
                        workspace=None, dst_rows="restore", out=None, lse_out=None,
-                       out_fp32=False, status=None, stream=None):
+                       out_fp32=False, max_seg_rows=None, status=None, stream=None):
     """Partial-KV decomposition in one library call (layout, split attention, merge).
 
     ``dst_rows="restore"`` scatters the merged rows to original token order
-    (the plan's gather index); ``None`` keeps cat order.  Returns (O, LSE, workspace).
+    (the plan's gather index); ``None`` keeps cat order.  ``max_seg_rows``
+    (default: the plan's bound from the request lengths) lets the library
+    pack two query heads per tile when every segment has at most 64 rows; 0
+    turns packing off.  Returns (O, LSE, workspace).
     """
     lib = L.load()
     N, Hq, d = q_cat.shape
@@ -542,7 +553,9 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
     L.check(lib.cp_attn_partial_kv(
         _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
         k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
-        float(scale), int(kv_block), int(max_blocks), 0, _p(idx), _p(out),
+        float(scale), int(kv_block), int(max_blocks),
+        plan_max_segment_rows(new_lens, plan.cp_size, plan.strategy) if max_seg_rows is None
+        else int(max_seg_rows), _p(idx), _p(out),
         1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
         workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
     return out, lse_out, workspace

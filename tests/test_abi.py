@@ -361,3 +361,16 @@ def test_binding_signatures_match_the_header():
         want = [_c_param_kind(p) for p in decls]
         got = [_ctypes_kind(t) for t in L.SIGNATURES[name][1]]
         assert got == want, (name, got, want)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_plan_segment_row_bound_holds(seed):
+    """The host bound on segment rows (it decides head packing in the
+    partial-KV call) is never below a segment of the oracle's plan."""
+    new, pre = W.random_batch(1300 + seed, max_reqs=6, max_new=500, max_prefix=100)
+    C = [1, 2, 3, 4, 8][seed % 5]
+    for strategy in ("zigzag", "interleave"):
+        op = oplan.make_plan(new, pre, C, strategy)
+        longest = max([s.q_len for r in range(C) for s in op.segments[r]] or [0])
+        bound = api.plan_max_segment_rows(new, C, strategy)
+        assert longest <= bound <= longest + 1, (strategy, longest, bound)

@@ -602,3 +602,30 @@ def test_packed_heads_reject_a_longer_segment():
                          status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == -6
+
+
+def test_partial_kv_short_requests_pack_heads():
+    """Plan-based partial-KV over short requests (every segment <= 64 rows):
+    the call packs two query heads per tile, bit-identical to unpacked tiles
+    and equal to the oracle, for both strategies."""
+    w = W.Workload(name="pkv_short", new_lens=[100, 37, 90, 5, 128], prefix_lens=[0, 20, 300, 3, 0],
+                   Hq=8, Hkv=2, d=128, dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=2,
+                   strategies=["zigzag", "interleave"], seed=4321, kv_block=64)
+    inputs = W.make_inputs(w)
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    k, v = inputs["k"].cuda(), inputs["v"].cuda()
+    for strategy in w.strategies:
+        assert cpa.api.plan_max_segment_rows(w.new_lens, w.cp_size, strategy) <= 64
+        status = cpa.new_status()
+        plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
+        q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
+        outs = [cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
+                                       new_lens=w.new_lens, prefix_lens=w.prefix_lens,
+                                       max_seg_rows=hint, status=status)[:2]
+                for hint in (None, 0)]
+        torch.cuda.synchronize()
+        cpa.check_status(status, f"pkv short {strategy}")
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+        assert_attn_close(outs[0][0], outs[0][1], O_ref, L_ref, f"pkv short/{strategy}")
