@@ -388,7 +388,7 @@ def run_ours(args):
         line["merge_sweep"] = bench_merge_sweep(args, dev, stream, pk)
         line["gpu_launches"] += line["merge_sweep"].pop("launches")
     if not args.skip_e2e:
-        line["e2e"] = bench_e2e(args, w, inputs, dev, stream)
+        line["e2e"] = bench_e2e(args, w, inputs, dev, stream, world)
     del q, k, v, ws, flush
     torch.cuda.empty_cache()
     if rank == 0 and not args.skip_cpu:
@@ -753,14 +753,17 @@ def bench_merge_sweep(args, dev, stream, pk):
                     "(blocks of 512) on strided views of the original-order KV"}
 
 
-def bench_e2e(args, w, inputs, dev, stream):
+def bench_e2e(args, w, inputs, dev, stream, world=1):
     """Same step through the public API with pinned host inputs and outputs.
 
     Every step uploads its q, k, v from pinned host memory, runs plan ->
     gather -> attention (restore fused into the store) and downloads O and
     LSE to pinned host memory (api.PrefillPipeline: batch n's attention
     overlaps batch n+1's upload and batch n-1's download).  The timed region
-    runs from before the first upload to after the last download."""
+    runs from before the first upload to after the last download.  With N
+    ranks the replicas start together after a barrier; the figure is the work
+    of all ranks over the slowest rank's time, and the bytes are the whole
+    job's."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -778,6 +781,9 @@ def bench_e2e(args, w, inputs, dev, stream):
     pipe.synchronize()
     torch.cuda.synchronize(dev)
     reps = max(3, args.steps // 2)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(pipe.s_up)
     for _ in range(reps):
@@ -786,12 +792,12 @@ def bench_e2e(args, w, inputs, dev, stream):
     pipe.s_down.wait_stream(pipe.s_comp)
     e1.record(pipe.s_down)
     pipe.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    h2d = hq.numel() * 2 + hk.numel() * 2 + (0 if hv is None else hv.numel() * 2)
-    d2h = ho.numel() * 2 + hl.numel() * 4
+    ms = reduce_max_over_ranks(e0.elapsed_time(e1) / reps, world, dev)
+    h2d = world * (hq.numel() * 2 + hk.numel() * 2 + (0 if hv is None else hv.numel() * 2))
+    d2h = world * (ho.numel() * 2 + hl.numel() * 4)
     del pipe
     torch.cuda.empty_cache()
-    return {"value": attention_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
+    return {"value": world * attention_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "steps": reps,
             "path": "api.PrefillPipeline: per step, pinned host q/k/v upload, plan, gather, "
