@@ -1,33 +1,43 @@
 #!/usr/bin/env python
 """Benchmark: causal prefill context-parallel attention on one GB300.
 
-Default workload: one 32768-token prompt, Llama-3-8B-shaped attention (32
+Headline workload: one 32768-token prompt, Llama-3-8B-shaped attention (32
 query / 8 KV heads, head dim 128), CP = 8 zigzag (16 blocks of 2048), bf16
-N(0,1) synthetic inputs.  One step is the whole hot path on the device:
-shard plan -> causal attention of all 8 shards against the gathered KV in
-one launch that reads each shard's query rows and writes O and LSE by token
-index (zigzag shards are runs of consecutive tokens: the query gather and the
-restore happen in the kernel's own loads and stores).  ``value`` is causal attention TFLOP/s over the step (2*Hq*(d+dv)
-flops per visible (query, key) pair), L2 flushed between steps.
+N(0,1) synthetic inputs.  One step is the whole hot path on the device: shard
+plan -> causal attention of all 8 shards against the gathered KV in one launch
+that reads each shard's query rows and writes O and LSE by token index
+(zigzag shards are runs of consecutive tokens, so the query gather and the
+restore happen in the kernel's own loads and stores).  ``value`` is causal
+attention TFLOP/s over the step (2*Hq*(d+dv) flops per visible (query, key)
+pair), L2 flushed between steps.
 
-The line also carries the LSE-merge GB/s of the 131072-token partial-KV
-decomposition (16 KV blocks of 8192, 136 visible fp32 partials merged and
-scattered to causal order), that decomposition end to end as one call
-(pass-KV) and through the pass-Q ring, the GB/s of the standalone restore kernel (the
-two-pass path's cp_restore of O and LSE), the attention kernel's
-roofline, clocks under load, an end-to-end figure through the public API with
-host buffers, and the CPU oracle timed on a bounded sample of the same
-workload.
+``per_config`` carries every workload of the benchmark set, each with its own
+roofline and the CPU oracle timed beside it on this machine's host cores:
+  1   1024-token prompt, d = 64, 8/8 heads, CP=4 zigzag (all rows to the oracle)
+  2   6-request varlen batch with cached prefixes, GQA 32/8, CP=4, zigzag and
+      interleave (all rows to the oracle)
+  3   the headline 32K workload (the top-level figures)
+  4   absorbed MLA 16K, 128 heads over one 576-wide latent head, CP=4
+      interleave
+  5a  the 131072-token partial-KV decomposition (LSE merge GB/s of 136 fp32
+      partials; the pass-KV step in one call; the pass-Q ring)
+  5b  the decode-style merge sweep (64 queries x 32 heads over 65536 keys on 8
+      interleaved shards)
+The line also carries the standalone restore kernel's GB/s, clocks sampled
+during every timed region, and an end-to-end figure through the C ABI's
+host-to-host call.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
 
 import argparse
 import json
-import math
+import multiprocessing as mp
 import os
+import shutil
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -38,8 +48,10 @@ UNIT = "TFLOP/s"
 WORKLOAD = "llama8b_32k"
 MERGE_WORKLOAD = "partialkv_128k"
 DECODE_KV_BLOCK = 4096  # keys per CTA in the decode step (2 blocks per rank)
+ORACLE_SAMPLE_ROWS = 512  # rows x all heads when the oracle runs a sample of a workload
 # ncu summary under profiles/ holding the attention kernel's DRAM bytes per launch
 PROFILE_MD = {"llama8b_32k": "attn_fwd_llama8b_32k.md", "mla_16k": "attn_mla_mla_16k.md"}
+L2_NOTE = "flushed between steps (256 MiB write outside the step's events)"
 
 
 def peaks():
@@ -120,147 +132,271 @@ def kernel_label(w):
     if w.d == 576:
         return "attn_mla_kernel (tcgen05; 128 rows x 1 head x one 256-column output half per CTA)"
     nq = 2 if (w.Hq // w.Hkv) % 2 == 0 else 1
-    return f"attn_fwd_kernel (tcgen05; {nq} head(s) x 128 rows per CTA)"
+    return f"attn_fwd_kernel<d={w.d}> (tcgen05; {nq} head(s) x 128 rows per CTA)"
 
 
-def config_of(w, extra=None):
-    cfg = {"workload": f"{w.name}: {w.description}", "new_lens": w.new_lens,
-           "prefix_lens": w.prefix_lens, "heads_q": w.Hq, "heads_kv": w.Hkv, "d": w.d,
-           "dv": w.dv, "cp_size": w.cp_size, "strategy": w.strategies[0],
-           "l2": "flushed between steps (256 MiB write outside the step's events)"}
-    if extra:
-        cfg.update(extra)
-    return cfg
+def config_of(w, world=1, strategy=None):
+    """The config dict of a workload; both arms print the same one."""
+    return {"workload": f"{w.name}: {w.description}", "new_lens": w.new_lens,
+            "prefix_lens": w.prefix_lens, "heads_q": w.Hq, "heads_kv": w.Hkv, "d": w.d,
+            "dv": w.dv, "cp_size": w.cp_size, "strategy": strategy or w.strategies[0],
+            "l2": L2_NOTE, "parallelism": f"replicas{world}"}
 
 
 # ----------------------------------------------------------------- clocks --
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms; entering
-    waits (up to 3 s) for the first sample so that the samples kept, those
-    read between entering and leaving, fall inside the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms for the
+    whole run.  Each sample carries nvidia-smi's own timestamp; samples are
+    attributed to the timed regions (``region(name)``) whose wall-clock span
+    contains them, so buffering of the tool's output cannot misplace them."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_ms=20):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
         self.lines = []
-        self.keep = False
+        self.regions = []
 
     def _reader(self):
         for line in self.proc.stdout:
-            if self.keep:
-                self.lines.append(line)
-            self.first.set()
+            self.lines.append(line)
 
-    def __enter__(self):
+    def start(self):
         import threading
-        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except Exception:  # noqa: BLE001
             self.proc = None
             return self
-        self.thread = threading.Thread(target=self._reader, daemon=True)
-        self.thread.start()
-        self.first.wait(timeout=3.0)
-        self.keep = True
+        threading.Thread(target=self._reader, daemon=True).start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 3.0:  # first sample in, tool running
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *a):
-        self.keep = False
-        self.out = "".join(self.lines)
+    def stop(self):
         if self.proc is not None:
+            time.sleep(2 * self.period_ms / 1000.0)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:  # noqa: BLE001
                 self.proc.kill()
 
-    def summary(self):
-        sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
+    class _Region:
+        def __init__(self, owner, name):
+            self.owner, self.name = owner, name
+
+        def __enter__(self):
+            self.t0 = time.time()
+            return self
+
+        def __exit__(self, *a):
+            self.owner.regions.append((self.name, self.t0, time.time()))
+
+    def region(self, name):
+        return ClockSampler._Region(self, name)
+
+    @staticmethod
+    def parse(lines):
+        """[(unix time, sm MHz, max MHz, set of active reasons)]"""
+        import datetime
+        out = []
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sms.append(float(parts[1]))
-                mx = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sms.sort()
-        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sms)}
+            reasons = {n for n, v in zip(ClockSampler.REASONS, parts[6:10])
+                       if v.lower().startswith("active")}
+            out.append((ts, sm, mx, reasons))
+        return out
+
+    def summary(self, names=None):
+        """Median SM clock and active reasons over the samples inside the
+        regions (all regions, or those in ``names``)."""
+        spans = [(a, b) for n, a, b in self.regions if names is None or n in names]
+        samples = [s for s in self.parse(self.lines)
+                   if any(a - 0.01 <= s[0] <= b + 0.01 for a, b in spans)]
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sms = sorted(s[1] for s in samples)
+        reasons = set().union(*[s[3] for s in samples])
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": samples[-1][2],
+                "reasons": sorted(reasons), "samples": len(samples),
+                "period_ms": self.period_ms,
+                "timed_s": round(sum(b - a for a, b in spans), 3)}
 
 
 # ------------------------------------------------------------- oracle leg --
-def oracle_sample_rate(w, inputs, budget_s, seed=0):
-    """Time the CPU oracle on seeded query rows of the workload for ~budget_s.
+# The CPU oracle (oracle.attention.attention_rows, unchanged) on selected
+# query rows, spread over spawned worker processes; each worker memory-maps
+# the float64 K and V that the parent wrote once.  Spawn, not fork: the parent
+# holds a CUDA context.
+_ORACLE_K = None
+_ORACLE_V = None
 
-    Returns (flops per second, rows, seconds, threads)."""
+
+def _oracle_init(k_path, k_shape, v_path, v_shape, v_cols):
     import numpy as np
-    import torch
-    from oracle import attention as oatt
+    global _ORACLE_K, _ORACLE_V
+    _ORACLE_K = np.memmap(k_path, dtype=np.float64, mode="r", shape=k_shape)
+    _ORACLE_V = (_ORACLE_K[:, :, :v_cols] if v_path is None else
+                 np.memmap(v_path, dtype=np.float64, mode="r", shape=v_shape))
 
-    threads = len(os.sched_getaffinity(0))
-    torch.set_num_threads(threads)
-    k64 = inputs["k"].float().numpy().astype(np.float64)
-    v64 = (k64[:, :, : w.dv] if w.v_is_k_prefix else
-           inputs["v"].float().numpy().astype(np.float64))
-    pos, kv0 = oatt.token_tables(w.new_lens, w.prefix_lens)
-    g = torch.Generator().manual_seed(seed)
-    order = torch.randperm(w.total_new, generator=g).tolist()
-    done, flops, t0 = 0, 0.0, time.perf_counter()
-    while done < len(order):
-        i = order[done]
-        q = inputs["q"][i: i + 1].float().numpy().astype(np.float64)
-        oatt.attention_rows(q, k64, v64, pos[i: i + 1], kv0[i: i + 1], w.scale)
-        flops += 2.0 * w.Hq * (w.d + w.dv) * (int(pos[i]) + 1)
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return flops / dt, done, dt, threads
+
+def _oracle_rows(args):
+    from oracle import attention as oatt
+    q, pos, kv0, scale = args
+    oatt.attention_rows(q, _ORACLE_K, _ORACLE_V, pos, kv0, scale)
+    return len(pos)
+
+
+def oracle_workers():
+    return max(1, min(16, len(os.sched_getaffinity(0))))
+
+
+class OracleRows:
+    """A pool of oracle workers over one workload's K and V."""
+
+    def __init__(self, w, inputs, procs=None):
+        import numpy as np
+        self.w = w
+        self.procs = procs or oracle_workers()
+        k64 = inputs["k"].float().numpy().astype(np.float64)
+        base = None
+        need = k64.nbytes * (1 if w.v_is_k_prefix else 2)
+        try:
+            if shutil.disk_usage("/dev/shm").free > 2 * need:
+                base = "/dev/shm"
+        except OSError:
+            pass
+        self.tmp = tempfile.mkdtemp(prefix="bench_oracle_", dir=base)
+        k_path = os.path.join(self.tmp, "k.f64")
+        k64.tofile(k_path)
+        v_path, v_shape = None, (w.total_kv, w.Hkv, w.dv)
+        if not w.v_is_k_prefix:
+            v_path = os.path.join(self.tmp, "v.f64")
+            inputs["v"].float().numpy().astype(np.float64).tofile(v_path)
+        del k64
+        self.q = inputs["q"]
+        from oracle import attention as oatt
+        self.pos, self.kv0 = oatt.token_tables(w.new_lens, w.prefix_lens)
+        self.pool = mp.get_context("spawn").Pool(
+            self.procs, initializer=_oracle_init,
+            initargs=(k_path, (w.total_kv, w.Hkv, w.d), v_path, v_shape, w.dv))
+        self.pool.map(_oracle_rows, [(self._q([0]), self.pos[:1], self.kv0[:1], w.scale)]
+                      * self.procs)  # workers up and mapped before any timing
+
+    def _q(self, rows):
+        import numpy as np
+        import torch
+        return self.q[torch.as_tensor(list(rows), dtype=torch.long)].float().numpy() \
+            .astype(np.float64)
+
+    def flops(self, rows):
+        w = self.w
+        return sum(2.0 * w.Hq * (w.d + w.dv) * (int(self.pos[r]) + 1) for r in rows)
+
+    def run(self, rows):
+        """Wall seconds the oracle takes on these rows (all heads)."""
+        import numpy as np
+        rows = np.asarray(rows, dtype=np.int64)
+        order = rows[np.argsort(-self.pos[rows], kind="stable")]
+        nchunks = max(1, min(len(rows), 4 * self.procs))
+        chunks = [order[c::nchunks] for c in range(nchunks)]
+        tasks = [(self._q(c), self.pos[c], self.kv0[c], self.w.scale) for c in chunks if len(c)]
+        t0 = time.perf_counter()
+        done = sum(self.pool.map(_oracle_rows, tasks, chunksize=1))
+        dt = time.perf_counter() - t0
+        assert done == len(rows)
+        return dt
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+        shutil.rmtree(self.tmp, ignore_errors=True)
+
+
+def sample_rows(w, count, seed):
+    from context_causal_attention_cp_gb300 import workloads as W
+    if count >= w.total_new:
+        return list(range(w.total_new))
+    return W.sample_rows(seed, w.total_new, count)
+
+
+def oracle_baseline(w, inputs, rows, what):
+    """cpu_baseline entry: the oracle on ``rows`` (all heads) in TFLOP/s."""
+    pool = OracleRows(w, inputs)
+    try:
+        dt = pool.run(rows)
+        fl = pool.flops(rows)
+    finally:
+        pool.close()
+    full = len(rows) == w.total_new
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": pool.procs, "kind": "oracle",
+            "seconds": round(dt, 3), "rows": len(rows), "extrapolated": not full,
+            "sample": (f"all {len(rows)} query rows" if full else
+                       f"{len(rows)} seeded random query rows of {w.total_new}") +
+                      f" x all {w.Hq} heads of {what}, fp64 NumPy oracle in {pool.procs} "
+                      f"processes, {dt:.1f} s" +
+                      ("" if full else "; the rate stands for the whole workload")}
 
 
 def run_reference(args):
-    """The oracle as the reference arm, on the host cores (rank 0 only)."""
+    """The oracle as the reference arm, on the host cores (rank 0 only).
+
+    Every step is a bounded sample of the headline workload: ``rows_per_step``
+    seeded random query rows x all heads through the fp64 oracle.  The line
+    reports what actually ran: its steps, their wall time, and the oracle's
+    rate on them (flops of the sampled rows / time); the time the full
+    workload would take at that rate is given separately."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
     from context_causal_attention_cp_gb300 import workloads as W
 
     w = W.WORKLOADS[args.workload]
     inputs = W.make_inputs(w)
-    rates, rows_total, secs = [], 0, 0.0
-    threads = len(os.sched_getaffinity(0))
-    for s in range(args.warmup + args.steps):
-        rate, rows, dt, threads = oracle_sample_rate(w, inputs, args.ref_step_seconds, seed=s)
-        if s >= args.warmup:
-            rates.append(rate)
-            rows_total += rows
-            secs += dt
-    value = sum(rates) / len(rates) / 1e12
-    ms = attention_flops(w) / (value * 1e12) * 1e3
-    sample = (f"{rows_total} random query rows x all {w.Hq} heads of the workload over "
-              f"{args.steps} steps of ~{args.ref_step_seconds:.0f} s; rate extrapolated to "
-              f"the full workload")
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+    pool = OracleRows(w, inputs)
+    times, flops, rows_done = [], 0.0, 0
+    try:
+        for s in range(args.warmup + args.steps):
+            rows = sample_rows(w, args.ref_rows_per_step, seed=100 + s)
+            dt = pool.run(rows)
+            if s >= args.warmup:
+                times.append(dt)
+                flops += pool.flops(rows)
+                rows_done += len(rows)
+    finally:
+        pool.close()
+    secs = sum(times)
+    value = flops / secs / 1e12
+    sample = (f"{args.ref_rows_per_step} seeded random query rows x all {w.Hq} heads per step "
+              f"({rows_done} rows over {args.steps} timed steps), fp64 NumPy oracle in "
+              f"{pool.procs} processes")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "impl": "reference", "config": config_of(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "data": "synthetic", "impl": "reference", "config": config_of(w, world),
+            "step": "one bounded sample of the workload (see sample)",
+            "rows_per_step": args.ref_rows_per_step, "rows_timed": rows_done,
+            "extrapolated": False,
+            "full_workload_seconds_at_this_rate": attention_flops(w) / (value * 1e12),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.procs, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -269,6 +405,101 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- our arm --
+def _events(n, k):
+    import torch
+    return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
+
+
+def bench_full_kv(w, strategy, inputs, dev, stream, pk, flush, steps, warmup, clk, status,
+                  region, world=1):
+    """Full-KV CP step of one workload: plan, then (zigzag) the token-row
+    attention launch, or (interleave) the query gather into shard order and
+    the attention launch with the restore in its store.  L2 flushed before
+    every step.  Returns the figures, the step / attention events' times and
+    the launch count."""
+    import torch
+
+    import context_causal_attention_cp_gb300 as cpa
+
+    q = inputs["q"].to(dev)
+    k = inputs["k"].to(dev)
+    v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].to(dev)
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, device=dev)
+    q_cat = torch.empty_like(q)
+    o = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    token_rows = strategy == "zigzag"   # zigzag shards are runs of consecutive tokens
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        cpa.cp_shard_plan(plan, status=status, stream=stream)
+        if not token_rows:
+            cpa.cp_restore(q, plan.gather_idx[:N], out=q_cat, status=status, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        if token_rows:
+            cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
+                                tiles=plan.tiles, num_tiles=plan.total_tiles, out=o, lse=lse,
+                                status=status, stream=stream)
+        else:
+            cpa.cp_attn_partial_restore(plan.segs, q_cat, k, v, w.scale, plan.gather_idx,
+                                        num_out_rows=N, num_segs=plan.total_segs,
+                                        tiles=plan.tiles, num_tiles=plan.total_tiles, out=o,
+                                        lse=lse, status=status, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    launches_per_step = 3 + (0 if token_rows else 1) + 1  # plan, [Q gather], attention
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, f"{w.name} warmup")
+    evs = _events(steps, 3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with clk.region(region):
+        t_wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    cpa.check_status(status, f"{w.name} timed steps")
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    flops = attention_flops(w)
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    achieved = flops / (attn_avg * 1e-3) / 1e12
+    traffic = profiled_traffic(PROFILE_MD.get(w.name, ""))
+    out = {"workload": f"{w.name}: {w.description}", "strategy": strategy,
+           "config": config_of(w, world, strategy),
+           "ms_per_step": sum(step_ms) / len(step_ms), "steps": steps,
+           "tflops": flops / (sum(step_ms) / len(step_ms) * 1e-3) / 1e12,
+           "attention_flops": flops,
+           "breakdown_ms": {("plan" if token_rows else "plan_and_q_gather"):
+                            sum(prep_ms) / len(prep_ms),
+                            ("attention_token_rows" if token_rows else
+                             "attention_with_restore_store"): attn_avg},
+           "roofline": {"kernel": kernel_label(w), "bound": "tensor", "achieved": achieved,
+                        "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                        "traffic_unit": "bytes per launch (ncu dram read + write)",
+                        "algorithmic_bytes": algorithmic_bytes(w),
+                        "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
+           "wall_ms_per_step": t_wall * 1e3 / steps}
+    launches = launches_per_step * (warmup + steps)
+    del q, k, v, q_cat, o, lse
+    return out, step_ms, launches, plan
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -283,121 +514,92 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    status = cpa.new_status(dev)
+    clk = ClockSampler(local).start()
+    launches = 0
+
+    # ---- headline: the 32K workload ----
     w = W.WORKLOADS[args.workload]
     strategy = w.strategies[0]
     inputs = W.make_inputs(w)
-    q = inputs["q"].to(dev)
-    k = inputs["k"].to(dev)
-    v = k[:, :, : w.dv] if w.v_is_k_prefix else inputs["v"].to(dev)
-    N, Hq, dv = w.total_new, w.Hq, w.dv
-    status = cpa.new_status(dev)
-    stream = torch.cuda.current_stream(dev)
-    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, device=dev)
-    ws = {"q_cat": torch.empty_like(q),
-          "o": torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev),
-          "lse": torch.empty((N, Hq), dtype=torch.float32, device=dev)}
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-
-    token_rows = strategy == "zigzag"   # zigzag shards are runs of consecutive tokens
-
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        cpa.cp_shard_plan(plan, status=status, stream=stream)
-        if not token_rows:
-            qc = cpa.cp_restore(q, plan.gather_idx[:N], out=ws["q_cat"], status=status,
-                                stream=stream)
-        if ev:
-            ev[1].record(stream)
-        if token_rows:
-            # zigzag: each shard's rows are token runs; the kernel reads its
-            # queries and writes O and LSE by token index (no gather, no restore)
-            cpa.cp_attn_prefill(plan.segs, q, k, v, w.scale, num_segs=plan.total_segs,
-                                tiles=plan.tiles, num_tiles=plan.total_tiles, out=ws["o"],
-                                lse=ws["lse"], status=status, stream=stream)
-        else:
-            # attention of every shard; the store puts O and LSE in causal order
-            cpa.cp_attn_partial_restore(plan.segs, qc, k, v, w.scale, plan.gather_idx,
-                                        num_out_rows=N, num_segs=plan.total_segs,
-                                        tiles=plan.tiles, num_tiles=plan.total_tiles,
-                                        out=ws["o"], lse=ws["lse"], status=status,
-                                        stream=stream)
-        if ev:
-            ev[2].record(stream)
-
-    launches_per_step = 3 + (0 if token_rows else 1) + 1  # plan, [Q gather], attention
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    cpa.check_status(status, "warmup")
-
-    evs = [[E() for _ in range(3)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            step(evs[i])
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall0
-    if world > 1:
-        dist.barrier()
-    cpa.check_status(status, "timed steps")
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    prep_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    main, step_ms, n, plan = bench_full_kv(w, strategy, inputs, dev, stream, pk, flush,
+                                           args.steps, args.warmup, clk, status, "main", world)
+    launches += n
     total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
-    flops = attention_flops(w)
-    value = job_throughput(flops, world, args.steps, total_ms)
-    pk = peaks()
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    achieved = flops / (attn_avg_ms * 1e-3) / 1e12
-
+    value = job_throughput(main["attention_flops"], world, args.steps, total_ms)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_of(w, {"parallelism": f"replicas{world}"}),
-            "wall_ms_per_step": t_wall * 1e3 / args.steps,
-            "breakdown_ms": {("plan" if token_rows else "plan_and_q_gather"):
-                             sum(prep_ms) / len(prep_ms),
-                             ("attention_token_rows" if token_rows else
-                              "attention_with_restore_store"): attn_avg_ms},
-            "roofline": {"kernel": kernel_label(w),
-                         "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                         "traffic": profiled_traffic(PROFILE_MD.get(w.name, "")),
-                         "traffic_unit": "bytes per launch (ncu dram read + write)",
-                         "algorithmic_bytes": algorithmic_bytes(w),
-                         "peak_source": f"{pk['source']} bf16 burst (MEASURED_PEAKS.json)"},
-            "restore": bench_restore(args, w, plan, ws, flush, dev, stream, pk, status),
-            "clocks": clk.summary(),
-            "gpu_launches": launches_per_step * args.steps}
-    line["gpu_launches"] += line["restore"].pop("launches")
+            "data": "synthetic", "config": config_of(w, world, strategy),
+            "wall_ms_per_step": main["wall_ms_per_step"],
+            "breakdown_ms": main["breakdown_ms"], "roofline": main["roofline"]}
+    line["restore"] = bench_restore(args, w, plan, dev, stream, pk, status, flush, clk)
+    launches += line["restore"].pop("launches")
 
+    per = {"3 llama8b_32k zigzag": {"see": "top-level value, roofline and cpu_baseline",
+                                    "tflops": main["tflops"],
+                                    "frac_of_bf16_peak": main["roofline"]["frac"]}}
+    small = {}
+    if not args.skip_configs:
+        for name, strat in (("single1k_d64", "zigzag"), ("varlen6_gqa", "zigzag"),
+                            ("varlen6_gqa", "interleave"), ("mla_16k", "interleave")):
+            wc = W.WORKLOADS[name]
+            inp = small.get(name) or W.make_inputs(wc)
+            small[name] = inp
+            tag = {"single1k_d64": "1", "varlen6_gqa": "2", "mla_16k": "4"}[name]
+            # the small workloads are launch-bound: more steps for a stable mean
+            steps = args.steps if wc.total_new > 8192 else max(args.steps, 100)
+            r, _, n, _ = bench_full_kv(wc, strat, inp, dev, stream, pk, flush, steps,
+                                       args.warmup, clk, status, f"cfg{tag}-{strat}", world)
+            launches += n
+            per[f"{tag} {name} {strat}"] = r
+            if name == "mla_16k":
+                del inp
+                small.pop(name)
+            torch.cuda.empty_cache()
     if not args.skip_merge:
-        line["merge"] = bench_merge(args, dev, stream, pk)
-        line["gpu_launches"] += line["merge"].pop("launches")
-    if not args.skip_merge:
-        line["partial_kv"] = bench_partial_kv(args, dev, stream, pk)
-        line["gpu_launches"] += line["partial_kv"].pop("launches")
-        line["pass_q"] = bench_pass_q(args, dev, stream, pk)
-        line["gpu_launches"] += line["pass_q"].pop("launches")
-        line["merge_sweep"] = bench_merge_sweep(args, dev, stream, pk)
-        line["gpu_launches"] += line["merge_sweep"].pop("launches")
+        per["5a partialkv_128k"] = bench_128k(args, dev, stream, pk, status, clk)
+        launches += per["5a partialkv_128k"].pop("launches")
+        per["5b merge_sweep"] = bench_merge_sweep(args, dev, stream, pk, clk)
+        launches += per["5b merge_sweep"].pop("launches")
     if not args.skip_e2e:
-        line["e2e"] = bench_e2e(args, w, inputs, dev, stream, world)
-    del q, k, v, ws, flush
+        line["e2e"] = bench_e2e(args, w, inputs, dev, world, clk)
+        launches += line["e2e"].pop("launches")
+    clk.stop()
+    line["clocks"] = clk.summary()
+    line["clocks"]["main_region"] = clk.summary(["main"])
+    line["gpu_launches"] = launches
+    del flush
     torch.cuda.empty_cache()
-    if rank == 0 and not args.skip_cpu:
-        rate, rows, dt, threads = oracle_sample_rate(w, inputs, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": rate / 1e12, "unit": UNIT, "cores": threads,
-                                "kind": "oracle",
-                                "sample": f"{rows} random query rows x all {w.Hq} heads of the "
-                                          f"workload in {dt:.1f} s, fp64 NumPy; rate "
-                                          f"extrapolated to the full workload"}
+
+    # ---- CPU oracle beside every workload (rank 0, N = 1 only) ----
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        line["cpu_baseline"] = oracle_baseline(
+            w, inputs, sample_rows(w, ORACLE_SAMPLE_ROWS, 7), w.name)
+        for key, r in per.items():
+            if key.startswith("3 ") or key.startswith("5"):
+                continue
+            name = key.split()[1]
+            wc = W.WORKLOADS[name]
+            inp = small.get(name) or W.make_inputs(wc)
+            if key.startswith("2 ") and "cpu_baseline" in per.get("2 varlen6_gqa zigzag", {}):
+                r["cpu_baseline"] = dict(per["2 varlen6_gqa zigzag"]["cpu_baseline"],
+                                         note="the same oracle run as the zigzag entry: the "
+                                              "oracle computes the unsharded result")
+                continue
+            r["cpu_baseline"] = oracle_baseline(
+                wc, inp, sample_rows(wc, ORACLE_SAMPLE_ROWS if wc.total_new > 8192 else
+                                     wc.total_new, 7), name)
+        if "5a partialkv_128k" in per:
+            wc = W.WORKLOADS[MERGE_WORKLOAD]
+            per["5a partialkv_128k"]["cpu_baseline"] = oracle_baseline(
+                wc, W.make_inputs(wc), sample_rows(wc, ORACLE_SAMPLE_ROWS, 7), MERGE_WORKLOAD)
+        if "5b merge_sweep" in per:
+            per["5b merge_sweep"]["cpu_baseline"] = oracle_decode_baseline()
+    line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -405,19 +607,19 @@ def run_ours(args):
     return 0
 
 
-def bench_restore(args, w, plan, ws, flush, dev, stream, pk, status):
+def bench_restore(args, w, plan, dev, stream, pk, status, flush, clk):
     """The standalone restore kernel (cp_restore of O and LSE, the two-pass
-    path), on the step's outputs taken in cat order; L2 flushed between reps."""
+    path) on rows in cat order; L2 flushed between reps."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
 
     N, Hq, dv = w.total_new, w.Hq, w.dv
-    o_cat = ws["o"]          # any [N, Hq, dv] rows will do: the kernel is a row gather
-    lse_cat = ws["lse"]
+    o_cat = torch.randn((N, Hq, dv), device=dev).to(torch.bfloat16)
+    lse_cat = torch.randn((N, Hq), device=dev)
     o = torch.empty_like(o_cat)
     lse = torch.empty_like(lse_cat)
-    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    cpa.cp_shard_plan(plan, status=status, stream=stream)
 
     def run():
         cpa.cp_restore(o_cat, plan.restore_idx[:N], out=o, status=status, stream=stream)
@@ -426,199 +628,177 @@ def bench_restore(args, w, plan, ws, flush, dev, stream, pk, status):
     for _ in range(3):
         run()
     reps = max(3, args.steps // 2)
-    evs = [(E(), E()) for _ in range(reps)]
-    for a, b in evs:
-        flush.zero_()
-        a.record(stream)
-        run()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
+    evs = _events(reps, 2)
+    with clk.region("restore"):
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            run()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
     cpa.check_status(status, "restore")
     ms = sum(a.elapsed_time(b) for a, b in evs) / reps
     nbytes = 2 * (N * Hq * dv * 2) + 2 * (N * Hq * 4)
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_per_call": nbytes,
-            "ms": ms, "launches": 2 * (3 + reps),
+            "ms": ms, "launches": 3 + 2 * (3 + reps),
+            "roofline": {"kernel": "row_gather_kernel", "bound": "hbm", "achieved": gbs,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                         "traffic": None},
             "path": "cp_restore of O then LSE (the step itself fuses the restore into the "
                     "attention store)"}
 
 
-def bench_merge(args, dev, stream, pk):
-    """LSE merge of the 128K partial-KV decomposition (136 fp32 partials)."""
+def partial_slots(plan, kv_block):
+    """Partial rows of a partial-KV decomposition laid out per segment of the
+    plan (block j of segment s at rows base_s + j * q_len_s; a segment whose
+    last row is at position P sees P // kv_block + 1 blocks).
+    Returns ([(q_row0, q_len, base, blocks)], total rows)."""
+    import context_causal_attention_cp_gb300 as cpa
+    out, base = [], 0
+    for s in cpa.segments_host(plan):
+        nb = (s["q_pos0"] + (s["q_len"] - 1) * s["q_pos_step"]) // kv_block + 1
+        out.append((s["q_row0"], s["q_len"], base, nb))
+        base += nb * s["q_len"]
+    return out, base
+
+
+def bench_128k(args, dev, stream, pk, status, clk):
+    """The 131072-token partial-KV workload: the LSE merge of its 136 fp32
+    partials (16 cp_lse_merge calls on synthetic partials, 18.4 GB read), the
+    pass-KV step in one library call, and the same workload through the
+    pass-Q ring."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
     from context_causal_attention_cp_gb300 import workloads as W
 
     w = W.WORKLOADS[MERGE_WORKLOAD]
-    N, Hq, dv, B = w.total_new, w.Hq, w.dv, w.kv_block
-    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev)
-    segs = cpa.segments_host(plan)
-    layout, slot_rows = cpa.api.partial_kv_layout(segs, B)
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    out = {"workload": f"{w.name}: {w.description}", "config": config_of(w)}
+    launches = 0
+
+    # -- merge of the partials (synthetic values; the kernel reads them all) --
+    torch.cuda.empty_cache()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
+                         status=status)
+    slots, slot_rows = partial_slots(plan, w.kv_block)
     g = torch.Generator(device=dev).manual_seed(5)
     parts_o = torch.randn((slot_rows, Hq, dv), device=dev, generator=g)
     parts_l = torch.randn((slot_rows, Hq), device=dev, generator=g) * 3 + 10
-    out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
-    status = cpa.new_status(dev)
 
     def merge_all():
-        for si, s in enumerate(segs):
-            base, nb = layout[si]
-            ql = s["q_len"]
+        for q_row0, ql, base, nb in slots:
             cpa.cp_lse_merge(parts_o[base: base + nb * ql].view(nb, ql, Hq, dv),
                              parts_l[base: base + nb * ql].view(nb, ql, Hq),
-                             dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql], out=out,
-                             lse_out=lse, num_out_rows=N, status=status, stream=stream)
+                             dst_rows=plan.gather_idx[q_row0: q_row0 + ql], out=o, lse_out=lse,
+                             num_out_rows=N, status=status, stream=stream)
 
     for _ in range(3):
         merge_all()
-    reps = max(3, args.steps // 2)
+    reps = max(3, args.steps // 4)
     times = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        merge_all()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
+    with clk.region("merge"):
+        for _ in range(reps):
+            e0, e1 = E(), E()
+            e0.record(stream)
+            merge_all()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
     cpa.check_status(status, "merge")
     read = slot_rows * Hq * (dv + 1) * 4
     written = N * Hq * (dv * 2 + 4)
     ms = sorted(times)[len(times) // 2]
     gbs = (read + written) / (ms * 1e-3) / 1e9
+    launches += len(slots) * (reps + 3) + 3
+    out["merge"] = {"kernel": "lse_merge_kernel", "ms": ms, "gbs": gbs,
+                    "frac_of_hbm": gbs / pk["hbm_gbs"], "bytes_read": read,
+                    "bytes_written": written, "parts": slot_rows // (N // 16),
+                    "roofline": {"kernel": "lse_merge_kernel / lse_merge_batched_kernel",
+                                 "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None},
+                    "note": "partials exceed L2 (18 GB), so every read comes from HBM"}
     del parts_o, parts_l
-    return {"workload": f"{w.name}: {w.description}", "kernel": "lse_merge_kernel",
-            "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"],
-            "bytes_read": read, "bytes_written": written, "parts": slot_rows // (N // 16),
-            "launches": len(segs) * (reps + 3),
-            "note": "partials exceed L2 (18 GB), so every read comes from HBM"}
-
-
-def bench_partial_kv(args, dev, stream, pk):
-    """The 128K partial-KV decomposition as one library call per step.
-
-    Step = plan + query gather + cp_attn_partial_kv (layout, split-KV
-    attention over the 136 visible (query block, KV block) pairs, fp32
-    partials in an 18.4 GB workspace, LSE merge scattered to causal order)."""
-    import torch
-
-    import context_causal_attention_cp_gb300 as cpa
-    from context_causal_attention_cp_gb300 import workloads as W
-
     torch.cuda.empty_cache()
-    w = W.WORKLOADS[MERGE_WORKLOAD]
+
+    # -- the pass-KV step in one call, then the pass-Q ring --
     inputs = W.make_inputs(w)
     q = inputs["q"].to(dev)
     k = inputs["k"].to(dev)
     v = inputs["v"].to(dev)
     del inputs
-    N, Hq, dv = w.total_new, w.Hq, w.dv
-    status = cpa.new_status(dev)
-    plan = cpa.alloc_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev)
-    nbytes, _ = cpa.cp_partial_kv_workspace_size(w.new_lens, w.prefix_lens, w.cp_size, "zigzag",
-                                                 w.kv_block, Hq, dv)
+    nbytes = cpa.cp_partial_kv_workspace_size(w.new_lens, w.prefix_lens, w.cp_size, "zigzag",
+                                              w.kv_block, Hq, dv)[0]
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     q_cat = torch.empty_like(q)
-    out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
 
-    def step():
+    def step_kv():
         cpa.cp_shard_plan(plan, status=status, stream=stream)
         cpa.cp_restore(q, plan.gather_idx[:N], out=q_cat, status=status, stream=stream)
-        cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
-                               prefix_lens=w.prefix_lens, workspace=ws, out=out, lse_out=lse,
-                               status=status, stream=stream)
+        cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block, workspace=ws, out=o,
+                               lse_out=lse, status=status, stream=stream)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize(dev)
-    reps = 3
-    times = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
+    def timed(fn, region, reps=3):
+        for _ in range(3):
+            fn()
         torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
+        ts = []
+        with clk.region(region):
+            for _ in range(reps):
+                e0, e1 = E(), E()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[len(ts) // 2], reps + 3
+
+    ms, n = timed(step_kv, "partial_kv")
     cpa.check_status(status, "partial kv")
-    ms = sorted(times)[len(times) // 2]
+    launches += (3 + 1 + 3) * n
     flops = attention_flops(w)
     tf = flops / (ms * 1e-3) / 1e12
-    del ws, q, k, v, q_cat, out, lse
+    out["partial_kv"] = {"ms_per_step": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+                         "workspace_bytes": nbytes,
+                         "path": "cp_shard_plan + cp_restore + cp_attn_partial_kv (one call: "
+                                 "layout, split-KV attention, merge + restore)"}
+    del ws
     torch.cuda.empty_cache()
-    return {"workload": f"{w.name}: {w.description}", "ms_per_step": ms,
-            "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
-            "workspace_bytes": nbytes, "launches": (3 + 1 + 3) * (reps + 3),
-            "path": "cp_shard_plan + cp_restore + cp_attn_partial_kv (one call: layout, "
-                    "split-KV attention, merge + restore)"}
 
-
-def bench_pass_q(args, dev, stream, pk):
-    """The same 128K workload through the pass-Q ring (KV resident in 2C
-    blocks per rank, each query shard carried round the ring with an fp32
-    accumulator; one accumulate launch per (hop, resident block) covers all
-    ranks, each segment with its own key window); the pass-KV figure is the
-    partial_kv entry.  Step = plan + query gather + the ring + restore of O
-    and LSE to causal order."""
-    import torch
-
-    import context_causal_attention_cp_gb300 as cpa
-    from context_causal_attention_cp_gb300 import workloads as W
-
-    torch.cuda.empty_cache()
-    w = W.WORKLOADS[MERGE_WORKLOAD]
-    inputs = W.make_inputs(w)
-    q = inputs["q"].to(dev)
-    k = inputs["k"].to(dev)
-    v = inputs["v"].to(dev)
-    del inputs
-    N, Hq, dv = w.total_new, w.Hq, w.dv
-    status = cpa.new_status(dev)
-    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
-                         status=status)
     sched = cpa.pass_q_schedule(plan)
-    q_cat = torch.empty_like(q)
     acc = (torch.empty((N, Hq, dv), dtype=torch.float32, device=dev),
            torch.empty((N, Hq), dtype=torch.float32, device=dev),
            torch.empty((N, Hq), dtype=torch.float32, device=dev))
-    o = torch.empty((N, Hq, dv), dtype=torch.float32, device=dev)
-    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    o32 = torch.empty((N, Hq, dv), dtype=torch.float32, device=dev)
 
-    def step():
+    def step_q():
         cpa.cp_shard_plan(plan, status=status, stream=stream)
         cpa.cp_restore(q, plan.gather_idx[:N], out=q_cat, status=status, stream=stream)
         o_cat, l_cat = cpa.cp_pass_q_attention(q_cat, k, v, plan, w.scale, schedule=sched,
                                                status=status, stream=stream, out=acc)
-        cpa.cp_restore(o_cat, plan.restore_idx[:N], out=o, status=status, stream=stream)
+        cpa.cp_restore(o_cat, plan.restore_idx[:N], out=o32, status=status, stream=stream)
         cpa.cp_restore(l_cat, plan.restore_idx[:N], out=lse, status=status, stream=stream)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize(dev)
-    reps = 3
-    times = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        times.append(e0.elapsed_time(e1))
+    ms, n = timed(step_q, "pass_q")
     cpa.check_status(status, "pass q")
-    ms = sorted(times)[len(times) // 2]
-    tf = attention_flops(w) / (ms * 1e-3) / 1e12
-    choice, score = cpa.cp_select_pass(N, 0, Hq, w.Hkv, "message")
-    del q, k, v, q_cat, acc, o, lse
+    launches += (3 + 1 + 1 + sched.num_launches + 2) * n
+    tf = flops / (ms * 1e-3) / 1e12
+    choice, _ = cpa.cp_select_pass(N, 0, Hq, w.Hkv, "message")
+    out["pass_q"] = {"ms_per_step": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
+                     "accumulate_launches": sched.num_launches,
+                     "selector_message_rule": choice,
+                     "path": "cp_shard_plan + cp_restore + cp_attn_pass_q (the library's ring "
+                             "schedule: one accumulate launch per hop and resident KV block, all "
+                             "ranks in one launch with per-segment key windows) + cp_restore of "
+                             "O and LSE"}
+    out["launches"] = launches
+    del q, k, v, q_cat, acc, o32, o, lse
     torch.cuda.empty_cache()
-    return {"workload": f"{w.name}: {w.description}", "ms_per_step": ms, "tflops": tf,
-            "frac_of_bf16_peak": tf / pk["bf16_tflops"], "accumulate_launches": len(sched),
-            "launches": (3 + 1 + len(sched) + 2) * (reps + 3),
-            "selector_message_rule": choice,
-            "path": "cp_shard_plan + cp_restore + cp_pass_q_attention (one "
-                    "cp_attn_partial_accumulate per hop and resident KV block, all ranks "
-                    "in one launch with per-segment key windows) + cp_restore of O and LSE"}
+    return out
 
 
 def decode_ranks(q, k, v, shards):
@@ -638,7 +818,7 @@ def decode_ranks(q, k, v, shards):
     return q_rank, k_rank, v_rank, segs_host
 
 
-def bench_merge_sweep(args, dev, stream, pk):
+def bench_merge_sweep(args, dev, stream, pk, clk):
     """Decode-style merge sweep: 64 single-token queries x 32 heads over 65536
     keys, key i resident on shard i mod 8.  Each rank's KV cache holds its
     tokens contiguously (laid out once before timing, as a KV cache is) and
@@ -698,22 +878,23 @@ def bench_merge_sweep(args, dev, stream, pk):
                              workspace=ws_all, status=status, stream=stream)
         merge()
 
-    def time_steps(fn, reps=50):
+    def time_steps(fn, region, reps=50):
         for _ in range(5):
             fn()
         torch.cuda.synchronize(dev)
         e0, e1 = E(), E()
         with torch.cuda.stream(stream):
             torch.cuda._sleep(300_000_000)  # let the host queue the launches ahead of the GPU
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        with clk.region(region):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e3 / reps
 
-    per_rank_us = time_steps(decode_step_per_rank)
-    step_us = time_steps(decode_step)
+    per_rank_us = time_steps(decode_step_per_rank, "decode_per_rank")
+    step_us = time_steps(decode_step, "decode")
     reps = 50
     e0, e1 = E(), E()
     with torch.cuda.stream(stream):
@@ -736,16 +917,24 @@ def bench_merge_sweep(args, dev, stream, pk):
     cpa.check_status(status, "merge sweep")
     cold_us = sorted(x.elapsed_time(y) for x, y in cold)[len(cold) // 2] * 1e3
     nbytes = S * nq * Hq * (dv + 1) * 4 + nq * Hq * (dv + 1) * 4
+    kv_bytes = 2 * m["kv_tokens"] * m["Hkv"] * m["d"] * 2
     # both steps: one sizing call + 5 warm-up + 50 timed; then the merge alone
     launches = 3 + (3 * S + 1) * 55 + 3 + 4 * 55 + reps + 20
     del q, k, v, po, pl, flush
     torch.cuda.empty_cache()
     return {"queries": nq, "heads": Hq, "kv_tokens": m["kv_tokens"], "shards": S,
             "decode_step_us": step_us, "decode_kv_block": DECODE_KV_BLOCK,
-            "decode_step_per_rank_calls_us": per_rank_us, "merge_bytes": nbytes,
+            "decode_step_per_rank_calls_us": per_rank_us,
+            "decode_kv_gbs": kv_bytes / (step_us * 1e-6) / 1e9,
+            "merge_bytes": nbytes,
             "merge_warm_us": warm_us, "merge_warm_gbs": nbytes / (warm_us * 1e-6) / 1e9,
             "merge_flushed_us": cold_us, "merge_flushed_gbs": nbytes / (cold_us * 1e-6) / 1e9,
             "merge_flushed_frac_of_hbm": nbytes / (cold_us * 1e-6) / 1e9 / pk["hbm_gbs"],
+            "roofline": {"kernel": "decode step (split-KV attention + merge)", "bound": "hbm",
+                         "achieved": kv_bytes / (step_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": kv_bytes / (step_us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                         "traffic": None,
+                         "note": "K and V of all 65536 keys (268 MB) over the whole step"},
             "launches": launches,
             "path": "one cp_attn_split_kv over the 8 ranks' segments (each rank's KV cache "
                     "contiguous, keys in blocks of DECODE_KV_BLOCK, merged per rank) + "
@@ -753,17 +942,47 @@ def bench_merge_sweep(args, dev, stream, pk):
                     "(blocks of 512) on strided views of the original-order KV"}
 
 
-def bench_e2e(args, w, inputs, dev, stream, world=1):
-    """Same step through the public API with pinned host inputs and outputs.
+def oracle_decode_baseline():
+    """The oracle's decode step of the merge sweep, in full, in one process:
+    every shard's partial (O_j, L_j) of the 64 queries against its keys
+    (oracle.attention.decode_attention), then the LSE merge of the 8 partials
+    (oracle.merge.lse_merge)."""
+    import numpy as np
 
-    Every step uploads its q, k, v from pinned host memory, runs plan ->
-    gather -> attention (restore fused into the store) and downloads O and
-    LSE to pinned host memory (api.PrefillPipeline: batch n's attention
-    overlaps batch n+1's upload and batch n-1's download).  The timed region
-    runs from before the first upload to after the last download.  With N
-    ranks the replicas start together after a barrier; the figure is the work
-    of all ranks over the slowest rank's time, and the bytes are the whole
-    job's."""
+    from context_causal_attention_cp_gb300 import workloads as W
+    from oracle import attention as oatt
+    from oracle import merge as omerge
+
+    m = W.MERGE_SWEEP
+    inp = W.make_merge_sweep_inputs()
+    f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    q, k, v = f64(inp["q"]), f64(inp["k"]), f64(inp["v"])
+    S = m["shards"]
+    t0 = time.perf_counter()
+    parts = [oatt.decode_attention(q, k, v, m["scale"], np.arange(j, m["kv_tokens"], S))
+             for j in range(S)]
+    t1 = time.perf_counter()
+    omerge.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    t2 = time.perf_counter()
+    nbytes = S * m["queries"] * m["Hq"] * (m["dv"] + 1) * 4 + m["queries"] * m["Hq"] * \
+        (m["dv"] + 1) * 4
+    return {"decode_step_us": (t2 - t0) * 1e6, "merge_us": (t2 - t1) * 1e6,
+            "merge_gbs": nbytes / (t2 - t1) / 1e9, "unit": "us", "cores": 1, "kind": "oracle",
+            "extrapolated": False,
+            "sample": "the whole decode step in fp64 NumPy in one process: 8 shard partials of "
+                      "64 queries x 32 heads over 8192 keys each, then their LSE merge"}
+
+
+def bench_e2e(args, w, inputs, dev, world, clk):
+    """The same workload end to end through the C ABI's host-to-host call
+    (cp_prefill_host): every step uploads its q, k, v from pinned host memory,
+    builds the plan, runs the attention of all shards (O / LSE in causal token
+    order) and downloads O and LSE to pinned host memory; the library overlaps
+    step i's attention with step i+1's upload and step i-1's download on three
+    streams.  The timed region runs from before the first upload to after the
+    last download.  With N ranks the replicas start together after a barrier;
+    the figure is the work of all ranks over the slowest rank's time, and the
+    bytes are the whole job's."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -772,37 +991,42 @@ def bench_e2e(args, w, inputs, dev, stream, world=1):
     hk = inputs["k"].pin_memory()
     hv = None if w.v_is_k_prefix else inputs["v"].pin_memory()
     N, Hq, dv = w.total_new, w.Hq, w.dv
-    ho = torch.empty((N, Hq, dv), dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty((N, Hq), dtype=torch.float32).pin_memory()
-    pipe = cpa.PrefillPipeline(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], Hq, w.Hkv,
-                               w.d, dv, w.scale, v_is_k_prefix=w.v_is_k_prefix, device=dev)
-    for _ in range(3):
-        pipe.submit(hq, hk, hv, ho, hl)
-    pipe.synchronize()
-    torch.cuda.synchronize(dev)
+    outs = [(torch.empty((N, Hq, dv), dtype=torch.bfloat16).pin_memory(),
+             torch.empty((N, Hq), dtype=torch.float32).pin_memory()) for _ in range(2)]
     reps = max(3, args.steps // 2)
+    batches = [(hq, hk, hv) + outs[i % 2] for i in range(reps)]
+    status = cpa.new_status(dev)
+    strategy = w.strategies[0]
+    # warm-up call (workspace and streams reused by the timed call)
+    ws, streams = cpa.cp_prefill_host(w.new_lens, w.prefix_lens, w.cp_size, strategy, Hq, w.Hkv,
+                                      w.d, dv, w.scale, batches[:3],
+                                      v_is_k_prefix=w.v_is_k_prefix, status=status, device=dev)
+    torch.cuda.synchronize(dev)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(pipe.s_up)
-    for _ in range(reps):
-        pipe.submit(hq, hk, hv, ho, hl)
-    pipe.s_down.wait_stream(pipe.s_up)
-    pipe.s_down.wait_stream(pipe.s_comp)
-    e1.record(pipe.s_down)
-    pipe.synchronize()
+    with clk.region("e2e"):
+        e0.record(streams[1])
+        cpa.cp_prefill_host(w.new_lens, w.prefix_lens, w.cp_size, strategy, Hq, w.Hkv, w.d, dv,
+                            w.scale, batches, v_is_k_prefix=w.v_is_k_prefix, workspace=ws,
+                            status=status, streams=streams, device=dev)
+        e1.record(streams[2])
+        streams[2].synchronize()
+    torch.cuda.synchronize(dev)
+    cpa.check_status(status, "e2e")
     ms = reduce_max_over_ranks(e0.elapsed_time(e1) / reps, world, dev)
     h2d = world * (hq.numel() * 2 + hk.numel() * 2 + (0 if hv is None else hv.numel() * 2))
-    d2h = world * (ho.numel() * 2 + hl.numel() * 4)
-    del pipe
+    d2h = world * (N * Hq * dv * 2 + N * Hq * 4)
+    per_step = 4 if strategy == "zigzag" else 5
+    del ws
     torch.cuda.empty_cache()
     return {"value": world * attention_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "steps": reps,
-            "path": "api.PrefillPipeline: per step, pinned host q/k/v upload, plan, gather, "
-                    "attention with the restore in its store, O and LSE download; uploads and "
-                    "downloads overlap neighbouring steps' attention"}
+            "steps": reps, "launches": per_step * (3 + reps),
+            "path": "C ABI cp_prefill_host: per step, pinned host q/k/v upload, plan, "
+                    "attention with O / LSE stored in token order, O and LSE download; "
+                    "uploads and downloads overlap neighbouring steps' attention"}
 
 
 def run_profile_case(args):
@@ -814,8 +1038,10 @@ def run_profile_case(args):
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
     merge4:    query block 3 of that workload (4 partials, 0.54 GB read; the
                few-partial kernel).
-    partial_kv: the whole 128K partial-KV call (layout, split-KV attention,
-               fused merge + restore), as in the partial_kv entry.
+    partial_kv: the partial-KV call (layout, split-KV attention, fused merge
+               + restore) on the workload given by --workload (default: the
+               128K workload; its counter captures use llama8b_32k, a quarter
+               of the 128K work per launch).
     restore:   the O restore of the default workload (268 MB each way).
     decode:    the decode step of the merge sweep (one split-KV call over
                the 8 ranks' KV caches, then the merge of the 8 partials)."""
@@ -827,18 +1053,17 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     status = cpa.new_status(dev)
     if args.profile_case == "partial_kv":
-        w = W.WORKLOADS[MERGE_WORKLOAD]
+        w = W.WORKLOADS[MERGE_WORKLOAD if args.workload == WORKLOAD else args.workload]
+        kv_block = w.kv_block or 8192
         inputs = W.make_inputs(w)
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
                              status=status)
         q = cpa.cp_restore(inputs["q"].to(dev), plan.gather_idx[: w.total_new], status=status)
         k, v = inputs["k"].to(dev), inputs["v"].to(dev)
         del inputs
-        ws = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
-                                    prefix_lens=w.prefix_lens, status=status)[2]
+        ws = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, kv_block, status=status)[2]
         run = lambda: cpa.cp_attn_partial_kv(  # noqa: E731
-            plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens, prefix_lens=w.prefix_lens,
-            workspace=ws, status=status)
+            plan, q, k, v, w.scale, kv_block, workspace=ws, status=status)
     elif args.profile_case == "decode":
         m = W.MERGE_SWEEP
         inputs = W.make_merge_sweep_inputs()
@@ -907,11 +1132,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--ref-step-seconds", type=float, default=4.0)
+    ap.add_argument("--ref-rows-per-step", type=int, default=128,
+                    help="query rows (x all heads) the reference arm's oracle runs per step")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-merge", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true")
     ap.add_argument("--profile-case",
                     choices=["attention", "merge", "merge4", "partial_kv", "restore", "decode"],
                     default=None,

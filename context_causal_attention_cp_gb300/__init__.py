@@ -7,8 +7,7 @@ absence raises: there is no CPU fallback.
 """
 
 from .api import (  # noqa: F401
-    PassQLaunch,
-    PrefillPipeline,
+    PassQSchedule,
     ShardPlan,
     alloc_plan,
     check_status,
@@ -20,16 +19,18 @@ from .api import (  # noqa: F401
     cp_attn_split_kv,
     cp_lse_merge,
     cp_partial_kv_workspace_size,
-    cp_partial_kv_attention,
+    cp_partial_kv_workspace_size_segs,
     cp_pass_q_attention,
     cp_prefill_attention,
+    cp_prefill_host,
+    cp_prefill_host_workspace_size,
     cp_restore,
     cp_select_pass,
     cp_shard_plan,
     cp_shard_plan_sizes,
     make_plan,
     new_status,
-    pass_q_kv_blocks,
     pass_q_schedule,
+    pass_q_schedule_host,
     segments_host,
 )

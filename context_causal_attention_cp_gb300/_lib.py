@@ -56,9 +56,20 @@ SIGNATURES = {
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
     "cp_partial_kv_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32,
-                                           ctypes.POINTER(ctypes.c_int64), c_i32p]),
+                                           ctypes.POINTER(ctypes.c_int64), c_i32p, c_i32p]),
     "cp_partial_kv_workspace_size_segs": (i32, [vp, i32, i32, i32, i32,
-                                                ctypes.POINTER(ctypes.c_int64), c_i32p]),
+                                                ctypes.POINTER(ctypes.c_int64), c_i32p, c_i32p]),
+    "cp_pass_q_schedule_size": (i32, [c_i32p, c_i32p, i32, i32, i32, c_i32p, c_i32p]),
+    "cp_pass_q_schedule": (i32, [c_i32p, c_i32p, i32, i32, i32, c_i32p, c_i32p, c_i32p, vp,
+                                 c_i32p, c_i32p]),
+    "cp_attn_pass_q": (i32, [vp, vp, c_i32p, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32, i32,
+                             i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp]),
+    "cp_prefill_host_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32, i32,
+                                             i32, ctypes.POINTER(ctypes.c_int64)]),
+    "cp_prefill_host": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                              i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                              ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                              i64, vp, vp, vp, vp]),
     "cp_attn_partial_kv": (i32, [vp, i32, vp, i32, vp, i32, vp, i64, i64, vp, i64, i64, i32,
                                  i32, i32, i32, i32, ctypes.c_float, i32, i32, i32, vp, vp, i32,
                                  vp, i32, vp, i64, vp, vp]),

@@ -132,6 +132,8 @@ class ShardPlan:
     new_lens_dev: torch.Tensor
     prefix_lens_dev: torch.Tensor
     num_reqs: int
+    new_lens: List[int]          # host copies of the lengths the plan was made from
+    prefix_lens: List[int]
 
     @property
     def total_rows(self):
@@ -159,7 +161,8 @@ def alloc_plan(new_lens, prefix_lens, cp_size, strategy, device="cuda") -> Shard
         restore_idx=torch.empty(max(N, 1), **i32), tiles=torch.empty((max(T, 1), 2), **i32),
         new_lens_dev=torch.tensor([int(x) for x in new_lens] or [0], **i32),
         prefix_lens_dev=torch.tensor([int(x) for x in prefix_lens] or [0], **i32),
-        num_reqs=len(new_lens))
+        num_reqs=len(new_lens), new_lens=[int(x) for x in new_lens],
+        prefix_lens=[int(x) for x in prefix_lens])
 
 
 def cp_shard_plan(plan: ShardPlan, status=None, stream=None) -> ShardPlan:
@@ -408,80 +411,73 @@ def cp_prefill_attention(q, k, v, plan: ShardPlan, scale, *, status=None, stream
     return o, lse
 
 
-class PrefillPipeline:
-    """Full-KV CP prefill over a stream of same-shaped batches held in host memory.
+def cp_prefill_host_workspace_size(new_lens, prefix_lens, cp_size, strategy, Hq, Hkv, d, dv,
+                                   v_is_k_prefix=False) -> int:
+    """Device bytes cp_prefill_host needs (plan buffers and two buffer sets)."""
+    lib = L.load()
+    nl, n = _i32_array(new_lens)
+    pl, _ = _i32_array(prefix_lens)
+    nbytes = ctypes.c_int64()
+    L.check(lib.cp_prefill_host_workspace_size(nl, pl, n, cp_size, _strategy(strategy), Hq, Hkv,
+                                                d, dv, 1 if v_is_k_prefix else 0,
+                                                ctypes.byref(nbytes)),
+            "cp_prefill_host_workspace_size")
+    return nbytes.value
 
-    Every ``submit`` copies one batch's q, k (and v) from pinned host memory,
-    runs plan -> query gather -> attention with the restore fused into its
-    store, and copies O and LSE back to pinned host memory.  Two device
-    buffer sets and three CUDA streams (upload, compute, download) let batch
-    n's attention overlap batch n+1's upload and batch n-1's download; events
-    order every reuse of a buffer set.  ``synchronize`` waits for all
-    submitted batches; host outputs of a batch are valid after it.
+
+def _host(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous {dtype} {tuple(shape)}")
+
+
+def cp_prefill_host(new_lens, prefix_lens, cp_size, strategy, Hq, Hkv, d, dv, scale, batches, *,
+                    v_is_k_prefix=False, workspace=None, status=None, streams=None,
+                    device="cuda"):
+    """Host-to-host full-KV CP prefill of same-shaped batches (cp_prefill_host in cpattn.h).
+
+    ``batches``: list of (q, k, v, o, lse) host tensors (pinned for the copies
+    to overlap; v may be None with ``v_is_k_prefix``); o and lse are written.
+    ``streams``: (compute, upload, download) CUDA streams (default: three new
+    ones).  Returns (workspace, streams); the outputs are valid once the
+    download stream has completed (``streams[2].synchronize()``).
     """
-
-    def __init__(self, new_lens, prefix_lens, cp_size, strategy, Hq, Hkv, d, dv, scale, *,
-                 v_is_k_prefix=False, device="cuda"):
-        dev = torch.device(device)
-        self.N = int(sum(new_lens))
-        kv_rows = int(sum(new_lens) + sum(prefix_lens))
-        self.scale = scale
-        self.dv = dv
-        self.v_is_k_prefix = v_is_k_prefix
-        self.plan = alloc_plan(new_lens, prefix_lens, cp_size, strategy, device=dev)
-        self.status = new_status(dev)
-        bf = dict(dtype=torch.bfloat16, device=dev)
-        self.bufs = []
-        for _ in range(2):
-            b = {"q": torch.empty((self.N, Hq, d), **bf), "k": torch.empty((kv_rows, Hkv, d), **bf),
-                 "q_cat": torch.empty((self.N, Hq, d), **bf),
-                 "o": torch.empty((self.N, Hq, dv), **bf),
-                 "lse": torch.empty((self.N, Hq), dtype=torch.float32, device=dev)}
-            b["v"] = None if v_is_k_prefix else torch.empty((kv_rows, Hkv, dv), **bf)
-            self.bufs.append(b)
-        self.s_up = torch.cuda.Stream(dev)
-        self.s_comp = torch.cuda.Stream(dev)
-        self.s_down = torch.cuda.Stream(dev)
-        self.ev_up = [torch.cuda.Event() for _ in range(2)]
-        self.ev_comp = [torch.cuda.Event() for _ in range(2)]
-        self.ev_down = [torch.cuda.Event() for _ in range(2)]
-        self.n = 0
-
-    def submit(self, hq, hk, hv, ho, hlse):
-        """Queue one batch: host q, k, v (v ignored when it is a view of k) in,
-        host O [N, Hq, dv] bf16 and LSE [N, Hq] fp32 out (all pinned)."""
-        i = self.n % 2
-        b = self.bufs[i]
-        reuse = self.n >= 2
-        if reuse:
-            self.s_up.wait_event(self.ev_comp[i])     # batch n-2 is done reading set i
-        with torch.cuda.stream(self.s_up):
-            b["q"].copy_(hq, non_blocking=True)
-            b["k"].copy_(hk, non_blocking=True)
-            if b["v"] is not None:
-                b["v"].copy_(hv, non_blocking=True)
-            self.ev_up[i].record(self.s_up)
-        self.s_comp.wait_event(self.ev_up[i])
-        if reuse:
-            self.s_comp.wait_event(self.ev_down[i])   # batch n-2's outputs are downloaded
-        with torch.cuda.stream(self.s_comp):
-            v = b["k"][:, :, : self.dv] if b["v"] is None else b["v"]
-            cp_shard_plan(self.plan, status=self.status, stream=self.s_comp)
-            cp_prefill_attention(b["q"], b["k"], v, self.plan, self.scale, status=self.status,
-                                 stream=self.s_comp, fuse_restore=True,
-                                 workspace={"q_cat": b["q_cat"], "o": b["o"], "lse": b["lse"]})
-            self.ev_comp[i].record(self.s_comp)
-        self.s_down.wait_event(self.ev_comp[i])
-        with torch.cuda.stream(self.s_down):
-            ho.copy_(b["o"], non_blocking=True)
-            hlse.copy_(b["lse"], non_blocking=True)
-            self.ev_down[i].record(self.s_down)
-        self.n += 1
-
-    def synchronize(self):
-        for s in (self.s_up, self.s_comp, self.s_down):
-            s.synchronize()
-        check_status(self.status, "prefill pipeline")
+    lib = L.load()
+    dev = torch.device(device)
+    nl, n = _i32_array(new_lens)
+    pl, _ = _i32_array(prefix_lens)
+    N, KV = int(sum(new_lens)), int(sum(new_lens) + sum(prefix_lens))
+    for i, (q, k, v, o, lse) in enumerate(batches):
+        _host(q, f"q[{i}]", torch.bfloat16, (N, Hq, d))
+        _host(k, f"k[{i}]", torch.bfloat16, (KV, Hkv, d))
+        if not v_is_k_prefix:
+            _host(v, f"v[{i}]", torch.bfloat16, (KV, Hkv, dv))
+        _host(o, f"o[{i}]", torch.bfloat16, (N, Hq, dv))
+        _host(lse, f"lse[{i}]", torch.float32, (N, Hq))
+    nbytes = cp_prefill_host_workspace_size(new_lens, prefix_lens, cp_size, strategy, Hq, Hkv,
+                                            d, dv, v_is_k_prefix)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace", torch.uint8)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace needs {nbytes} bytes")
+    _status(status, workspace)
+    if streams is None:
+        streams = tuple(torch.cuda.Stream(dev) for _ in range(3))
+    nb = len(batches)
+    ptrs = lambda xs: (ctypes.c_void_p * max(1, nb))(  # noqa: E731
+        *[x.data_ptr() if x is not None else None for x in xs])
+    q_p, k_p = ptrs([b[0] for b in batches]), ptrs([b[1] for b in batches])
+    v_p = ptrs([b[2] if not v_is_k_prefix else None for b in batches])
+    o_p, l_p = ptrs([b[3] for b in batches]), ptrs([b[4] for b in batches])
+    L.check(lib.cp_prefill_host(
+        nl, pl, n, cp_size, _strategy(strategy), Hq, Hkv, d, dv, float(scale),
+        1 if v_is_k_prefix else 0, nb, q_p, k_p, v_p, o_p, l_p, _p(workspace), workspace.numel(),
+        _p(status), ctypes.c_void_p(streams[0].cuda_stream),
+        ctypes.c_void_p(streams[1].cuda_stream), ctypes.c_void_p(streams[2].cuda_stream)),
+        "cp_prefill_host")
+    return workspace, streams
 
 
 def segments_host(plan: ShardPlan):
@@ -490,54 +486,51 @@ def segments_host(plan: ShardPlan):
     return [dict(zip(SEGMENT_FIELDS, row)) for row in s]
 
 
-def partial_kv_layout(segs_host, kv_block):
-    """Visible KV blocks per segment and the offset of its partial slots."""
-    out, slot = [], 0
-    for s in segs_host:
-        last_pos = s["q_pos0"] + (s["q_len"] - 1) * s["q_pos_step"]
-        nb = last_pos // kv_block + 1
-        out.append((slot, nb))
-        slot += nb * s["q_len"]
-    return out, slot
-
-
 def cp_partial_kv_workspace_size(new_lens, prefix_lens, cp_size, strategy, kv_block, Hq, dv):
-    """(workspace bytes, max blocks per segment) for cp_attn_partial_kv."""
+    """(workspace bytes, max blocks per segment, longest segment) for
+    cp_attn_partial_kv over the plan these lengths make."""
     lib = L.load()
     nl, n = _i32_array(new_lens)
     pl, _ = _i32_array(prefix_lens)
     nbytes = ctypes.c_int64()
     mb = ctypes.c_int32()
+    msr = ctypes.c_int32()
     L.check(lib.cp_partial_kv_workspace_size(nl, pl, n, cp_size, _strategy(strategy), kv_block,
-                                             Hq, dv, ctypes.byref(nbytes), ctypes.byref(mb)),
+                                             Hq, dv, ctypes.byref(nbytes), ctypes.byref(mb),
+                                             ctypes.byref(msr)),
             "cp_partial_kv_workspace_size")
-    return nbytes.value, mb.value
+    return nbytes.value, mb.value, msr.value
 
 
-def plan_max_segment_rows(new_lens, cp_size, strategy) -> int:
-    """Upper bound on the rows of any segment a plan makes: a zigzag block
-    holds at most ceil(n / 2C) tokens of its request, an interleave run at
-    most ceil(n / C)."""
-    per = 2 * cp_size if _strategy(strategy) == L.ZIGZAG else cp_size
-    return max([(int(n) + per - 1) // per for n in new_lens] or [0])
+def cp_partial_kv_workspace_size_segs(segs_host, kv_block, Hq, dv):
+    """The same sizing for an explicit host segment table (int32 [S, 8])."""
+    lib = L.load()
+    sh = torch.as_tensor(segs_host, dtype=torch.int32).contiguous()
+    if sh.dim() != 2 or sh.shape[1] != 8:
+        raise ValueError("segs_host must be int32 [S, 8] (cp_segment_t rows)")
+    nbytes, mb, msr = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+    L.check(lib.cp_partial_kv_workspace_size_segs(
+        ctypes.c_void_p(sh.data_ptr()), sh.shape[0], int(kv_block), Hq, dv, ctypes.byref(nbytes),
+        ctypes.byref(mb), ctypes.byref(msr)), "cp_partial_kv_workspace_size_segs")
+    return nbytes.value, mb.value, msr.value
 
 
-def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_lens, prefix_lens,
-                       workspace=None, dst_rows="restore", out=None, lse_out=None,
-                       out_fp32=False, max_seg_rows=None, status=None, stream=None):
+def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, workspace=None,
+                       dst_rows="restore", out=None, lse_out=None, out_fp32=False,
+                       max_seg_rows=None, status=None, stream=None):
     """Partial-KV decomposition in one library call (layout, split attention, merge).
 
     ``dst_rows="restore"`` scatters the merged rows to original token order
     (the plan's gather index); ``None`` keeps cat order.  ``max_seg_rows``
-    (default: the plan's bound from the request lengths) lets the library
-    pack two query heads per tile when every segment has at most 64 rows; 0
-    turns packing off.  Returns (O, LSE, workspace).
+    (default: the longest segment of the plan, from the library's sizing
+    call) lets the library pack two query heads per tile when every segment
+    has at most 64 rows; 0 turns packing off.  Returns (O, LSE, workspace).
     """
     lib = L.load()
     N, Hq, d = q_cat.shape
     Hkv, dv = v.shape[1], v.shape[2]
-    nbytes, max_blocks = cp_partial_kv_workspace_size(new_lens, prefix_lens, plan.cp_size,
-                                                      plan.strategy, kv_block, Hq, dv)
+    nbytes, max_blocks, longest = cp_partial_kv_workspace_size(
+        plan.new_lens, plan.prefix_lens, plan.cp_size, plan.strategy, kv_block, Hq, dv)
     _check_qkv(q_cat, k, v)
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_cat.device)
@@ -554,8 +547,7 @@ def cp_attn_partial_kv(plan: ShardPlan, q_cat, k, v, scale, kv_block, *, new_len
         _p(plan.segs), plan.total_segs, _p(plan.tiles), plan.total_tiles, _p(q_cat), N, _p(k),
         k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
         float(scale), int(kv_block), int(max_blocks),
-        plan_max_segment_rows(new_lens, plan.cp_size, plan.strategy) if max_seg_rows is None
-        else int(max_seg_rows), _p(idx), _p(out),
+        longest if max_seg_rows is None else int(max_seg_rows), _p(idx), _p(out),
         1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
         workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
     return out, lse_out, workspace
@@ -581,17 +573,11 @@ def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_
     ns, _ = _segments(segs, None, None, None, q)
     if segs_host is None:
         segs_host = segs.cpu()
-    sh = segs_host.to(torch.int32).contiguous()
-    # the longest segment: decode-sized segments (<= 64 rows) let the kernel
-    # pack two query heads into each 128-row tile
-    max_rows = (int(sh[:ns, 1].max()) if ns > 0 else 0) if max_seg_rows is None \
-        else int(max_seg_rows)
-    nbytes, max_blocks = ctypes.c_int64(), ctypes.c_int32()
-    L.check(lib.cp_partial_kv_workspace_size_segs(
-        ctypes.c_void_p(sh.data_ptr()), ns, int(kv_block), Hq, dv, ctypes.byref(nbytes),
-        ctypes.byref(max_blocks)), "cp_partial_kv_workspace_size_segs")
+    nbytes, max_blocks, longest = cp_partial_kv_workspace_size_segs(segs_host[:ns], kv_block, Hq,
+                                                                    dv)
+    max_rows = longest if max_seg_rows is None else int(max_seg_rows)
     if workspace is None:
-        workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     _dev(workspace, "workspace", torch.uint8, q)
     if dst_rows is not None:
         _dev(dst_rows, "dst_rows", torch.int32, q)
@@ -603,163 +589,102 @@ def cp_attn_split_kv(segs, q, k, v, scale, kv_block, *, segs_host=None, num_out_
     L.check(lib.cp_attn_partial_kv(
         _p(segs), ns, None, 0, _p(q), rows, _p(k), k.stride(0), k.stride(1), _p(v), v.stride(0),
         v.stride(1), k.shape[0], Hq, Hkv, d, dv, float(scale), int(kv_block),
-        max(1, int(max_blocks.value)), max_rows, _p(dst_rows), _p(out),
+        max(1, int(max_blocks)), max_rows, _p(dst_rows), _p(out),
         1 if out.dtype == torch.float32 else 0, _p(lse_out), out.shape[0], _p(workspace),
         workspace.numel(), _p(status), _stream(stream)), "cp_attn_partial_kv")
     return out, lse_out, workspace
 
 
-def cp_partial_kv_attention(q_cat, k, v, plan: ShardPlan, scale, kv_block, *, segs_host=None,
-                            parts_o=None, parts_lse=None, out=None, lse_out=None, status=None,
-                            stream=None):
-    """Partial-KV (ring-style) CP on one GPU, one KV block at a time.
-
-    Emulates the ring schedule step by step: for every segment and every
-    visible block of ``kv_block`` keys, one cp_attn_partial call gives the fp32
-    partial (O_j, L_j); then one cp_lse_merge per segment merges them and
-    scatters straight to original token order.  cp_attn_partial_kv computes
-    the same in three launches.
-    Returns (O [N, Hq, dv] bf16, LSE [N, Hq]).
-    """
-    N, Hq, _ = q_cat.shape
-    dv = v.shape[2]
-    segs_host = segs_host or segments_host(plan)
-    layout, total_slot_rows = partial_kv_layout(segs_host, kv_block)
-    dev = q_cat.device
-    if parts_o is None:
-        parts_o = torch.empty((total_slot_rows, Hq, dv), dtype=torch.float32, device=dev)
-    if parts_lse is None:
-        parts_lse = torch.empty((total_slot_rows, Hq), dtype=torch.float32, device=dev)
-    if out is None:
-        out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
-    if lse_out is None:
-        lse_out = torch.empty((N, Hq), dtype=torch.float32, device=dev)
-    for si, s in enumerate(segs_host):
-        base, nb = layout[si]
-        ql = s["q_len"]
-        for j in range(nb):
-            o_j = parts_o[base + j * ql: base + (j + 1) * ql]
-            l_j = parts_lse[base + j * ql: base + (j + 1) * ql]
-            cp_attn_partial(plan.segs[si: si + 1], q_cat, k, v, scale, kv_lo=j * kv_block,
-                            kv_hi=(j + 1) * kv_block, out=o_j, lse=l_j,
-                            out_row_base=s["q_row0"], num_out_rows=ql, status=status,
-                            stream=stream)
-    for si, s in enumerate(segs_host):
-        base, nb = layout[si]
-        ql = s["q_len"]
-        o_parts = parts_o[base: base + nb * ql].view(nb, ql, Hq, dv)
-        l_parts = parts_lse[base: base + nb * ql].view(nb, ql, Hq)
-        cp_lse_merge(o_parts, l_parts, dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql],
-                     out=out, lse_out=lse_out, num_out_rows=N, status=status, stream=stream)
-    return out, lse_out
-
-
-def pass_q_kv_blocks(kv_total: int, cp_size: int):
-    """Resident KV shards of the pass-Q ring for one request.
-
-    The request's KV positions 0..kv_total-1 are cut into 2C near-equal blocks
-    (the remainder to the first blocks, as for the zigzag query split) and
-    rank r keeps blocks r and 2C-1-r.  Returns, per rank, its two (lo, hi)
-    position ranges.
-    """
-    nb = 2 * cp_size
-    base, rem = divmod(int(kv_total), nb)
-    starts = [0]
-    for i in range(nb):
-        starts.append(starts[-1] + base + (1 if i < rem else 0))
-    return [[(starts[r], starts[r + 1]), (starts[nb - 1 - r], starts[nb - r])]
-            for r in range(cp_size)]
-
-
 @dataclass
-class PassQLaunch:
-    """One accumulate launch of the pass-Q ring: at ring hop ``hop`` every
-    rank merges the query shard visiting it against resident block ``block``
-    of its KV (0: block r of the request's 2C, 1: block 2C-1-r; see
-    pass_q_kv_blocks).  ``segs`` holds copies of the plan's segment rows that
-    see that block (int32 [n, 8]), ``windows`` their key windows (int32
-    [n, 2]), ``seg_ids`` their indices in the plan."""
-    hop: int
-    block: int
+class PassQSchedule:
+    """The pass-Q ring schedule from cp_pass_q_schedule: launch i covers
+    entries launch_first[i] .. launch_first[i+1]-1 at ring hop hops[i] and
+    resident block blocks[i] (0: block r of the request's 2C KV blocks, 1:
+    block 2C-1-r).  ``segs`` (int32 [E, 8], device) are copies of the plan's
+    segment rows, ``windows`` (int32 [E, 2], device) their key windows and
+    ``seg_ids`` (host) their indices in the plan's segment table."""
+    launch_first: List[int]
+    hops: List[int]
+    blocks: List[int]
     segs: torch.Tensor
     windows: torch.Tensor
     seg_ids: List[int]
 
+    @property
+    def num_launches(self):
+        return len(self.hops)
 
-def pass_q_schedule(plan: ShardPlan, segs_host=None) -> List[PassQLaunch]:
-    """Host schedule of the pass-Q ring: one launch per (hop, resident block).
 
-    At hop s the shard of rank q visits rank (q + s) mod C.  Each launch
-    takes every segment of every shard, with the key window of its host
-    rank's block for the segment's request; a segment that cannot see the
-    block (the block is empty or starts after the segment's last position)
-    is left out.  All windows of one launch belong to different rows, so one
-    launch merges every rank's hop at once: at most 2C launches for any
-    batch.  The segment copies are taken from the plan as it is now: build
-    the schedule again after re-planning a different batch.
-    """
-    C = plan.cp_size
-    segs_host = segs_host or segments_host(plan)
-    new_lens = plan.new_lens_dev.cpu().tolist()[: plan.num_reqs]
-    prefix_lens = plan.prefix_lens_dev.cpu().tolist()[: plan.num_reqs]
-    blocks = [pass_q_kv_blocks(p + n, C) for n, p in zip(new_lens, prefix_lens)]
-    shard_of = []
-    for r, c in enumerate(plan.segs_per_rank):
-        shard_of += [r] * c
-    raw = plan.segs[: plan.total_segs].cpu()
-    dev = plan.segs.device
-    launches = []
-    for hop in range(C):
-        for b in (0, 1):
-            ids, wins = [], []
-            for i, sg in enumerate(segs_host):
-                lo, hi = blocks[sg["req"]][(shard_of[i] + hop) % C][b]
-                last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
-                if hi > lo and lo <= last:
-                    ids.append(i)
-                    wins.append((lo, hi))
-            if ids:
-                launches.append(PassQLaunch(
-                    hop=hop, block=b, segs=raw[ids].contiguous().to(dev),
-                    windows=torch.tensor(wins, dtype=torch.int32).to(dev), seg_ids=ids))
-    return launches
+def pass_q_schedule(plan: ShardPlan, device=None) -> PassQSchedule:
+    """The library's pass-Q ring schedule for the plan's lengths (host call),
+    with its entry arrays copied to the plan's device."""
+    return pass_q_schedule_host(plan.new_lens, plan.prefix_lens, plan.cp_size, plan.strategy,
+                                plan.segs.device if device is None else device)
+
+
+def pass_q_schedule_host(new_lens, prefix_lens, cp_size, strategy, device="cpu") -> PassQSchedule:
+    """cp_pass_q_schedule for these lengths; entry arrays on ``device``."""
+    lib = L.load()
+    nl, n = _i32_array(new_lens)
+    pl, _ = _i32_array(prefix_lens)
+    strategy = _strategy(strategy)
+    nlaunch, nent = ctypes.c_int32(), ctypes.c_int32()
+    L.check(lib.cp_pass_q_schedule_size(nl, pl, n, cp_size, strategy,
+                                        ctypes.byref(nlaunch), ctypes.byref(nent)),
+            "cp_pass_q_schedule_size")
+    nL, nE = nlaunch.value, nent.value
+    first = (ctypes.c_int32 * (nL + 1))()
+    hops = (ctypes.c_int32 * max(1, nL))()
+    blocks = (ctypes.c_int32 * max(1, nL))()
+    segs = torch.zeros((max(1, nE), 8), dtype=torch.int32)
+    wins = torch.zeros((max(1, nE), 2), dtype=torch.int32)
+    ids = (ctypes.c_int32 * max(1, nE))()
+    L.check(lib.cp_pass_q_schedule(nl, pl, n, cp_size, strategy, first, hops, blocks,
+                                   ctypes.c_void_p(segs.data_ptr()),
+                                   ctypes.cast(ctypes.c_void_p(wins.data_ptr()), L.c_i32p), ids),
+            "cp_pass_q_schedule")
+    return PassQSchedule(launch_first=list(first), hops=list(hops)[:nL],
+                         blocks=list(blocks)[:nL], segs=segs.to(device), windows=wins.to(device),
+                         seg_ids=list(ids)[:nE])
 
 
 def cp_pass_q_attention(q_cat, k, v, plan: ShardPlan, scale, *, schedule=None, status=None,
                         stream=None, out=None):
-    """Pass-Q ring CP on one GPU, hop by hop.
-
-    KV stays resident: rank r holds the KV blocks of pass_q_kv_blocks.  Each
-    rank's query shard travels round the ring with an fp32 accumulator
-    (O_acc, L_acc) that starts empty (0, -inf); at hop s rank r merges the
-    partial of the visiting shard (of rank (r - s) mod C) against its own KV
-    blocks into that accumulator.  One cp_attn_partial_accumulate per launch
-    of pass_q_schedule covers every rank of a hop for one of its two blocks,
-    each segment with its own key window.  After C hops every accumulator is
-    the exact result.
+    """Pass-Q ring CP on one GPU (cp_attn_pass_q in cpattn.h): every query
+    shard travels round the ring with an fp32 accumulator that each hop's
+    partial against the host rank's resident KV is merged into.
+    ``schedule``: from pass_q_schedule(plan) (built when omitted).
     ``out``: optional (O_acc fp32 [N, Hq, dv], LSE [N, Hq], LSE scratch [N, Hq]).
     Returns (O fp32 [N, Hq, dv], LSE [N, Hq]) in cat order.
     """
-    N, Hq, _ = q_cat.shape
-    dv = v.shape[2]
+    lib = L.load()
+    _check_qkv(q_cat, k, v)
+    N, Hq, d = q_cat.shape
+    Hkv, dv = v.shape[1], v.shape[2]
     dev = q_cat.device
-    sched = pass_q_schedule(plan) if schedule is None else schedule
-    with torch.cuda.stream(stream):  # the fills and LSE copies run on the launches' stream
-        if out is None:
-            o_acc = torch.empty((max(N, 1), Hq, dv), dtype=torch.float32, device=dev)
-            lse_a = torch.empty((max(N, 1), Hq), dtype=torch.float32, device=dev)
-            lse_b = torch.empty_like(lse_a)
-        else:
-            o_acc, lse_a, lse_b = out
-        o_acc.zero_()
-        lse_a.fill_(float("-inf"))
-        lse_b.fill_(float("-inf"))
-        for launch in sched:
-            cp_attn_partial_accumulate(launch.segs, q_cat, k, v, scale, o_acc, lse_a, lse_b,
-                                       seg_windows=launch.windows, status=status, stream=stream)
-            # rows outside the launch hold equal values in both buffers
-            lse_a.copy_(lse_b)
-    return o_acc[:N], lse_a[:N]
+    sched = pass_q_schedule(plan, dev) if schedule is None else schedule
+    if out is None:
+        out = (torch.empty((max(N, 1), Hq, dv), dtype=torch.float32, device=dev),
+               torch.empty((max(N, 1), Hq), dtype=torch.float32, device=dev),
+               torch.empty((max(N, 1), Hq), dtype=torch.float32, device=dev))
+    o_acc, lse, lse_b = out
+    for t, name in ((o_acc, "o_acc"), (lse, "lse"), (lse_b, "lse_scratch")):
+        _dev(t, name, torch.float32, q_cat)
+    if o_acc.shape[0] < N or tuple(o_acc.shape[1:]) != (Hq, dv):
+        raise ValueError("o_acc must be [N, Hq, dv]")
+    if lse.shape[0] < N or lse_b.shape[0] < N or lse.shape[1:] != (Hq,) or \
+            lse_b.shape[1:] != (Hq,):
+        raise ValueError("lse buffers must be [N, Hq]")
+    _dev(sched.segs, "schedule.segs", torch.int32, q_cat)
+    _dev(sched.windows, "schedule.windows", torch.int32, q_cat)
+    _status(status, q_cat)
+    first = (ctypes.c_int32 * len(sched.launch_first))(*sched.launch_first)
+    L.check(lib.cp_attn_pass_q(
+        _p(sched.segs), _p(sched.windows), first, sched.num_launches, _p(q_cat), N, _p(k),
+        k.stride(0), k.stride(1), _p(v), v.stride(0), v.stride(1), k.shape[0], Hq, Hkv, d, dv,
+        float(scale), _p(o_acc), _p(lse), _p(lse_b), _p(status), _stream(stream)),
+        "cp_attn_pass_q")
+    return o_acc[:N], lse[:N]
 
 
 def cp_select_pass(new_tokens: int, cached_tokens: int, Hq: int, Hkv: int, rule="message"):

@@ -25,6 +25,7 @@
 #include <vector>
 
 #include "attn_common.cuh"
+#include "host_plan.h"
 
 namespace cpattn {
 namespace {
@@ -326,14 +327,17 @@ pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_blo
   }
 }
 
+// SM count of the current device, cached per device.
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-  }
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < kMaxDev && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < kMaxDev) cached[dev] = n;
   return n;
 }
 
@@ -342,69 +346,63 @@ int num_sms() {
 
 using namespace cpattn;
 
+namespace {
+
+// Workspace bytes for `rows` partial rows of `segs` segments (the layout at
+// the top of this file).
+int64_t pkv_workspace_bytes(long long segs, long long rows, int Hq, int dv) {
+  const long long header = round256((2 * segs + 2) * 8);
+  return header + round256(rows * Hq * dv * 4) + round256(rows * Hq * 4) + 256;
+}
+
+// Running sizes over a segment table: partial rows, segments, the largest
+// block count and the longest segment.
+struct PkvSizes {
+  long long rows = 0, segs = 0, max_blocks = 0, max_rows = 0;
+  void add(const cp_segment_t& s, int kv_block) {
+    if (s.q_len <= 0) return;
+    const long long nb = segment_last_pos(s) / kv_block + 1;
+    rows += nb * s.q_len;
+    segs += 1;
+    max_blocks = std::max(max_blocks, nb);
+    max_rows = std::max<long long>(max_rows, s.q_len);
+  }
+  void write(int Hq, int dv, int64_t* bytes, int32_t* mb, int32_t* msr, long long table_segs) const {
+    *bytes = pkv_workspace_bytes(table_segs, rows, Hq, dv);
+    if (mb) *mb = (int32_t)std::min<long long>(max_blocks, 0x7fffffff);
+    if (msr) *msr = (int32_t)max_rows;
+  }
+};
+
+}  // namespace
+
 extern "C" int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
                                             int num_reqs, int cp_size, int strategy, int kv_block,
-                                            int Hq, int dv, int64_t* bytes, int32_t* max_blocks) {
-  if (num_reqs < 0 || num_reqs > CPATTN_MAX_REQS || cp_size < 1 || cp_size > CPATTN_MAX_CP)
-    return CPATTN_ERR_INVALID_ARG;
-  if (strategy != CP_ZIGZAG && strategy != CP_INTERLEAVE) return CPATTN_ERR_INVALID_ARG;
+                                            int Hq, int dv, int64_t* bytes, int32_t* max_blocks,
+                                            int32_t* max_seg_rows) {
   if (kv_block < 1 || Hq < 1 || dv < 4 || (dv % 4) != 0 || !bytes) return CPATTN_ERR_INVALID_ARG;
-  if (num_reqs > 0 && (!new_lens || !prefix_lens)) return CPATTN_ERR_INVALID_ARG;
-  const long long C = cp_size;
-  long long rows = 0, segs = 0, flat0 = 0, mb = 0;
-  auto add = [&](long long len, long long last_pos) {
-    if (len <= 0) return;
-    const long long nb = last_pos / kv_block + 1;
-    rows += nb * len;
-    segs += 1;
-    mb = std::max(mb, nb);
-  };
-  for (int b = 0; b < num_reqs; ++b) {
-    const long long n = new_lens[b], p = prefix_lens[b];
-    if (n < 0 || p < 0) return CPATTN_ERR_INVALID_ARG;
-    if (strategy == CP_ZIGZAG) {
-      // the segments cp_shard_plan makes: one per non-empty block
-      const long long nb2 = 2 * C, base = n / nb2, rem = n % nb2;
-      long long st = 0;
-      for (long long k = 0; k < nb2; ++k) {
-        const long long sz = base + (k < rem);
-        add(sz, p + st + sz - 1);
-        st += sz;
-      }
-    } else {
-      for (long long r = 0; r < C; ++r) {
-        const long long i0 = flat0 + (((r - flat0 % C) % C) + C) % C;
-        const long long cnt = (i0 < flat0 + n) ? (flat0 + n - 1 - i0) / C + 1 : 0;
-        if (cnt > 0) add(cnt, p + (i0 + (cnt - 1) * C - flat0));
-      }
-    }
-    flat0 += n;
-  }
-  const long long header = round256((2 * segs + 2) * 8);
-  *bytes = header + round256(rows * Hq * dv * 4) + round256(rows * Hq * 4) + 256;
-  if (max_blocks) *max_blocks = (int32_t)std::min<long long>(mb, 0x7fffffff);
+  PkvSizes sz;
+  // the segments cp_shard_plan makes for these lengths
+  const int rc = for_each_plan_segment(new_lens, prefix_lens, num_reqs, cp_size, strategy,
+                                       [&](int, const cp_segment_t& s) { sz.add(s, kv_block); });
+  if (rc != CPATTN_OK) return rc;
+  sz.write(Hq, dv, bytes, max_blocks, max_seg_rows, sz.segs);
   return CPATTN_OK;
 }
 
 extern "C" int cp_partial_kv_workspace_size_segs(const cp_segment_t* segs_host, int num_segs,
                                                  int kv_block, int Hq, int dv, int64_t* bytes,
-                                                 int32_t* max_blocks) {
+                                                 int32_t* max_blocks, int32_t* max_seg_rows) {
   if (num_segs < 0 || kv_block < 1 || Hq < 1 || dv < 4 || (dv % 4) != 0 || !bytes)
     return CPATTN_ERR_INVALID_ARG;
   if (num_segs > 0 && !segs_host) return CPATTN_ERR_INVALID_ARG;
-  long long rows = 0, mb = 0;
+  PkvSizes sz;
   for (int i = 0; i < num_segs; ++i) {
     const cp_segment_t& sg = segs_host[i];
     if (sg.q_len < 0 || sg.q_pos0 < 0 || sg.q_pos_step < 0) return CPATTN_ERR_INVALID_ARG;
-    if (sg.q_len == 0) continue;
-    const long long last = (long long)sg.q_pos0 + (long long)(sg.q_len - 1) * sg.q_pos_step;
-    const long long nb = last / kv_block + 1;
-    rows += nb * sg.q_len;
-    mb = std::max(mb, nb);
+    sz.add(sg, kv_block);
   }
-  const long long header = round256((2LL * num_segs + 2) * 8);
-  *bytes = header + round256(rows * Hq * dv * 4) + round256(rows * Hq * 4) + 256;
-  if (max_blocks) *max_blocks = (int32_t)std::min<long long>(mb, 0x7fffffff);
+  sz.write(Hq, dv, bytes, max_blocks, max_seg_rows, num_segs);
   return CPATTN_OK;
 }
 

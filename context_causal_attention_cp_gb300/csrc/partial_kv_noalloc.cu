@@ -10,11 +10,18 @@
 // every GPU loading this library holds until the process exits.
 //
 // The host code cannot use the array's name as a device address (in host code
-// it is only a stand-in symbol), so the first call on each device looks its
-// address up with cudaGetSymbolAddress while that device is current, checks
-// the result and caches it; later calls on that device reuse the address.
+// it is only a stand-in symbol), so the first call in each CUDA context looks
+// its address up with cudaGetSymbolAddress while that context's device is
+// current, checks the result and caches it together with the context's unique
+// id; later calls in the same context reuse the address.  A new context on the
+// same device (after cudaDeviceReset, or a caller that switches to a context
+// of its own) has a new id, so its first call looks the address up again
+// instead of using a stale one.
 #include <cstdint>
 #include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "../../include/cpattn.h"
 
@@ -24,19 +31,66 @@ static __device__ __align__(256) unsigned char g_pkv_scratch[CPATTN_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to
+  void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of g_pkv_scratch on the current device (set up once).
-int scratch_on_current_device(void** out) {
+// Driver entry points for the current context and its id (resolved once
+// through the runtime, so the library needs no link against libcuda).
+struct CtxApi {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxApi& ctx_api() {
+  static CtxApi api;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      api.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      api.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return api;
+}
+
+// Unique id of the context current on this thread.  When no context is
+// current yet, the device's primary context is made current first, as any
+// runtime call would do.
+int current_context_id(int dev, unsigned long long* id) {
+  const CtxApi& api = ctx_api();
+  if (!api.get_current || !api.get_id) return CPATTN_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (api.get_current(&ctx) != CUDA_SUCCESS) return CPATTN_ERR_CUDA;
+  if (!ctx) {
+    if (cudaSetDevice(dev) != cudaSuccess || api.get_current(&ctx) != CUDA_SUCCESS || !ctx)
+      return CPATTN_ERR_CUDA;
+  }
+  return api.get_id(ctx, id) == CUDA_SUCCESS ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+// Device address of g_pkv_scratch in the current context (looked up once per
+// context).
+int scratch_in_current_context(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CPATTN_ERR_CUDA;
+  unsigned long long id = 0;
+  const int rc = current_context_id(dev, &id);
+  if (rc != CPATTN_OK) return rc;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
+  ScratchEntry& e = g_scratch[dev];
+  if (!e.ptr || e.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pkv_scratch) != cudaSuccess || !p) return CPATTN_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    e.ptr = p;
+    e.ctx_id = id;
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return CPATTN_OK;
 }
 
@@ -53,12 +107,15 @@ extern "C" int cp_attn_partial_kv_noalloc(
   if (workspace_bytes_needed < 0) return CPATTN_ERR_INVALID_ARG;
   if (workspace_bytes_needed > (int64_t)CPATTN_NOALLOC_SCRATCH_BYTES) return CPATTN_ERR_TOO_LARGE;
   void* scratch = nullptr;
-  const int rc = scratch_on_current_device(&scratch);
+  const int rc = scratch_in_current_context(&scratch);
   if (rc != CPATTN_OK) return rc;
   // The same three launches as cp_attn_partial_kv, on the static scratch.
   // Nothing in the scratch must start at zero: the layout kernel rewrites
   // the slot table and every partial the merge reads is written earlier in
-  // the same call.
+  // the same call.  The layout kernel also checks the real need against the
+  // array's size on the device, so a caller figure that is too small gives
+  // the device-status error of cp_attn_partial_kv rather than a write past
+  // the array.
   return cp_attn_partial_kv(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k,
                             k_row_stride, k_head_stride, v, v_row_stride, v_head_stride,
                             num_kv_rows, Hq, Hkv, d, dv, scale, kv_block, max_blocks,

@@ -303,14 +303,23 @@ int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, i
  *     overwritten.  Too small: CPATTN_ERR_INVALID_ARG in *status_dev and the
  *     partials that do not fit are skipped.
  * Three launches on the stream (layout, attention, merge). */
+/* Sizing (host only).  bytes: the workspace for the segments cp_shard_plan
+ * makes from these lengths; max_blocks (nullable): the largest block count of
+ * any segment, the value to pass to cp_attn_partial_kv; max_seg_rows
+ * (nullable): the longest segment's q_len, the value to pass as
+ * max_seg_rows (it turns on head packing when it is at most
+ * CPATTN_TILE_ROWS / 2). */
 int cp_partial_kv_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
                                  int num_reqs, int cp_size, int strategy, int kv_block, int Hq,
-                                 int dv, int64_t* bytes, int32_t* max_blocks);
+                                 int dv, int64_t* bytes, int32_t* max_blocks,
+                                 int32_t* max_seg_rows);
 /* The same sizing for an explicit segment table on the host (for segments
  * that no plan made, e.g. a decode step's few queries over a KV shard):
- * bytes and the largest block count over segs_host[0 .. num_segs). */
+ * bytes, the largest block count and the longest segment over
+ * segs_host[0 .. num_segs). */
 int cp_partial_kv_workspace_size_segs(const cp_segment_t* segs_host, int num_segs, int kv_block,
-                                      int Hq, int dv, int64_t* bytes, int32_t* max_blocks);
+                                      int Hq, int dv, int64_t* bytes, int32_t* max_blocks,
+                                      int32_t* max_seg_rows);
 int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t* tiles_dev,
                        int num_tiles, const void* q, int num_q_rows, const void* k,
                        int64_t k_row_stride, int64_t k_head_stride, const void* v,
@@ -330,11 +339,19 @@ int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs, const int32_t
  *   array of CPATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU
  *   that loads the library keeps until the process exits.
  *   workspace_bytes_needed: what cp_partial_kv_workspace_size reports for
- *     the plan's lengths; above CPATTN_NOALLOC_SCRATCH_BYTES the call returns
- *     CPATTN_ERR_TOO_LARGE and launches nothing.
- *   The first call on a device looks up the scratch address on that device
- *   (cudaGetSymbolAddress, with the device current); make that first call
- *   before any stream capture.  It allocates nothing (no cudaMalloc/cudaFree).
+ *     the plan's lengths.  Above CPATTN_NOALLOC_SCRATCH_BYTES the call returns
+ *     CPATTN_ERR_TOO_LARGE and launches nothing.  This host check trusts the
+ *     caller's figure: if the figure is too small and the real need exceeds
+ *     the array, the call launches and the device reports it as
+ *     cp_attn_partial_kv does for a small workspace (CPATTN_ERR_INVALID_ARG in
+ *     *status_dev, the partials that do not fit skipped); nothing is written
+ *     past the array.
+ *   The first call in a CUDA context looks up the scratch address in that
+ *   context (cudaGetSymbolAddress, with the device current) and caches it
+ *   under the context's unique id; make that first call before any stream
+ *   capture.  A new context on the device (e.g. after cudaDeviceReset) has a
+ *   new id, so its first call looks the address up again, also outside any
+ *   capture.  The call allocates nothing (no cudaMalloc/cudaFree).
  *   All calls share one scratch array, which keeps the last call's contents:
  *   calls that overlap on the GPU (other streams, other host threads) race on
  *   it and must be serialised by the caller.  Nothing in it needs clearing.
@@ -350,6 +367,96 @@ int cp_attn_partial_kv_noalloc(const cp_segment_t* segs_dev, int num_segs,
                                int o_is_fp32,
                                float* lse_out, int num_out_rows, int64_t workspace_bytes_needed,
                                int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Pass-Q ring: schedule (host only) and the whole ring in one call.
+ * [CPB-PQ]; [CPB-3.5] (the persistent KV cache split into 2C first/last-paired
+ * blocks).
+ *
+ * KV residency: each request's key positions 0 .. p+n-1 are cut into 2C blocks
+ * like the zigzag query split (block k has (p+n)/2C keys plus one when
+ * k < (p+n) mod 2C) and rank r keeps blocks r and 2C-1-r.  At ring hop s
+ * (0 <= s < C) the query shard of rank q is on rank (q+s) mod C.  Launch
+ * (s, b), b in {0, 1}, holds every segment of the plan (cp_shard_plan's
+ * table order) whose request's resident block b on its host rank is non-empty
+ * and starts at or before the segment's last position, with that block as the
+ * segment's key window.  Launches run hop-major, block-minor; empty ones are
+ * left out, so num_launches <= 2C.
+ *
+ * cp_pass_q_schedule_size: num_launches and num_entries (total segment
+ *   entries over all launches), to size the buffers below.
+ * cp_pass_q_schedule (host arrays, caller-allocated):
+ *   launch_first [num_launches+1]  first entry of each launch, then num_entries
+ *   launch_hop, launch_block [num_launches]  (nullable) s and b of each launch
+ *   entry_segs [num_entries]       copies of the plan's segment rows
+ *   entry_windows [2*num_entries]  key window [lo, hi) of each entry
+ *   entry_seg_ids [num_entries]    (nullable) index of the entry's segment in
+ *                                  the plan's segment table
+ * Arguments as cp_shard_plan_sizes; errors CPATTN_ERR_INVALID_ARG. */
+int cp_pass_q_schedule_size(const int32_t* new_lens, const int32_t* prefix_lens, int num_reqs,
+                            int cp_size, int strategy, int32_t* num_launches,
+                            int32_t* num_entries);
+int cp_pass_q_schedule(const int32_t* new_lens, const int32_t* prefix_lens, int num_reqs,
+                       int cp_size, int strategy, int32_t* launch_first, int32_t* launch_hop,
+                       int32_t* launch_block, cp_segment_t* entry_segs, int32_t* entry_windows,
+                       int32_t* entry_seg_ids);
+
+/* The pass-Q ring on the device: the accumulator starts at the identity
+ * (O = 0, L = -inf) and every launch of the schedule merges its entries'
+ * partials into it (cp_attn_partial_accumulate with per-segment windows).
+ * After the last launch every row holds attention over all its visible keys.
+ *   entry_segs_dev, entry_windows_dev: the schedule's entry arrays copied to
+ *     the device (16- and 4-byte aligned).  launch_first: HOST int32
+ *     [num_launches+1] from cp_pass_q_schedule.
+ *   q, k, v and shapes: as cp_attn_partial (q in cat order, num_q_rows rows).
+ *   o_acc: fp32 [num_q_rows, Hq, dv]; lse: fp32 [num_q_rows, Hq] (natural log);
+ *     both written (cat order).  lse_scratch: fp32 [num_q_rows, Hq], scratch
+ *     that must not overlap lse.
+ * Launches on the stream: one initialisation kernel, then per launch one
+ * attention launch and one device-to-device copy of the LSE. */
+int cp_attn_pass_q(const cp_segment_t* entry_segs_dev, const int32_t* entry_windows_dev,
+                   const int32_t* launch_first, int num_launches, const void* q, int num_q_rows,
+                   const void* k, int64_t k_row_stride, int64_t k_head_stride, const void* v,
+                   int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
+                   int d, int dv, float scale, float* o_acc, float* lse, float* lse_scratch,
+                   int32_t* status_dev, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host-to-host full-KV CP prefill of a sequence of same-shaped batches (the
+ * end-to-end path).  [SGL-ZZ], [SGL-IL], [SGL-BE], [CPB-2.1]
+ *
+ * Batch i (0 <= i < num_batches) has host inputs q_host[i] bf16 [N, Hq, d] in
+ * original token order, k_host[i] bf16 [KV, Hkv, d] and v_host[i] bf16
+ * [KV, Hkv, dv] (KV rows as in cp_attn_partial; with v_is_k_prefix the value
+ * is the first dv columns of each key row, v_host is ignored and may be NULL,
+ * as for the absorbed MLA shape), and host outputs o_host[i] bf16 [N, Hq, dv]
+ * and lse_host[i] fp32 [N, Hq], in original token order.  N and KV follow
+ * from new_lens / prefix_lens (host arrays [num_reqs]).
+ * Per batch: its inputs are copied in on `upload`; on `compute` the plan is
+ * built (cp_shard_plan) and every shard attends to the gathered KV (zigzag:
+ * cp_attn_prefill; interleave: cp_restore of the queries into shard order and
+ * cp_attn_partial_restore); O and LSE are copied out on `download`.  Two
+ * device buffer sets let batch i's attention overlap batch i+1's upload and
+ * batch i-1's download.  The streams may be the same stream (then nothing
+ * overlaps).  The call returns once everything is queued; the outputs are
+ * valid once `download` has completed.  Host buffers should be page-locked
+ * for the copies to run asynchronously, and must stay valid until then.
+ *   workspace: device memory of at least cp_prefill_host_workspace_size bytes,
+ *     256-byte aligned, owned by the caller (plan buffers and two buffer sets).
+ *   The call creates and destroys six CUDA events (no memory is allocated).
+ * Errors: argument errors as CPATTN_ERR_* before anything is queued; a failed
+ * CUDA call returns CPATTN_ERR_CUDA (work queued before it stays queued);
+ * device-detected errors go to *status_dev. */
+int cp_prefill_host_workspace_size(const int32_t* new_lens, const int32_t* prefix_lens,
+                                   int num_reqs, int cp_size, int strategy, int Hq, int Hkv,
+                                   int d, int dv, int v_is_k_prefix, int64_t* bytes);
+int cp_prefill_host(const int32_t* new_lens, const int32_t* prefix_lens, int num_reqs,
+                    int cp_size, int strategy, int Hq, int Hkv, int d, int dv, float scale,
+                    int v_is_k_prefix, int num_batches, const void* const* q_host,
+                    const void* const* k_host, const void* const* v_host, void* const* o_host,
+                    float* const* lse_host, void* workspace, int64_t workspace_bytes,
+                    int32_t* status_dev, cudaStream_t compute, cudaStream_t upload,
+                    cudaStream_t download);
 
 /* ------------------------------------------------------------------------ */
 /* Merge num_parts partial results with the log-sum-exp rule.  [CPB-3.6]

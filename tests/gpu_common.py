@@ -57,3 +57,31 @@ def boundary_rows(new_lens, prefix_lens, cp_size, strategy, extra):
                 rows.add(plan.gather_idx[s.q_row0 + 127])
                 rows.add(plan.gather_idx[s.q_row0 + 128])
     return sorted(rows)
+
+
+def stepwise_partial_kv(q_cat, k, v, plan, scale, kv_block, status=None):
+    """The ring's pass-KV schedule emulated call by call through the C ABI
+    (a test cross-check of the one-call cp_attn_partial_kv): for every segment
+    and every visible block of ``kv_block`` keys one cp_attn_partial with that
+    key window gives the fp32 partial (O_j, L_j), then one cp_lse_merge per
+    segment merges them, scattered to original token order.
+    Returns (O bf16 [N, Hq, dv], LSE [N, Hq]) in original order."""
+    import context_causal_attention_cp_gb300 as cpa
+
+    N, Hq, _ = q_cat.shape
+    dv = v.shape[2]
+    dev = q_cat.device
+    out = torch.empty((N, Hq, dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((N, Hq), dtype=torch.float32, device=dev)
+    for si, s in enumerate(cpa.segments_host(plan)):
+        ql = s["q_len"]
+        nb = (s["q_pos0"] + (ql - 1) * s["q_pos_step"]) // kv_block + 1
+        po = torch.empty((nb, ql, Hq, dv), dtype=torch.float32, device=dev)
+        pl = torch.empty((nb, ql, Hq), dtype=torch.float32, device=dev)
+        for j in range(nb):
+            cpa.cp_attn_partial(plan.segs[si: si + 1], q_cat, k, v, scale, kv_lo=j * kv_block,
+                                kv_hi=(j + 1) * kv_block, out=po[j], lse=pl[j],
+                                out_row_base=s["q_row0"], num_out_rows=ql, status=status)
+        cpa.cp_lse_merge(po, pl, dst_rows=plan.gather_idx[s["q_row0"]: s["q_row0"] + ql],
+                         out=out, lse_out=lse, num_out_rows=N, status=status)
+    return out, lse

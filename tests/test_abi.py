@@ -87,15 +87,16 @@ def test_invalid_arguments_are_rejected_on_host():
     nbytes, mb = ctypes.c_int64(), ctypes.c_int32()
     one = (ctypes.c_int32 * 1)(1000)
     zero = (ctypes.c_int32 * 1)(0)
+    msr = ctypes.c_int32()
     assert lib.cp_partial_kv_workspace_size(one, zero, 1, 2, 0, 0, 8, 128, ctypes.byref(nbytes),
-                                            ctypes.byref(mb)) == L.ERR_INVALID_ARG
+                                            ctypes.byref(mb), None) == L.ERR_INVALID_ARG
     assert lib.cp_partial_kv_workspace_size(one, zero, 1, 2, 0, 256, 8, 128, ctypes.byref(nbytes),
-                                            ctypes.byref(mb)) == L.OK
-    assert mb.value == 4
+                                            ctypes.byref(mb), ctypes.byref(msr)) == L.OK
+    assert (mb.value, msr.value) == (4, 250)
     # a batch without new tokens: max_blocks 0, and the call is a no-op
     assert lib.cp_partial_kv_workspace_size(zero, one, 1, 2, 0, 256, 8, 128, ctypes.byref(nbytes),
-                                            ctypes.byref(mb)) == L.OK
-    assert mb.value == 0
+                                            ctypes.byref(mb), ctypes.byref(msr)) == L.OK
+    assert (mb.value, msr.value) == (0, 0)
     empty = [fake[0], 0] + args[2:]
     assert lib.cp_attn_partial_kv(*empty, 8, 4, 128, 128, 0.1, 64, 0, 0, nul, nul, 0, nul, 0,
                                   nul, 0, nul, nul) == L.OK
@@ -158,13 +159,44 @@ def test_restore_and_accumulate_calls_validate_on_host():
                                           nul) == L.ERR_ALIGNMENT
 
 
-@pytest.mark.parametrize("total", [0, 1, 5, 16, 333, 131072])
-@pytest.mark.parametrize("C", [1, 2, 4, 8])
-def test_pass_q_blocks_match_oracle(total, C):
-    """Host logic of the pass-Q ring: resident KV windows as the oracle's."""
-    from oracle import pipeline as opipe
-    assert api.pass_q_kv_blocks(total, C) == [[tuple(w) for w in ws]
-                                              for ws in opipe.resident_kv_windows(total, C)]
+def test_ring_and_host_prefill_calls_validate_on_host():
+    """Argument checks of cp_attn_pass_q and cp_prefill_host (every call fails
+    validation before anything is queued; pointers are never used)."""
+    lib = L.load()
+    nul = None
+    fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+    first = (ctypes.c_int32 * 3)(0, 4, 2)        # decreasing: invalid
+    qkv = [fake[2], 128, fake[3], 1024, 128, fake[3], 1024, 128, 256, 8, 8, 128, 128, 0.1]
+    assert lib.cp_attn_pass_q(fake[0], fake[1], first, 2, *qkv, fake[4], fake[5], fake[6], nul,
+                              nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_pass_q(fake[0], fake[1], first, 1, *qkv, nul, fake[5], fake[6], nul,
+                              nul) == L.ERR_INVALID_ARG
+    assert lib.cp_attn_pass_q(fake[0], fake[1], first, 1, *qkv, ctypes.c_void_p(0x40008),
+                              fake[5], fake[6], nul, nul) == L.ERR_ALIGNMENT
+    lens = (ctypes.c_int32 * 1)(1000)
+    pre = (ctypes.c_int32 * 1)(0)
+    nbytes = ctypes.c_int64()
+    assert lib.cp_prefill_host_workspace_size(lens, pre, 1, 4, 0, 8, 8, 128, 128, 0,
+                                              ctypes.byref(nbytes)) == L.OK
+    set_bytes = 2 * (1000 * 8 * 128 * 2) + 1000 * 8 * 128 * 2 + 1000 * 8 * 4
+    assert nbytes.value >= 2 * set_bytes
+    ptrs = (ctypes.c_void_p * 1)(0x1000)
+    args = [lens, pre, 1, 4, 0, 8, 8, 128, 128, 0.1, 0, 1, ptrs, ptrs, ptrs, ptrs, ptrs]
+    # too small a workspace, a misaligned one, a missing host pointer, a bad strategy
+    assert lib.cp_prefill_host(*args, fake[0], nbytes.value - 1, nul, nul, nul,
+                               nul) == L.ERR_INVALID_ARG
+    assert lib.cp_prefill_host(*args, ctypes.c_void_p(0x10010), nbytes.value, nul, nul, nul,
+                               nul) == L.ERR_ALIGNMENT
+    none = (ctypes.c_void_p * 1)(None)
+    bad = args[:12] + [none] + args[13:]
+    assert lib.cp_prefill_host(*bad, fake[0], nbytes.value, nul, nul, nul,
+                               nul) == L.ERR_INVALID_ARG
+    bad = args[:4] + [7] + args[5:]
+    assert lib.cp_prefill_host(*bad, fake[0], nbytes.value, nul, nul, nul,
+                               nul) == L.ERR_INVALID_ARG
+    # no batches: nothing to do
+    zero = args[:11] + [0] + args[12:]
+    assert lib.cp_prefill_host(*zero, nul, 0, nul, nul, nul, nul) == L.OK
 
 
 def test_status_strings():
@@ -185,9 +217,11 @@ def test_partial_kv_workspace_matches_oracle_segments(seed, strategy):
     segs = [s for r in range(C) for s in op.segments[r]]
     rows = sum(((s.q_pos0 + (s.q_len - 1) * s.q_pos_step) // kv_block + 1) * s.q_len for s in segs)
     mb = max([(s.q_pos0 + (s.q_len - 1) * s.q_pos_step) // kv_block + 1 for s in segs] or [0])
+    longest = max([s.q_len for s in segs] or [0])
     r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
     expect = r256((2 * len(segs) + 2) * 8) + r256(rows * Hq * dv * 4) + r256(rows * Hq * 4) + 256
-    assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv) == (expect, mb)
+    assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv) == \
+        (expect, mb, longest)
 
 
 def test_select_pass_matches_oracle():
@@ -256,76 +290,90 @@ def test_workspace_size_from_segments_matches_plan_sizing(seed, strategy):
              op.gather_idx[s.q_row0], s.req] for r in range(C) for s in op.segments[r]]
     lib = L.load()
     seg = torch.tensor(rows or [[0] * 8], dtype=torch.int32)
-    b1, m1 = ctypes.c_int64(), ctypes.c_int32()
+    b1, m1, r1 = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
     assert lib.cp_partial_kv_workspace_size_segs(ctypes.c_void_p(seg.data_ptr()), len(rows),
                                                  kv_block, Hq, dv, ctypes.byref(b1),
-                                                 ctypes.byref(m1)) == L.OK
-    b2, m2 = api.cp_partial_kv_workspace_size(new, pre, C, strategy, kv_block, Hq, dv)
-    assert (b1.value, m1.value) == (b2, m2)
+                                                 ctypes.byref(m1), ctypes.byref(r1)) == L.OK
+    assert (b1.value, m1.value, r1.value) == api.cp_partial_kv_workspace_size(
+        new, pre, C, strategy, kv_block, Hq, dv)
 
 
 def test_workspace_size_for_decode_segment():
     import torch
     lib = L.load()
     seg = torch.tensor([[0, 64, 8191, 0, 0, 8192, 0, 0]], dtype=torch.int32)
-    b, m = ctypes.c_int64(), ctypes.c_int32()
+    b, m, r = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
     assert lib.cp_partial_kv_workspace_size_segs(ctypes.c_void_p(seg.data_ptr()), 1, 512, 32, 128,
-                                                 ctypes.byref(b), ctypes.byref(m)) == L.OK
+                                                 ctypes.byref(b), ctypes.byref(m), None) == L.OK
     rows = 16 * 64                       # 16 blocks of 512 keys, 64 rows each
     expect = 256 + ((rows * 32 * 128 * 4 + 255) // 256) * 256 + ((rows * 32 * 4 + 255) // 256) * 256 + 256
     assert (b.value, m.value) == (expect, 16)
+    assert api.cp_partial_kv_workspace_size_segs(seg, 512, 32, 128) == (expect, 16, 64)
 
 
-def _host_plan(new, pre, C, strategy):
-    """A ShardPlan on the CPU built from the oracle's plan (for host logic)."""
-    import torch
+def _oracle_segments(new, pre, C, strategy):
+    """The oracle plan's segments in table order, as cp_segment_t rows."""
     op = oplan.make_plan(new, pre, C, strategy)
-    rows = []
+    rows, shard = [], []
     for r in range(C):
         for s in op.segments[r]:
-            rows.append([s.q_row0, s.q_len, s.q_pos0, s.q_pos_step, s.kv_row0, s.kv_len, 0, s.req])
-    i32 = torch.int32
-    empty = torch.empty(0, dtype=i32)
-    return api.ShardPlan(
-        cp_size=C, strategy=L.ZIGZAG if strategy == "zigzag" else L.INTERLEAVE,
-        rows_per_rank=[len(op.rank_rows[r]) for r in range(C)],
-        segs_per_rank=[len(op.segments[r]) for r in range(C)], tiles_per_rank=[0] * C,
-        segs=torch.tensor(rows or [[0] * 8], dtype=i32), seg_offsets=empty, row_offsets=empty,
-        gather_idx=empty, positions=empty, restore_idx=empty, tiles=empty,
-        new_lens_dev=torch.tensor(list(new) or [0], dtype=i32),
-        prefix_lens_dev=torch.tensor(list(pre) or [0], dtype=i32), num_reqs=len(new))
+            rows.append([s.q_row0, s.q_len, s.q_pos0, s.q_pos_step, s.kv_row0, s.kv_len,
+                         op.gather_idx[s.q_row0], s.req])
+            shard.append(r)
+    return rows, shard
 
 
 @pytest.mark.parametrize("seed", range(12))
 def test_pass_q_schedule_covers_every_visible_key_once(seed):
-    """Host logic of the ring schedule: over all launches, each segment meets
-    every key its rows can see exactly once, at hop s from the blocks of rank
-    (its shard + s) mod C, and no launch holds a segment twice."""
+    """The library's ring schedule (host call) against the oracle: every entry
+    is a copy of an oracle plan segment, its window is the oracle's resident
+    KV block of rank (shard + hop) mod C, no launch holds a segment twice, and
+    over all launches each segment meets every key its rows can see exactly
+    once."""
+    from oracle import pipeline as opipe
     new, pre = W.random_batch(900 + seed, max_reqs=5, max_new=400, max_prefix=200)
     C = [1, 2, 3, 4, 8, 5][seed % 6]
     strategy = "zigzag" if seed % 2 == 0 else "interleave"
-    plan = _host_plan(new, pre, C, strategy)
-    segs = api.segments_host(plan)
-    shard = [r for r, c in enumerate(plan.segs_per_rank) for _ in range(c)]
-    sched = api.pass_q_schedule(plan)
-    assert len(sched) <= 2 * C
+    segs, shard = _oracle_segments(new, pre, C, strategy)
+    sched = api.pass_q_schedule_host(new, pre, C, strategy)
+    assert sched.num_launches <= 2 * C
+    assert sched.launch_first[-1] == len(sched.seg_ids)
     seen = {i: [] for i in range(len(segs))}
-    for launch in sched:
-        assert len(set(launch.seg_ids)) == len(launch.seg_ids)
-        assert launch.segs.shape[0] == launch.windows.shape[0] == len(launch.seg_ids)
-        for i, row, (lo, hi) in zip(launch.seg_ids, launch.segs.tolist(),
-                                    launch.windows.tolist()):
-            assert row == [segs[i][f] for f in api.SEGMENT_FIELDS]
-            sg = segs[i]
-            host = (shard[i] + launch.hop) % C
-            blocks = api.pass_q_kv_blocks(new[sg["req"]] + pre[sg["req"]], C)
-            assert (lo, hi) == tuple(blocks[host][launch.block]), blocks
-            seen[i].append((lo, hi))
+    rows, wins = sched.segs.tolist(), sched.windows.tolist()
+    for li in range(sched.num_launches):
+        hop, block = sched.hops[li], sched.blocks[li]
+        ids = sched.seg_ids[sched.launch_first[li]: sched.launch_first[li + 1]]
+        assert ids and len(set(ids)) == len(ids)
+        for e in range(sched.launch_first[li], sched.launch_first[li + 1]):
+            i = sched.seg_ids[e]
+            assert rows[e] == segs[i]
+            req = segs[i][7]
+            host = (shard[i] + hop) % C
+            expect = opipe.resident_kv_windows(new[req] + pre[req], C)[host][block]
+            assert tuple(wins[e]) == tuple(expect)
+            seen[i].append(tuple(wins[e]))
     for i, sg in enumerate(segs):
-        last = sg["q_pos0"] + (sg["q_len"] - 1) * sg["q_pos_step"]
-        covered = sorted(seen[i])
-        keys = [k for lo, hi in covered for k in range(lo, min(hi, last + 1))]
-        assert keys == list(range(last + 1)), (i, covered)
+        last = sg[2] + (sg[1] - 1) * sg[3]
+        keys = [k for lo, hi in sorted(seen[i]) for k in range(lo, min(hi, last + 1))]
+        assert keys == list(range(last + 1)), (i, sorted(seen[i]))
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+def test_host_segment_table_matches_oracle_plan(seed, strategy):
+    """The library's host mirror of the plan, read back through the ring
+    schedule's segment copies, holds exactly the oracle plan's segments, field
+    by field."""
+    new, pre = W.random_batch(1700 + seed, max_reqs=6, max_new=600, max_prefix=300)
+    C = [1, 2, 3, 4, 8, 6, 16, 5][seed]
+    segs, _ = _oracle_segments(new, pre, C, strategy)
+    sched = api.pass_q_schedule_host(new, pre, C, strategy)
+    got = {}
+    for e, i in enumerate(sched.seg_ids):
+        got[i] = sched.segs[e].tolist()
+    # every segment appears: at some hop it visits the rank holding key 0
+    assert sorted(got) == list(range(len(segs)))
+    assert [got[i] for i in range(len(segs))] == segs
 
 
 def _c_param_kind(decl):
@@ -364,13 +412,13 @@ def test_binding_signatures_match_the_header():
 
 
 @pytest.mark.parametrize("seed", range(10))
-def test_plan_segment_row_bound_holds(seed):
-    """The host bound on segment rows (it decides head packing in the
-    partial-KV call) is never below a segment of the oracle's plan."""
+def test_sizing_reports_the_longest_segment(seed):
+    """The longest-segment figure of the library's sizing call (it decides head
+    packing in the partial-KV call) equals the longest segment of the
+    oracle's plan."""
     new, pre = W.random_batch(1300 + seed, max_reqs=6, max_new=500, max_prefix=100)
     C = [1, 2, 3, 4, 8][seed % 5]
     for strategy in ("zigzag", "interleave"):
         op = oplan.make_plan(new, pre, C, strategy)
         longest = max([s.q_len for r in range(C) for s in op.segments[r]] or [0])
-        bound = api.plan_max_segment_rows(new, C, strategy)
-        assert longest <= bound <= longest + 1, (strategy, longest, bound)
+        assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, 512, 8, 64)[2] == longest

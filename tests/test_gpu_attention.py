@@ -18,7 +18,8 @@ from oracle import attention as oatt
 from oracle import merge as omerge
 from oracle import plan as oplan
 
-from gpu_common import assert_attn_close, boundary_rows, np64, oracle_dense_rows
+from gpu_common import (assert_attn_close, boundary_rows, np64, oracle_dense_rows,
+                        stepwise_partial_kv)
 
 pytestmark = pytest.mark.gpu
 
@@ -110,7 +111,7 @@ def test_partial_kv_small_all_rows():
         status = cpa.new_status()
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
         q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
-        o, lse = cpa.cp_partial_kv_attention(q_cat, inputs["k"].cuda(), inputs["v"].cuda(), plan,
+        o, lse = stepwise_partial_kv(q_cat, inputs["k"].cuda(), inputs["v"].cuda(), plan,
                                              w.scale, w.kv_block, status=status)
         torch.cuda.synchronize()
         cpa.check_status(status, "partial kv")
@@ -125,7 +126,7 @@ def test_partialkv_128k_sampled():
     k = inputs["k"].cuda()
     v = inputs["v"].cuda()
     q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
-    o, lse = cpa.cp_partial_kv_attention(q_cat, k, v, plan, w.scale, w.kv_block, status=status)
+    o, lse = stepwise_partial_kv(q_cat, k, v, plan, w.scale, w.kv_block, status=status)
     torch.cuda.synchronize()
     cpa.check_status(status, w.name)
     rows = sorted(set(W.sample_rows(11, w.total_new, 16) +
@@ -388,14 +389,12 @@ def test_partial_kv_fused_small_all_rows(strategy):
     q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
     k, v = inputs["k"].cuda(), inputs["v"].cuda()
     o, lse, ws = cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
-                                        new_lens=w.new_lens, prefix_lens=w.prefix_lens,
                                         status=status)
     torch.cuda.synchronize()
     cpa.check_status(status, "fused partial kv")
     assert_attn_close(o, lse, O_ref, L_ref, f"pkv fused/{strategy}")
     # cat order, fp32 output, workspace reused
     o2, lse2, _ = cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
-                                         new_lens=w.new_lens, prefix_lens=w.prefix_lens,
                                          workspace=ws, dst_rows=None, out_fp32=True,
                                          status=status)
     torch.cuda.synchronize()
@@ -415,7 +414,6 @@ def test_partial_kv_fused_mla_small():
     q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
     k = inputs["k"].cuda()
     o, lse, _ = cpa.cp_attn_partial_kv(plan, q_cat, k, k[:, :, :512], w.scale, 100,
-                                       new_lens=w.new_lens, prefix_lens=w.prefix_lens,
                                        status=status)
     torch.cuda.synchronize()
     cpa.check_status(status, "fused partial kv mla")
@@ -429,8 +427,7 @@ def test_partialkv_128k_fused_sampled():
     plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", status=status)
     q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
     o, lse, ws = cpa.cp_attn_partial_kv(plan, q_cat, inputs["k"].cuda(), inputs["v"].cuda(),
-                                        w.scale, w.kv_block, new_lens=w.new_lens,
-                                        prefix_lens=w.prefix_lens, status=status)
+                                        w.scale, w.kv_block, status=status)
     torch.cuda.synchronize()
     cpa.check_status(status, w.name)
     del ws
@@ -445,10 +442,10 @@ def test_partial_kv_workspace_too_small_is_reported():
     plan = cpa.make_plan([500], [0], 2, "zigzag")
     q = torch.zeros(500, 2, 64, dtype=torch.bfloat16, device="cuda")
     k = torch.zeros(500, 1, 64, dtype=torch.bfloat16, device="cuda")
-    need, _ = cpa.cp_partial_kv_workspace_size([500], [0], 2, "zigzag", 64, 2, 64)
+    need = cpa.cp_partial_kv_workspace_size([500], [0], 2, "zigzag", 64, 2, 64)[0]
     small = torch.empty(need // 3, dtype=torch.uint8, device="cuda")
     status = cpa.new_status()
-    cpa.cp_attn_partial_kv(plan, q, k, k, 0.125, 64, new_lens=[500], prefix_lens=[0],
+    cpa.cp_attn_partial_kv(plan, q, k, k, 0.125, 64,
                            workspace=small, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) in (cpa.api.L.ERR_INVALID_ARG, cpa.api.L.ERR_RANGE)
@@ -617,12 +614,12 @@ def test_partial_kv_short_requests_pack_heads():
                                                w.scale)
     k, v = inputs["k"].cuda(), inputs["v"].cuda()
     for strategy in w.strategies:
-        assert cpa.api.plan_max_segment_rows(w.new_lens, w.cp_size, strategy) <= 64
+        assert cpa.cp_partial_kv_workspace_size(w.new_lens, w.prefix_lens, w.cp_size, strategy,
+                                            w.kv_block, w.Hq, w.dv)[2] <= 64
         status = cpa.new_status()
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, strategy, status=status)
         q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[: w.total_new], status=status)
         outs = [cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, w.kv_block,
-                                       new_lens=w.new_lens, prefix_lens=w.prefix_lens,
                                        max_seg_rows=hint, status=status)[:2]
                 for hint in (None, 0)]
         torch.cuda.synchronize()

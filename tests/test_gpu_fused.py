@@ -258,41 +258,65 @@ def test_pass_q_ring_128k_sampled():
 
 # ------------------------------------------------------ host pipeline ----
 
-@pytest.mark.parametrize("name", ["varlen6_gqa", "single1k_d64"])
-def test_prefill_pipeline_matches_single_calls(name):
-    """Batches submitted through the overlapped host pipeline (two buffer sets,
-    three streams) give exactly what one cp_prefill_attention call gives."""
+def _host_batch(w, b, v_is_k_prefix=False):
+    ho = torch.empty((w.total_new, w.Hq, w.dv), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.total_new, w.Hq), dtype=torch.float32).pin_memory()
+    return (b["q"].pin_memory(), b["k"].pin_memory(),
+            None if v_is_k_prefix else b["v"].pin_memory(), ho, hl)
+
+
+@pytest.mark.parametrize("name,strategy", [("varlen6_gqa", "zigzag"), ("varlen6_gqa", "interleave"),
+                                           ("single1k_d64", "zigzag")])
+def test_prefill_host_matches_single_calls(name, strategy):
+    """Batches run host to host by cp_prefill_host (two device buffer sets,
+    three streams) give exactly what one cp_prefill_attention call gives on
+    each batch, and match the oracle."""
     w = W.WORKLOADS[name]
     batches = [W.make_inputs(w, seed_offset=i) for i in range(5)]
-    pipe = cpa.PrefillPipeline(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], w.Hq,
-                               w.Hkv, w.d, w.dv, w.scale)
-    outs = []
-    for b in batches:
-        ho = torch.empty((w.total_new, w.Hq, w.dv), dtype=torch.bfloat16).pin_memory()
-        hl = torch.empty((w.total_new, w.Hq), dtype=torch.float32).pin_memory()
-        pipe.submit(b["q"].pin_memory(), b["k"].pin_memory(), b["v"].pin_memory(), ho, hl)
-        outs.append((ho, hl))
-    pipe.synchronize()
-    for b, (ho, hl) in zip(batches, outs):
-        status, plan, _, q, k, v = setup(w, w.strategies[0], b)
-        o, lse = cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=status,
-                                          fuse_restore=True)
+    host = [_host_batch(w, b) for b in batches]
+    status = cpa.new_status()
+    _, streams = cpa.cp_prefill_host(w.new_lens, w.prefix_lens, w.cp_size, strategy, w.Hq, w.Hkv,
+                                     w.d, w.dv, w.scale, host, status=status)
+    streams[2].synchronize()
+    cpa.check_status(status, "host prefill")
+    for b, (_, _, _, ho, hl) in zip(batches, host):
+        st, plan, _, q, k, v = setup(w, strategy, b)
+        o, lse = cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=st, fuse_restore=True)
         torch.cuda.synchronize()
         assert torch.equal(ho, o.cpu())
         assert torch.equal(hl, lse.cpu())
+    O_ref, L_ref = dense_ref(w, batches[-1])
+    assert_attn_close(host[-1][3], host[-1][4], O_ref, L_ref, f"{name}/{strategy}/host prefill")
 
 
-def test_prefill_pipeline_mla_latent_view():
+def test_prefill_host_mla_latent_view():
     w = mla_case([300, 77], [0, 40], 4, 3, 951)
     b = W.make_inputs(w)
-    pipe = cpa.PrefillPipeline(w.new_lens, w.prefix_lens, w.cp_size, "interleave", w.Hq, w.Hkv,
-                               w.d, w.dv, w.scale, v_is_k_prefix=True)
-    ho = torch.empty((w.total_new, w.Hq, w.dv), dtype=torch.bfloat16).pin_memory()
-    hl = torch.empty((w.total_new, w.Hq), dtype=torch.float32).pin_memory()
-    pipe.submit(b["q"].pin_memory(), b["k"].pin_memory(), None, ho, hl)
-    pipe.synchronize()
+    host = [_host_batch(w, b, v_is_k_prefix=True)]
+    status = cpa.new_status()
+    _, streams = cpa.cp_prefill_host(w.new_lens, w.prefix_lens, w.cp_size, "interleave", w.Hq,
+                                     w.Hkv, w.d, w.dv, w.scale, host, v_is_k_prefix=True,
+                                     status=status)
+    streams[2].synchronize()
+    cpa.check_status(status, "host prefill mla")
     O_ref, L_ref = dense_ref(w, b)
-    assert_attn_close(ho, hl, O_ref, L_ref, "mla/pipeline")
+    assert_attn_close(host[0][3], host[0][4], O_ref, L_ref, "mla/host prefill")
+
+
+def test_prefill_host_one_stream():
+    """The same call with one stream for all three roles (nothing overlaps)."""
+    w = W.WORKLOADS["varlen6_gqa"]
+    b = W.make_inputs(w, seed_offset=3)
+    host = [_host_batch(w, b) for _ in range(3)]
+    s = torch.cuda.Stream()
+    status = cpa.new_status()
+    cpa.cp_prefill_host(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", w.Hq, w.Hkv, w.d, w.dv,
+                        w.scale, host, status=status, streams=(s, s, s))
+    s.synchronize()
+    cpa.check_status(status, "host prefill, one stream")
+    O_ref, L_ref = dense_ref(w, b)
+    for i in range(3):
+        assert_attn_close(host[i][3], host[i][4], O_ref, L_ref, f"one stream, batch {i}")
 
 
 # -------------------------------------------------- token-order prefill ----
@@ -356,8 +380,7 @@ def test_batch_without_new_tokens_is_a_no_op(strategy):
     assert q.shape[0] == 0 and plan.total_segs == 0
     outs = [cpa.cp_prefill_attention(q, k, v, plan, w.scale, status=status, fuse_restore=f)
             for f in (False, True)]
-    o, lse, _ = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, w.kv_block, new_lens=w.new_lens,
-                                       prefix_lens=w.prefix_lens, status=status)
+    o, lse, _ = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, w.kv_block, status=status)
     outs.append((o, lse))
     outs.append(cpa.cp_pass_q_attention(q, k, v, plan, w.scale, status=status))
     torch.cuda.synchronize()

@@ -451,3 +451,23 @@ def test_select_fitted_reading():
     assert osel.select_fitted(1, 131071) == "pass_q"
     assert osel.fitted_score(1000, 1000) > osel.fitted_score(2000, 2000)
     assert osel.fitted_score(1, 0) == pytest.approx(12.112)
+
+
+def test_parallel_row_harness_equals_direct_oracle_calls():
+    """The test harness that spreads oracle rows over spawned processes gives,
+    row by row, exactly the oracle's own single-process values (also with V
+    a view of K and with a key window)."""
+    import oracle_rows
+    rng = np.random.default_rng(5)
+    new, pre = [40, 7, 65], [3, 0, 20]
+    kv = sum(new) + sum(pre)
+    q = rng.standard_normal((sum(new), 4, 16))
+    k = rng.standard_normal((kv, 2, 16))
+    v = rng.standard_normal((kv, 2, 8))
+    pos, kv0 = oatt.token_tables(new, pre)
+    rows = np.array([0, 5, 39, 40, 46, 47, 100, 111])
+    for vv, pref, lo, hi in ((v, False, 0, None), (k[:, :, :8], True, 0, None), (v, False, 10, 30)):
+        O1, L1 = oatt.attention_rows(q[rows], k, vv, pos[rows], kv0[rows], 0.3, lo, hi)
+        O2, L2 = oracle_rows.attention_rows_parallel(q[rows], k, vv, pos[rows], kv0[rows], 0.3,
+                                                     lo, hi, v_is_k_prefix=pref, procs=2)
+        assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
