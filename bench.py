@@ -795,6 +795,22 @@ def bench_128k(args, dev, stream, pk, status, clk):
                              "schedule: one accumulate launch per hop and resident KV block, all "
                              "ranks in one launch with per-segment key windows) + cp_restore of "
                              "O and LSE"}
+    # the cost-driven selector fed with this run's measured attention and
+    # merge rates, at two per-GPU ring bandwidths (an InfiniBand NDR port and
+    # an NVLink 5 direction), over miss rates of a 131072-token context
+    sel = {"attn_tflops_measured": out["partial_kv"]["tflops"],
+           "merge_gbs_measured": out["merge"]["gbs"]}
+    for link in (50.0, 900.0):
+        row = {}
+        for miss in (0.01, 0.05, 0.125, 0.5, 1.0):
+            T = max(1, int(N * miss))
+            choice, ekv, eq = cpa.cp_select_pass_cost(T, N - T, Hq, w.Hkv, w.d, w.cp_size,
+                                                      out["partial_kv"]["tflops"], link,
+                                                      out["merge"]["gbs"])
+            row[f"miss_{miss}"] = {"choice": choice, "exposed_kv_ms": ekv * 1e3,
+                                   "exposed_q_ms": eq * 1e3}
+        sel[f"link_{int(link)}_gbs"] = row
+    out["selector_cost_rule"] = sel
     out["launches"] = launches
     del q, k, v, q_cat, acc, o32, o, lse
     torch.cuda.empty_cache()

@@ -26,6 +26,7 @@ from .api import (  # noqa: F401
     cp_prefill_host_workspace_size,
     cp_restore,
     cp_select_pass,
+    cp_select_pass_cost,
     cp_shard_plan,
     cp_shard_plan_sizes,
     make_plan,

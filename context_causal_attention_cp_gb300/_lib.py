@@ -25,6 +25,7 @@ SELECT_FITTED = 1
 
 DEBUG_WAIT_LIMIT_NS = 1
 DEBUG_WITHHOLD_Q = 2
+DEBUG_NVTX = 3
 
 ZIGZAG = 0
 INTERLEAVE = 1
@@ -53,6 +54,10 @@ SIGNATURES = {
                                          vp, vp, vp, i32, i32, vp, vp]),
     "cp_select_pass": (i32, [ctypes.c_int64, ctypes.c_int64, i32, i32, i32,
                              ctypes.POINTER(ctypes.c_double)]),
+    "cp_select_pass_cost": (i32, [ctypes.c_int64, ctypes.c_int64, i32, i32, i32, i32,
+                                  ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                  ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]),
     "cp_lse_merge": (i32, [vp, vp, i32, i64, i64, i32, i32, i32, vp, vp, i32, vp, i32, vp, vp]),
     "cp_restore": (i32, [vp, i32, vp, i32, i64, vp, vp, vp]),
     "cp_partial_kv_workspace_size": (i32, [c_i32p, c_i32p, i32, i32, i32, i32, i32, i32,

@@ -701,3 +701,17 @@ def cp_select_pass(new_tokens: int, cached_tokens: int, Hq: int, Hkv: int, rule=
     if r < 0:
         L.check(r, "cp_select_pass")
     return ("pass_q" if r == L.PASS_Q else "pass_kv"), score.value
+
+
+def cp_select_pass_cost(new_tokens: int, cached_tokens: int, Hq: int, Hkv: int, head_dim: int,
+                        cp_size: int, attn_tflops: float, link_gbs: float, merge_gbs: float):
+    """Pass-KV or pass-Q by exposed communication (see cp_select_pass_cost in
+    cpattn.h).  Returns ("pass_kv" | "pass_q", E_kv seconds, E_q seconds)."""
+    lib = L.load()
+    ekv, eq = ctypes.c_double(), ctypes.c_double()
+    r = lib.cp_select_pass_cost(int(new_tokens), int(cached_tokens), int(Hq), int(Hkv),
+                                int(head_dim), int(cp_size), float(attn_tflops), float(link_gbs),
+                                float(merge_gbs), ctypes.byref(ekv), ctypes.byref(eq))
+    if r < 0:
+        L.check(r, "cp_select_pass_cost")
+    return ("pass_q" if r == L.PASS_Q else "pass_kv"), ekv.value, eq.value

@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "attn_common.cuh"
+#include "trace.h"
 
 namespace cpattn {
 namespace {
@@ -326,6 +327,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (key < win_lo || key >= row_hi) x[c] = -INFINITY;
         }
       }
+      // P = 2^(x*scale - m_ref) for this row, written to TMEM as bf16 over the
+      // S columns; returns the row sum.  Warp-collective (tcgen05.st).
+      auto exp_tile = [&](float m_ref) {
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float a, b;
+            ffma2(a, b, x[q * 32 + c], x[q * 32 + c + 1], sl2, sl2, -m_ref, -m_ref);
+            a = ex2_approx(a);
+            b = ex2_approx(b);
+            fadd2(sum0, sum1, sum0, sum1, a, b);
+            pk[c >> 1] = pack_bf16x2(a, b);
+          }
+          tmem_st16(lane_addr + s_col + q * 16, pk);
+        }
+        return sum0 + sum1;
+      };
       float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
       for (int c = 4; c < BN; c += 8) {
@@ -343,22 +364,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const float m_new = move ? mx : m_run;
       const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = move ? ex2_approx(m_run - m_new_use) : 1.f;  // 0 while m_run = -inf
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float a, b;
-          ffma2(a, b, x[q * 32 + c], x[q * 32 + c + 1], sl2, sl2, -m_new_use, -m_new_use);
-          a = ex2_approx(a);
-          b = ex2_approx(b);
-          fadd2(sum0, sum1, sum0, sum1, a, b);
-          pk[c >> 1] = pack_bf16x2(a, b);
-        }
-        tmem_st16(lane_addr + s_col + q * 16, pk);
+      // The exponentials do not wait for the tile max: they are taken against
+      // the running max first, which is the final reference unless the tile
+      // moves the max (rare once a row has seen a few tiles).  Rows whose max
+      // moved take the pass again with the new reference; the warp runs a
+      // pass when any of its rows needs it (the TMEM stores are
+      // warp-collective), every row with its own reference.
+      float sum = 0.f;
+      if (__any_sync(0xffffffffu, !(move && m_run == -INFINITY))) sum = exp_tile(m_use);
+      if (__any_sync(0xffffffffu, move)) {
+        const float s2 = exp_tile(m_new_use);
+        if (move) sum = s2;
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      l_run = l_run * alpha + sum;
       // rescale the running O (its previous PV has completed: S of this
       // iteration was committed after it)
       const bool need = (it > 0) && move;
@@ -537,6 +555,9 @@ extern "C" int cp_attn_debug(int knob, long long value) {
     case CPATTN_DEBUG_WITHHOLD_Q:
       attn_debug().withhold_q = value ? 1 : 0;
       return CPATTN_OK;
+    case CPATTN_DEBUG_NVTX:
+      nvtx_flag().store(value ? 1 : 0);
+      return CPATTN_OK;
     default:
       return CPATTN_ERR_INVALID_ARG;
   }
@@ -614,6 +635,7 @@ extern "C" int cp_attn_partial(const cp_segment_t* segs_dev, int num_segs, const
                                int Hkv, int d, int dv, float scale, int kv_lo, int kv_hi, void* o,
                                int o_is_fp32, float* lse, int out_row_base, int num_out_rows,
                                int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_partial");
   if (num_out_rows < 0) return CPATTN_ERR_INVALID_ARG;
   if (num_segs > 0 && (!o || !lse || num_out_rows == 0)) return CPATTN_ERR_INVALID_ARG;
   if (o && (!a16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))) return CPATTN_ERR_ALIGNMENT;
@@ -639,6 +661,7 @@ extern "C" int cp_attn_prefill(const cp_segment_t* segs_dev, int num_segs,
                                int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
                                int dv, float scale, void* o, int o_is_fp32, float* lse,
                                int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_prefill");
   if (num_tokens < 0) return CPATTN_ERR_INVALID_ARG;
   if (num_segs > 0 && (!o || !lse || num_tokens == 0)) return CPATTN_ERR_INVALID_ARG;
   if (o && (!a16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))) return CPATTN_ERR_ALIGNMENT;
@@ -664,6 +687,7 @@ extern "C" int cp_attn_partial_restore(
     const void* v, int64_t v_row_stride, int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv,
     int d, int dv, float scale, int kv_lo, int kv_hi, const int32_t* dst_rows, void* o,
     int o_is_fp32, float* lse, int num_out_rows, int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_partial_restore");
   if (num_out_rows < 0) return CPATTN_ERR_INVALID_ARG;
   if (num_segs > 0 && (!o || !lse || !dst_rows || num_out_rows == 0))
     return CPATTN_ERR_INVALID_ARG;
@@ -692,6 +716,7 @@ extern "C" int cp_attn_partial_accumulate(
     int d, int dv, float scale, int kv_lo, int kv_hi, const int32_t* seg_windows_dev,
     float* o_acc, const float* lse_acc, float* lse_out, int out_row_base, int num_out_rows,
     int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_partial_accumulate");
   if (num_out_rows < 0 || Hq <= 0) return CPATTN_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(seg_windows_dev) & 3u) return CPATTN_ERR_ALIGNMENT;
   if (num_segs > 0 && (!o_acc || !lse_acc || !lse_out || num_out_rows == 0))

@@ -18,6 +18,7 @@
 
 #include "../../include/cpattn.h"
 #include "ptx.cuh"
+#include "trace.h"
 
 namespace cpattn {
 namespace {
@@ -260,6 +261,7 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
                             int dv, const int32_t* dst_rows, void* o_out, int o_out_is_fp32,
                             float* lse_out, int num_out_rows, int32_t* status_dev,
                             cudaStream_t stream) {
+  CPATTN_TRACE("cp_lse_merge");
   if (num_parts < 1 || num_parts > kMaxParts) return CPATTN_ERR_INVALID_ARG;
   if (rows < 0 || Hq < 1 || dv < 4 || dv > 1024 || (dv % 4) != 0) return CPATTN_ERR_INVALID_ARG;
   if (num_out_rows < 0 || (!dst_rows && num_out_rows < rows)) return CPATTN_ERR_INVALID_ARG;
@@ -307,6 +309,7 @@ extern "C" int cp_lse_merge(const float* o_parts, const float* lse_parts, int nu
 
 extern "C" int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int rows,
                           int64_t row_bytes, void* dst, int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_restore");
   if (rows < 0 || num_src_rows < 0 || row_bytes <= 0 || (row_bytes % 4) != 0)
     return CPATTN_ERR_INVALID_ARG;
   if (rows == 0) return CPATTN_OK;

@@ -26,6 +26,7 @@
 
 #include "attn_common.cuh"
 #include "host_plan.h"
+#include "trace.h"
 
 namespace cpattn {
 namespace {
@@ -417,6 +418,7 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
                                   float* lse_out, int num_out_rows, void* workspace,
                                   int64_t workspace_bytes, int32_t* status_dev,
                                   cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_partial_kv");
   if (num_segs < 0 || kv_block < 1 || max_blocks < 0 || max_blocks > 32 || num_out_rows < 0 ||
       max_seg_rows < 0)
     return CPATTN_ERR_INVALID_ARG;

@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/cpattn.h"
+#include "trace.h"
 
 namespace {
 
@@ -104,6 +105,7 @@ extern "C" int cp_attn_partial_kv_noalloc(
     const int32_t* dst_rows,
     void* o_out, int o_is_fp32, float* lse_out, int num_out_rows, int64_t workspace_bytes_needed,
     int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_partial_kv_noalloc");
   if (workspace_bytes_needed < 0) return CPATTN_ERR_INVALID_ARG;
   if (workspace_bytes_needed > (int64_t)CPATTN_NOALLOC_SCRATCH_BYTES) return CPATTN_ERR_TOO_LARGE;
   void* scratch = nullptr;

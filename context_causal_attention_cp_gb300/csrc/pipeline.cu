@@ -24,6 +24,7 @@
 
 #include "../../include/cpattn.h"
 #include "host_plan.h"
+#include "trace.h"
 
 namespace {
 
@@ -109,6 +110,7 @@ extern "C" int cp_prefill_host(const int32_t* new_lens, const int32_t* prefix_le
                                float* const* lse_host, void* workspace, int64_t workspace_bytes,
                                int32_t* status_dev, cudaStream_t compute, cudaStream_t upload,
                                cudaStream_t download) {
+  CPATTN_TRACE("cp_prefill_host");
   PrefillLayout L;
   int rc = prefill_layout(new_lens, prefix_lens, num_reqs, cp_size, strategy, Hq, Hkv, d, dv,
                           v_is_k_prefix, &L);

@@ -17,6 +17,7 @@
 
 #include "../../include/cpattn.h"
 #include "ptx.cuh"
+#include "trace.h"
 
 namespace cpattn {
 namespace {
@@ -278,6 +279,7 @@ extern "C" int cp_shard_plan(const int32_t* new_lens_dev, const int32_t* prefix_
                              int32_t* gather_idx_dev, int32_t* positions_dev,
                              int32_t* restore_idx_dev, int32_t* tiles_dev, int32_t* status_dev,
                              cudaStream_t stream) {
+  CPATTN_TRACE("cp_shard_plan");
   if (num_reqs < 0 || num_reqs > CPATTN_MAX_REQS) return CPATTN_ERR_INVALID_ARG;
   if (cp_size < 1 || cp_size > CPATTN_MAX_CP) return CPATTN_ERR_INVALID_ARG;
   if (strategy != CP_ZIGZAG && strategy != CP_INTERLEAVE) return CPATTN_ERR_INVALID_ARG;

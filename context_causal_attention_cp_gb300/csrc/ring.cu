@@ -21,6 +21,7 @@
 
 #include "attn_common.cuh"
 #include "host_plan.h"
+#include "trace.h"
 
 namespace cpattn {
 namespace {
@@ -134,6 +135,7 @@ extern "C" int cp_attn_pass_q(const cp_segment_t* entry_segs_dev, const int32_t*
                               int64_t v_head_stride, int num_kv_rows, int Hq, int Hkv, int d,
                               int dv, float scale, float* o_acc, float* lse, float* lse_scratch,
                               int32_t* status_dev, cudaStream_t stream) {
+  CPATTN_TRACE("cp_attn_pass_q");
   if (num_launches < 0 || num_q_rows < 0 || Hq < 1 || dv < 4 || (dv % 4) != 0)
     return CPATTN_ERR_INVALID_ARG;
   if (num_q_rows == 0) return CPATTN_OK;

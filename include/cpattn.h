@@ -268,6 +268,31 @@ int cp_attn_partial_accumulate(const cp_segment_t* segs_dev, int num_segs,
 int cp_select_pass(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, int rule,
                    double* score);
 
+/* Pass-KV or pass-Q by cost, from measured rates.  [CPB-3.5]  Host only.
+ * The page lays a roofline condition over the message comparison (pass-KV is
+ * preferred when its per-hop SendRecv hides behind that hop's attention) and
+ * refines pass-Q with the All2All that returns its scattered partials before
+ * the LSE merge.  This call prices both for one rank of a ring of cp_size
+ * ranks (T = new_tokens, P = cached_tokens, d = head_dim = dv, bf16 messages,
+ * fp32 partials):
+ *   F     = 2 Hq 2d (T P + T (T+1) / 2)          attention flops of the step
+ *   t_a   = F / C^2 / (attn_tflops 1e12)         attention of one hop
+ *   t_kv  = 2 ceil((T+P)/C) Hkv d 2 / (link_gbs 1e9)      K and V of one hop
+ *   t_q   = ceil(T/C) Hq d 2 / (link_gbs 1e9)             Q of one hop
+ *   t_a2a = (C-1)/C ceil(T/C) Hq (d+1) 4 / (link_gbs 1e9) the All2All
+ *   t_m   = C ceil(T/C) Hq (d+1) 4 / (merge_gbs 1e9)      the final merge
+ *   E_kv  = (C-1) max(0, t_kv - t_a)
+ *   E_q   = (C-1) max(0, t_q - t_a) + t_a2a + t_m
+ * and returns CP_PASS_KV iff E_kv <= E_q, else CP_PASS_Q.  attn_tflops and
+ * merge_gbs are meant to be this library's measured attention and merge
+ * rates; link_gbs the per-GPU ring bandwidth.  exposed_kv_s / exposed_q_s
+ * (nullable) receive E_kv and E_q in seconds.  Arguments as cp_select_pass,
+ * plus head_dim in [1, 4096], cp_size in [1, CPATTN_MAX_CP] and positive
+ * finite rates; otherwise CPATTN_ERR_INVALID_ARG. */
+int cp_select_pass_cost(int64_t new_tokens, int64_t cached_tokens, int Hq, int Hkv, int head_dim,
+                        int cp_size, double attn_tflops, double link_gbs, double merge_gbs,
+                        double* exposed_kv_s, double* exposed_q_s);
+
 /* ------------------------------------------------------------------------ */
 /* Partial-KV (ring-style) decomposition in one call.  [CPB-2.1] item 2,
  * [CPB-3.3] (pass-KV: a rank's queries meet the KV one block at a time, each
@@ -498,9 +523,14 @@ int cp_restore(const void* src, int num_src_rows, const int32_t* idx_dev, int ro
  *     CPATTN_ERR_TIMEOUT to the status word, drains its own copies, frees its
  *     tensor memory and returns (outputs of the affected tiles are not
  *     written).  Nothing traps and no wait is unbounded.  Reset to 0 after use.
+ *   CPATTN_DEBUG_NVTX: value != 0 turns on NVTX ranges named after each entry
+ *     point that queues device work (pushed for the host call's duration, for
+ *     timeline tools); 0 turns them off.  Off by default unless the
+ *     environment variable CPATTN_NVTX is set to a non-zero value.
  * Returns CPATTN_OK or CPATTN_ERR_INVALID_ARG. */
 #define CPATTN_DEBUG_WAIT_LIMIT_NS 1
 #define CPATTN_DEBUG_WITHHOLD_Q 2
+#define CPATTN_DEBUG_NVTX 3
 int cp_attn_debug(int knob, long long value);
 
 /* Human-readable name of a status code (static string). */

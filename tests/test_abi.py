@@ -199,6 +199,30 @@ def test_ring_and_host_prefill_calls_validate_on_host():
     assert lib.cp_prefill_host(*zero, nul, 0, nul, nul, nul, nul) == L.OK
 
 
+def test_select_pass_cost_matches_oracle():
+    """Host logic of cp_select_pass_cost against the oracle on a grid: the
+    same exposed times (to rounding) and the same choice."""
+    from oracle import select as osel
+    for Hq, Hkv in ((128, 8), (32, 8), (64, 64)):
+        for T in (1, 7, 1000, 16384, 131072):
+            for P in (0, 3, 4096, 124518):
+                for C in (1, 2, 4, 8):
+                    for tf, link, merge in ((620.0, 50.0, 3000.0), (1500.0, 450.0, 6000.0)):
+                        got, ekv, eq = api.cp_select_pass_cost(T, P, Hq, Hkv, 128, C, tf, link,
+                                                               merge)
+                        r_kv, r_q = osel.exposed_times(T, P, Hq, Hkv, 128, C, tf, link, merge)
+                        assert ekv == pytest.approx(r_kv, rel=1e-12, abs=1e-18)
+                        assert eq == pytest.approx(r_q, rel=1e-12, abs=1e-18)
+                        if abs(r_kv - r_q) > 1e-9 * max(r_kv, r_q):
+                            assert got == osel.select_by_cost(T, P, Hq, Hkv, 128, C, tf, link,
+                                                              merge)
+    lib = L.load()
+    for bad in ((0, 0, 8, 8, 128, 4, 1.0, 1.0, 1.0), (1, 0, 8, 8, 128, 4, 0.0, 1.0, 1.0),
+                (1, 0, 8, 8, 128, 4, 1.0, float("inf"), 1.0), (1, 0, 8, 3, 128, 4, 1.0, 1.0, 1.0),
+                (1, 0, 8, 8, 0, 4, 1.0, 1.0, 1.0), (1, 0, 8, 8, 128, 0, 1.0, 1.0, 1.0)):
+        assert lib.cp_select_pass_cost(*bad, None, None) == L.ERR_INVALID_ARG, bad
+
+
 def test_status_strings():
     for code in (L.OK, L.ERR_INVALID_ARG, L.ERR_UNSUPPORTED, L.ERR_CUDA, L.ERR_TIMEOUT,
                  L.ERR_ALIGNMENT, L.ERR_RANGE, L.ERR_TOO_LARGE):
@@ -422,3 +446,16 @@ def test_sizing_reports_the_longest_segment(seed):
         op = oplan.make_plan(new, pre, C, strategy)
         longest = max([s.q_len for r in range(C) for s in op.segments[r]] or [0])
         assert api.cp_partial_kv_workspace_size(new, pre, C, strategy, 512, 8, 64)[2] == longest
+
+
+def test_nvtx_knob():
+    """The NVTX switch of cp_attn_debug toggles, and host validation is the
+    same with the ranges on (no tool attached: the ranges are no-ops)."""
+    lib = L.load()
+    try:
+        assert lib.cp_attn_debug(L.DEBUG_NVTX, 1) == L.OK
+        assert lib.cp_restore(None, 4, None, 4, 22, None, None, None) == L.ERR_INVALID_ARG
+        assert lib.cp_attn_debug(L.DEBUG_NVTX, 0) == L.OK
+    finally:
+        lib.cp_attn_debug(L.DEBUG_NVTX, 0)
+    assert lib.cp_attn_debug(99, 1) == L.ERR_INVALID_ARG

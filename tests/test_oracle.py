@@ -471,3 +471,95 @@ def test_parallel_row_harness_equals_direct_oracle_calls():
         O2, L2 = oracle_rows.attention_rows_parallel(q[rows], k, vv, pos[rows], kv0[rows], 0.3,
                                                      lo, hi, v_is_k_prefix=pref, procs=2)
         assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+# ------------------------------------------------ cost-driven selector ----
+
+@pytest.mark.parametrize("link_gbs", [25.0, 50.0, 450.0])
+@pytest.mark.parametrize("ratio", [4, 8, 16])
+def test_select_cost_page_statements(link_gbs, ratio):
+    """§3.5: decode (T = 1) over a long cache picks pass-Q; full prefill under
+    GQA picks pass-KV (its SendRecv hides behind the attention), for attention
+    rates and links of real GPUs."""
+    from oracle import select as osel
+    Hkv = 8
+    Hq = ratio * Hkv
+    for C in (2, 4, 8):
+        for tf in (300.0, 1000.0, 2000.0):
+            for P in (4096, 131071, 10 ** 6):
+                assert osel.select_by_cost(1, P, Hq, Hkv, 128, C, tf, link_gbs, 3000.0) == "pass_q"
+            for T in (16384, 131072):
+                assert osel.select_by_cost(T, 0, Hq, Hkv, 128, C, tf, link_gbs, 3000.0) == \
+                    "pass_kv"
+
+
+def test_select_cost_reduces_to_the_message_rule_without_overlap():
+    """With no overlap to gain (a very slow link) and the All2All and merge
+    terms negligible (a long ring, a free merge), the exposed times are the
+    ring's messages, so the cost rule decides like the message rule (pinned
+    to the page's 12.5 %) away from the tie."""
+    from oracle import select as osel
+    C = 1024
+    for Hq, Hkv in ((128, 8), (32, 8), (64, 64)):
+        for Tb in (1, 3, 17, 100):
+            for Pb in (0, 1, 5, 64, 1000):
+                T, P = Tb * C, Pb * C
+                lhs, rhs = T * Hq, 2 * (T + P) * Hkv
+                if abs(lhs - rhs) <= 0.02 * rhs:
+                    continue
+                assert osel.select_by_cost(T, P, Hq, Hkv, 128, C, 1000.0, 1e-6, 1e12) == \
+                    osel.select_by_messages(T, P, Hq, Hkv), (T, P, Hq, Hkv)
+
+
+def _check_slow_attention_hides_pass_kv():
+    from oracle import select as osel
+    for T in (1, 100, 4096):
+        for P in (0, 10 ** 5):
+            e_kv, e_q = osel.exposed_times(T, P, 128, 8, 128, 4, 1e-9, 50.0, 3000.0)
+            assert e_kv == 0.0 and e_q > 0.0
+            assert osel.select_by_cost(T, P, 128, 8, 128, 4, 1e-9, 50.0, 3000.0) == "pass_kv"
+
+
+def test_select_cost_slow_attention_hides_pass_kv():
+    """The roofline condition: when attention is slow enough that any hop's
+    SendRecv hides behind it, pass-KV wins whatever the miss rate."""
+    _check_slow_attention_hides_pass_kv()
+
+
+def _check_all2all_refines_pass_q():
+    from oracle import select as osel
+    for C in (2, 4, 8):
+        for total in (8192, 131072):
+            T = total // 8                     # 12.5 %: the message rule's tie for 128 / 8 heads
+            assert osel.select_by_messages(T, total - T, 128, 8) == "pass_q"
+            assert osel.select_by_cost(T, total - T, 128, 8, 128, C, 1000.0, 1e-6, 1e12) == \
+                "pass_kv"
+
+
+def test_select_cost_all2all_refines_pass_q():
+    """The page's refinement counts pass-Q's All2All: at the message rule's
+    tie (equal ring messages) and without overlap, pass-Q still has its
+    partials to move, so pass-KV wins."""
+    _check_all2all_refines_pass_q()
+
+
+def test_planted_cost_rule_mistakes_are_caught(monkeypatch):
+    """Plausible slips in the cost rule each fail a pin: dropping the overlap
+    with attention fails the roofline pin; charging the All2All to pass-KV
+    instead of pass-Q fails the refinement pin."""
+    from oracle import select as osel
+    real = osel.exposed_times
+
+    def no_overlap(T, P, Hq, Hkv, d, C, tf, link, merge):
+        return real(T, P, Hq, Hkv, d, C, 1e30, link, merge)   # attention takes no time
+    monkeypatch.setattr(osel, "exposed_times", no_overlap)
+    with pytest.raises(AssertionError):
+        _check_slow_attention_hides_pass_kv()
+
+    def a2a_on_kv(T, P, Hq, Hkv, d, C, tf, link, merge):
+        e_kv, e_q = real(T, P, Hq, Hkv, d, C, tf, link, merge)
+        partials = math.ceil(T / C) * Hq * (d + 1) * 4 * (C - 1) / C / (link * 1e9)
+        return e_kv + partials, e_q - partials
+    monkeypatch.setattr(osel, "exposed_times", a2a_on_kv)
+    with pytest.raises(AssertionError):
+        _check_all2all_refines_pass_q()
