@@ -327,26 +327,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (key < win_lo || key >= row_hi) x[c] = -INFINITY;
         }
       }
-      // P = 2^(x*scale - m_ref) for this row, written to TMEM as bf16 over the
-      // S columns; returns the row sum.  Warp-collective (tcgen05.st).
-      auto exp_tile = [&](float m_ref) {
-        float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < BN / 32; ++q) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float a, b;
-            ffma2(a, b, x[q * 32 + c], x[q * 32 + c + 1], sl2, sl2, -m_ref, -m_ref);
-            a = ex2_approx(a);
-            b = ex2_approx(b);
-            fadd2(sum0, sum1, sum0, sum1, a, b);
-            pk[c >> 1] = pack_bf16x2(a, b);
-          }
-          tmem_st16(lane_addr + s_col + q * 16, pk);
-        }
-        return sum0 + sum1;
-      };
       float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
 #pragma unroll
       for (int c = 4; c < BN; c += 8) {
@@ -364,19 +344,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const float m_new = move ? mx : m_run;
       const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = move ? ex2_approx(m_run - m_new_use) : 1.f;  // 0 while m_run = -inf
-      // The exponentials do not wait for the tile max: they are taken against
-      // the running max first, which is the final reference unless the tile
-      // moves the max (rare once a row has seen a few tiles).  Rows whose max
-      // moved take the pass again with the new reference; the warp runs a
-      // pass when any of its rows needs it (the TMEM stores are
-      // warp-collective), every row with its own reference.
-      float sum = 0.f;
-      if (__any_sync(0xffffffffu, !(move && m_run == -INFINITY))) sum = exp_tile(m_use);
-      if (__any_sync(0xffffffffu, move)) {
-        const float s2 = exp_tile(m_new_use);
-        if (move) sum = s2;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float a, b;
+          ffma2(a, b, x[q * 32 + c], x[q * 32 + c + 1], sl2, sl2, -m_new_use, -m_new_use);
+          a = ex2_approx(a);
+          b = ex2_approx(b);
+          fadd2(sum0, sum1, sum0, sum1, a, b);
+          pk[c >> 1] = pack_bf16x2(a, b);
+        }
+        tmem_st16(lane_addr + s_col + q * 16, pk);
       }
-      l_run = l_run * alpha + sum;
+      l_run = l_run * alpha + (sum0 + sum1);
       // rescale the running O (its previous PV has completed: S of this
       // iteration was committed after it)
       const bool need = (it > 0) && move;

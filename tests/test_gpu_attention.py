@@ -516,6 +516,34 @@ def test_decode_sweep_split_kv(kv_block):
     assert_attn_close(out, lse, O_ref, L_ref, f"decode split {kv_block}")
 
 
+@pytest.mark.parametrize("kv_block", [2048, 4096, 8192])
+def test_decode_step_as_one_merge_over_all_ranks(kv_block):
+    """The decode step in one call with no second merge: the 8 ranks' KV
+    caches (each rank's interleaved tokens contiguous, rank after rank) form
+    one segment, its keys split in blocks of kv_block that never straddle two
+    ranks' caches, so every block partial is part of one rank's partial and
+    the library's LSE merge of all of them is the merge of the 8 rank
+    partials.  Equals attention over all 65536 keys."""
+    m = W.MERGE_SWEEP
+    inputs = W.make_merge_sweep_inputs()
+    q, k, v = inputs["q"].cuda(), inputs["k"].cuda(), inputs["v"].cuda()
+    S, nq = m["shards"], m["queries"]
+    n_kv = m["kv_tokens"] // S
+    assert n_kv % kv_block == 0
+    Hkv, d, dv = k.shape[1], k.shape[2], v.shape[2]
+    k_rank = k.view(n_kv, S, Hkv, d).transpose(0, 1).contiguous().view(S * n_kv, Hkv, d)
+    v_rank = v.view(n_kv, S, Hkv, dv).transpose(0, 1).contiguous().view(S * n_kv, Hkv, dv)
+    seg = torch.tensor([[0, nq, S * n_kv - 1, 0, 0, S * n_kv, 0, 0]], dtype=torch.int32)
+    status = cpa.new_status()
+    out, lse, _ = cpa.cp_attn_split_kv(seg.cuda(), q, k_rank, v_rank, m["scale"], kv_block,
+                                       segs_host=seg, status=status)
+    torch.cuda.synchronize()
+    cpa.check_status(status, "decode one merge")
+    O_ref, L_ref = oatt.decode_attention(np64(inputs["q"]), np64(inputs["k"]), np64(inputs["v"]),
+                                         m["scale"], np.arange(m["kv_tokens"]))
+    assert_attn_close(out, lse, O_ref, L_ref, f"decode one merge {kv_block}")
+
+
 @pytest.mark.parametrize("kv_block", [512, 4096])
 def test_decode_one_call_over_all_ranks(kv_block):
     """The decode step as the bench times it: each rank's KV cache holds its

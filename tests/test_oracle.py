@@ -563,3 +563,22 @@ def test_planted_cost_rule_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(osel, "exposed_times", a2a_on_kv)
     with pytest.raises(AssertionError):
         _check_all2all_refines_pass_q()
+
+
+def test_fitted_heuristic_readings_miss_the_page_switch_point():
+    """Documents why the fitted heuristic stays unpinned: under every reading
+    tried (log base e, 2 or 10; T and P in tokens, thousands of tokens or
+    tokens per rank at CP=4) the switch of h(T, P) at a 131072-token context
+    is nowhere near the page's measured ~5 % miss rate (blog §3.5): it is
+    either absent or below 0.01 %."""
+    N, C = 131072, 4
+    for log in (math.log, math.log2, math.log10):
+        for unit in (1.0, 1e-3, 1.0 / C):
+            def h(m):
+                T = m * N
+                return -1.059 * log(T * unit) + 1.145 * log(T / N) + 12.112
+            grid = [10 ** (-6 + 6 * i / 3000) for i in range(3001)]
+            switches = [grid[i] for i in range(1, len(grid))
+                        if (h(grid[i]) > 0) != (h(grid[i - 1]) > 0)]
+            assert all(s < 1e-4 for s in switches), (log, unit, switches)
+            assert not any(0.025 <= s <= 0.1 for s in switches)
