@@ -1082,8 +1082,11 @@ def run_profile_case(args):
                128K workload; its counter captures use llama8b_32k, a quarter
                of the 128K work per launch).
     restore:   the O restore of the default workload (268 MB each way).
-    decode:    the decode step of the merge sweep (one split-KV call over
-               the 8 ranks' KV caches, then the merge of the 8 partials)."""
+    decode:    the rank-partials decode step of the merge sweep (one split-KV
+               call over the 8 ranks' KV caches, then the merge of the 8
+               partials).
+    decode1:   the decode step as one split-KV call over the ranks' caches as
+               one segment (block partials merged in the call)."""
     import torch
 
     import context_causal_attention_cp_gb300 as cpa
@@ -1103,6 +1106,22 @@ def run_profile_case(args):
         ws = cpa.cp_attn_partial_kv(plan, q, k, v, w.scale, kv_block, status=status)[2]
         run = lambda: cpa.cp_attn_partial_kv(  # noqa: E731
             plan, q, k, v, w.scale, kv_block, workspace=ws, status=status)
+    elif args.profile_case == "decode1":
+        m = W.MERGE_SWEEP
+        inputs = W.make_merge_sweep_inputs()
+        S, nq, Hq, dv = m["shards"], m["queries"], m["Hq"], m["dv"]
+        q = inputs["q"].to(dev)
+        _, k_rank, v_rank, _ = decode_ranks(q, inputs["k"].to(dev), inputs["v"].to(dev), S)
+        n_kv = m["kv_tokens"] // S
+        seg_host = torch.tensor([[0, nq, S * n_kv - 1, 0, 0, S * n_kv, 0, 0]], dtype=torch.int32)
+        seg = seg_host.to(dev)
+        out = torch.empty(nq, Hq, dv, device=dev)
+        lse = torch.empty(nq, Hq, device=dev)
+        ws = cpa.cp_attn_split_kv(seg, q, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK,
+                                  segs_host=seg_host, out=out, lse_out=lse, status=status)[2]
+        run = lambda: cpa.cp_attn_split_kv(  # noqa: E731
+            seg, q, k_rank, v_rank, m["scale"], DECODE_KV_BLOCK, segs_host=seg_host, out=out,
+            lse_out=lse, workspace=ws, status=status)
     elif args.profile_case == "decode":
         m = W.MERGE_SWEEP
         inputs = W.make_merge_sweep_inputs()
@@ -1178,7 +1197,8 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-configs", action="store_true")
     ap.add_argument("--profile-case",
-                    choices=["attention", "merge", "merge4", "partial_kv", "restore", "decode"],
+                    choices=["attention", "merge", "merge4", "partial_kv", "restore", "decode",
+                             "decode1"],
                     default=None,
                     help="run one kernel on a small case (for ncu) instead of the bench")
     args = ap.parse_args()
