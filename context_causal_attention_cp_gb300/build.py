@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcpattn.so")
 SOURCES = ["plan.cu", "merge.cu", "attn.cu", "attn_mla.cu", "partial_kv.cu",
-           "partial_kv_noalloc.cu", "select.cu", "ring.cu", "pipeline.cu"]
+           "partial_kv_noalloc.cu", "select.cu", "ring.cu", "pipeline.cu", "attn_mla2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,638 @@
+// Shard partial attention, absorbed-MLA shape, on pairs of SMs (sm_103a).
+//
+// The same computation as attn_mla.cu (query and key rows are the 576-wide
+// absorbed latent, V = K[:, :512]; blog "什么是 Context Parallelism", §4.2)
+// with every MMA issued for two SMs at once (tcgen05 cta_group::2): a cluster
+// of two CTAs holds the same 128 query rows of two query heads (2h', 2h'+1;
+// all heads share the one latent KV head) for one 256-column output half, and
+// one thread of the even CTA issues M = 256 MMAs that read each CTA's own
+// operands.  Keys come in tiles of 128.
+//
+// Why pairs: one SM's tensor and shared memory cannot hold a 128-key S tile
+// next to the 576-wide query and the 256-column O half, and with 64-key tiles
+// the single issuing thread, not the tensor core, sets the pace (an N = 64
+// MMA executes in less time than it takes to issue).  A pair splits the key
+// tile of Q K^T (each CTA stores 64 of its 128 keys) and the value columns of
+// P V (each CTA stores 128 of the 256), so every MMA has N = 128 or 256.
+//
+// Per CTA:
+//   tensor memory (512 columns): S (128 x 128 fp32, single buffer), query
+//     chunks 5..8 (A operand of their Q K^T MMAs, packed bf16) and the O half.
+//   shared memory: query chunks 0..4, a 6-slot ring of K chunks (64 keys x 64
+//     columns), two buffers of this CTA's V columns (128 keys x 128 columns)
+//     and P (128 x 128 bf16, the A operand of P V).
+//   MMA order: Q K_j^T, then P_{j-1} V_{j-1}.  The softmax loads S_j into
+//     registers and releases it at once, so Q K_{j+1}^T overlaps the rest of
+//     the softmax; P_j is written to shared memory once P_{j-1} V_{j-1} is done
+//     (which also makes the rare O rescale safe).
+// Loads: each CTA's TMA copies land in its own shared memory and complete on
+// its own barriers; the odd CTA relays completions to the even CTA's barriers
+// with cluster-scope arrivals, so an aborted CTA drains its copies locally.
+// Every wait is bounded; a wait that runs out sets CPATTN_ERR_TIMEOUT and
+// aborts both CTAs of the pair, which drain, meet and free tensor memory.
+#include <algorithm>
+#include <cstdint>
+
+#include "attn_common.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int kD2 = 576, kDV2 = 512, kDVH2 = 256, kBN2 = 128, kCh2 = kD2 / 64;
+constexpr int kQS2 = 5;                 // query chunks 0..4 in shared memory
+constexpr int kQT2 = kCh2 - kQS2;       // chunks 5..8 in tensor memory
+constexpr int kThreads2 = 192;          // 4 softmax warps, producer warp, MMA / relay warp
+constexpr int kKSlots2 = 6;
+constexpr int kQChunk2 = BM * 128;      // 16 KB: 128 rows x 64 columns
+constexpr int kKChunk2 = 64 * 128;      // 8 KB: this CTA's 64 keys x 64 columns
+constexpr int kVChunk2 = kBN2 * 128;    // 16 KB: 128 keys x 64 columns
+constexpr int kPChunk2 = BM * 128;      // 16 KB: 128 rows x 64 keys
+constexpr int kQOff2 = 0;
+constexpr int kKOff2 = kQOff2 + kQS2 * kQChunk2;
+constexpr int kVOff2 = kKOff2 + kKSlots2 * kKChunk2;
+constexpr int kPOff2 = kVOff2 + 2 * 2 * kVChunk2;
+constexpr int kBarOff2 = kPOff2 + 2 * kPChunk2;
+// barriers ("pair" ones live in the even CTA and count both CTAs)
+constexpr int kBQ = 0;                    // pair: query chunks 0..4 of both CTAs
+constexpr int kBQT = 1;                   // pair: query chunks 5..8 in both CTAs' TMEM
+constexpr int kBKF = 2;                   // pair [6]: K chunk slot full in both CTAs
+constexpr int kBKE = kBKF + kKSlots2;     // local [6]: K slot free (multicast commit)
+constexpr int kBVF = kBKE + kKSlots2;     // pair [2]: V buffer full in both CTAs
+constexpr int kBVE = kBVF + 2;            // local [2]: V buffer free (multicast commit)
+constexpr int kBSF = kBVE + 2;            // local: S ready (multicast commit)
+constexpr int kBSR = kBSF + 1;            // pair: S read by both CTAs' softmax
+constexpr int kBPF = kBSR + 1;            // pair: P written in both CTAs
+constexpr int kBPR = kBPF + 1;            // local: P V done (P and O free), multicast
+constexpr int kBOF = kBPR + 1;            // local: last P V done, multicast
+constexpr int kBDR = kBOF + 1;            // even CTA: every MMA complete
+constexpr int kBLQ = kBDR + 1;            // odd CTA: own query loads
+constexpr int kBLK = kBLQ + 1;            // odd CTA [6]: own K chunk loads
+constexpr int kBLV = kBLK + kKSlots2;     // odd CTA [2]: own V loads
+constexpr int kNumBars2 = kBLV + 2;
+constexpr int kSmem2 = kBarOff2 + kNumBars2 * 8 + 32 + 1024;
+static_assert(kSmem2 <= 232448, "MLA pair tile exceeds shared memory");
+constexpr uint32_t kSCol2 = 0, kQtCol2 = 128, kOCol2 = 256;  // TMEM column map
+
+// ------------------------------------------------------- pair primitives --
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the same location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(local)), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void store_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (barriers that other CTAs or the
+// pair's MMAs arrive on).
+__device__ __forceinline__ bool wait_pair(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t timeout_ns) {
+  if (try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+  }
+}
+// Warp-uniform version (before warp-collective tcgen05.ld / st).
+__device__ __forceinline__ bool wait_pair_warp(uint64_t* bar, uint32_t parity,
+                                               const volatile int* abort, uint64_t timeout) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t t0 = lane == 0 ? global_timer_ns() : 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = try_wait_cluster(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 63u) == 63u) {
+      int give_up = 0;
+      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > timeout);
+      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the barrier at this offset in both CTAs once the MMAs issued so
+// far by this thread have completed.
+__device__ __forceinline__ void commit2_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The MMA issuer (one thread of the even CTA).
+__device__ __noinline__ void mla2_mma_issue(const AttnParams& p, uint8_t* smem, uint32_t tmem_base,
+                                            int n_kv, uint64_t* bars, volatile int* abort_flag,
+                                            uint32_t peer_abort) {
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(2 * BM, kBN2, 0, 0);
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(2 * BM, kDVH2, 0, 1);
+  const uint64_t dq0 = smem_desc_sw128(smem_u32(smem + kQOff2), 16, 1024);
+  const uint64_t dk0 = smem_desc_sw128(smem_u32(smem + kKOff2), 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(smem_u32(smem + kVOff2), kVChunk2, 1024);
+  const uint64_t dp0 = smem_desc_sw128(smem_u32(smem + kPOff2), 16, 1024);
+  const uint32_t s_tm = tmem_base + kSCol2, o_tm = tmem_base + kOCol2;
+  const uint32_t qt = tmem_base + kQtCol2;
+  auto pv = [&](int i, bool last) -> bool {
+    if (!wait_pair(bars + kBPF, i & 1, abort_flag, p.timeout_ns)) return false;
+    if (!wait_pair(bars + kBVF + (i & 1), (i >> 1) & 1, abort_flag, p.timeout_ns)) return false;
+    tc_fence_after();
+    const uint64_t vd = dv0 + (uint64_t)(((i & 1) * 2 * kVChunk2) >> 4);
+#pragma unroll
+    for (int kk = 0; kk < kBN2 / 16; ++kk)
+      mma2_ss(o_tm, dp0 + (uint64_t)((kk >> 2) * (kPChunk2 >> 4) + (kk & 3) * 2),
+              vd + (uint64_t)(kk * ((16 * 128) >> 4)), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+    commit2_both(bars + kBVE + (i & 1));
+    commit2_both(bars + (last ? kBOF : kBPR));
+    return true;
+  };
+  bool ok = wait_pair(bars + kBQ, 0, abort_flag, p.timeout_ns);
+  if (ok) ok = wait_pair(bars + kBQT, 0, abort_flag, p.timeout_ns);
+  int g = 0;  // K chunks consumed
+  for (int j = 0; j < n_kv && ok; ++j) {
+    if (j > 0) {
+      ok = wait_pair(bars + kBSR, (j - 1) & 1, abort_flag, p.timeout_ns);  // S_{j-1} read
+      if (!ok) break;
+    }
+#pragma unroll
+    for (int c = 0; c < kCh2; ++c, ++g) {
+      const int slot = g % kKSlots2;
+      ok = wait_pair(bars + kBKF + slot, (g / kKSlots2) & 1, abort_flag, p.timeout_ns);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t kd = dk0 + (uint64_t)((slot * kKChunk2) >> 4);
+      if (c < kQS2) {
+        const uint64_t qd = dq0 + (uint64_t)((c * kQChunk2) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma2_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (c == 0 && kk == 0) ? 0u : 1u);
+      } else {
+        const uint32_t qa = qt + (c - kQS2) * 32;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma2_ts(s_tm, qa + kk * 8, kd + kk * 2, kIdescQK, 1u);
+      }
+      commit2_both(bars + kBKE + slot);
+    }
+    if (!ok) break;
+    commit2_both(bars + kBSF);
+    if (j > 0) ok = pv(j - 1, false);
+  }
+  if (ok && n_kv > 0) ok = pv(n_kv - 1, true);
+  if (!ok) {
+    set_status(p.status, CPATTN_ERR_TIMEOUT);
+    *abort_flag = 1;
+    store_cluster_u32(peer_abort, 1);
+  }
+  // drain: every MMA issued by this thread has completed
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bars + kBDR))
+               : "memory");
+  mbar_wait(bars + kBDR, 0, nullptr, p.timeout_ns);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
+attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* issued = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0]: K, [1]: V, [2]: Q
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t peer_abort = peer_addr((const void*)abort_flag, peer);
+
+  // ---- work item: (128-row tile [, KV block], head pair, output half); CTA
+  // `rank` of the pair takes head 2 * pair_head + rank ----
+  const int pair_id = blockIdx.x >> 1;
+  const int half = pair_id & 1;
+  const int n_hp = p.Hq >> 1;
+  const int hp = (pair_id >> 1) % n_hp;
+  const int rest = (pair_id >> 1) / n_hp;
+  const int h = 2 * hp + (int)rank;
+  const int jblk = p.split_block > 0 ? rest % p.max_blocks : 0;
+  const int tile_idx = p.split_block > 0 ? rest / p.max_blocks : rest;
+  cp_segment_t sg;
+  int t, seg_id, kv_lo, kv_hi;
+  long long out_row0;
+  // both CTAs of a pair resolve the same tile and window, so they leave together
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
+  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
+  const int r0 = t * BM;
+  const int rows_valid = min(BM, sg.q_len - r0);
+  const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
+  const int win_lo = max(kv_lo, 0);
+  const int win_hi_tile = kv_hi < 0 ? pos_max + 1 : min(kv_hi, pos_max + 1);
+  const int j0 = win_lo / kBN2;
+  const int n_kv = win_hi_tile > win_lo ? (win_hi_tile + kBN2 - 1) / kBN2 - j0 : 0;
+  const int kv_head = h / p.g;  // both heads share it (the latent head)
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars + kBQ, 1 + (rank == 0 ? 1 : 0));
+    mbar_init(bars + kBQT, 8);
+    for (int s = 0; s < kKSlots2; ++s) {
+      mbar_init(bars + kBKF + s, 2);
+      mbar_init(bars + kBKE + s, 1);
+      mbar_init(bars + kBLK + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars + kBVF + b, 2);
+      mbar_init(bars + kBVE + b, 1);
+      mbar_init(bars + kBLV + b, 1);
+    }
+    mbar_init(bars + kBSF, 1);
+    mbar_init(bars + kBSR, 8);
+    mbar_init(bars + kBPF, 8);
+    mbar_init(bars + kBPR, 1);
+    mbar_init(bars + kBOF, 1);
+    mbar_init(bars + kBDR, 1);
+    mbar_init(bars + kBLQ, 1);
+    *abort_flag = 0;
+    issued[0] = issued[1] = issued[2] = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // barriers and tensor memory of both CTAs are ready
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t to = p.timeout_ns;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0 && n_kv > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      // rank 0's loads complete on the pair barriers directly; rank 1's on its
+      // own barriers, which its relay thread forwards
+      uint64_t* fq = rank == 0 ? bars + kBQ : bars + kBLQ;
+      if (!p.withhold_q) {
+        mbar_arrive_expect_tx(fq, kQS2 * kQChunk2);
+        for (int c = 0; c < kQS2; ++c)
+          tma_load_3d(smem + kQOff2 + c * kQChunk2, &tm_q, fq, c * 64, h, sg.q_row0 + r0);
+        issued[2] = 1;
+      }
+      bool ok = true;
+      int g = 0, nv = 0;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int kv_row = sg.kv_row0 + (j0 + j) * kBN2;
+        for (int c = 0; c < kCh2; ++c, ++g) {
+          const int slot = g % kKSlots2;
+          ok = wait_pair(bars + kBKE + slot, ((g / kKSlots2) & 1) ^ 1, abort_flag, to);
+          if (!ok) break;
+          uint64_t* fb = rank == 0 ? bars + kBKF + slot : bars + kBLK + slot;
+          mbar_arrive_expect_tx(fb, kKChunk2);
+          tma_load_3d(smem + kKOff2 + slot * kKChunk2, &tm_k, fb, c * 64, kv_head,
+                      kv_row + 64 * (int)rank);
+          issued[0] = g + 1;
+        }
+        if (!ok) break;
+        const int b = j & 1;
+        ok = wait_pair(bars + kBVE + b, ((j >> 1) & 1) ^ 1, abort_flag, to);
+        if (!ok) break;
+        uint64_t* fv = rank == 0 ? bars + kBVF + b : bars + kBLV + b;
+        mbar_arrive_expect_tx(fv, 2 * kVChunk2);
+        for (int t2 = 0; t2 < 2; ++t2)
+          tma_load_3d(smem + kVOff2 + (b * 2 + t2) * kVChunk2, &tm_v, fv,
+                      (4 * half + 2 * (int)rank + t2) * 64, kv_head, kv_row);
+        issued[1] = ++nv;
+      }
+      if (!ok) {
+        set_status(p.status, CPATTN_ERR_TIMEOUT);
+        *abort_flag = 1;
+        store_cluster_u32(peer_abort, 1);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0 && n_kv > 0) {
+      if (rank == 0) {
+        // -------------------------------------------------------- MMA issuer --
+        mla2_mma_issue(p, smem, tmem_base, n_kv, bars, abort_flag, peer_abort);
+      } else {
+        // --------------------------------------------- relay (odd CTA only) --
+        // forward the completion of this CTA's loads to the even CTA's pair
+        // barriers, in the producer's order
+        bool ok = true;
+        if (!p.withhold_q) {
+          ok = wait_pair(bars + kBLQ, 0, abort_flag, to);
+          if (ok) arrive_cluster(peer_addr(bars + kBQ, 0));
+        }
+        int g = 0;
+        for (int j = 0; j < n_kv && ok; ++j) {
+          for (int c = 0; c < kCh2; ++c, ++g) {
+            const int slot = g % kKSlots2;
+            ok = wait_pair(bars + kBLK + slot, (g / kKSlots2) & 1, abort_flag, to);
+            if (!ok) break;
+            arrive_cluster(peer_addr(bars + kBKF + slot, 0));
+          }
+          if (!ok) break;
+          const int b = j & 1;
+          ok = wait_pair(bars + kBLV + b, (j >> 1) & 1, abort_flag, to);
+          if (!ok) break;
+          arrive_cluster(peer_addr(bars + kBVF + b, 0));
+        }
+        if (!ok) {
+          set_status(p.status, CPATTN_ERR_TIMEOUT);
+          *abort_flag = 1;
+          store_cluster_u32(peer_abort, 1);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax --
+    const int row = warp * 32 + lane;
+    const bool valid = row < rows_valid;
+    const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
+    const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const uint32_t bar_sr = peer_addr(bars + kBSR, 0), bar_pf = peer_addr(bars + kBPF, 0);
+    uint8_t* prow = smem + kPOff2 + row * 128;
+    float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
+    bool ok = true;
+    if (n_kv > 0) {
+      // query chunks 5..8 of this row into tensor memory (A-operand layout)
+      const long long qrow = (long long)sg.q_row0 + r0 + row;
+      const bool in_q = qrow < p.num_q_rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + (in_q ? qrow * p.Hq + h : 0) * kD2);
+#pragma unroll
+      for (int c = 0; c < kQT2; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w = in_q ? __ldg(src + (kQS2 + c) * 8 + v) : make_uint4(0, 0, 0, 0);
+          r[4 * v] = w.x;
+          r[4 * v + 1] = w.y;
+          r[4 * v + 2] = w.z;
+          r[4 * v + 3] = w.w;
+        }
+        tmem_st32(lane_addr + kQtCol2 + c * 32, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_cluster(peer_addr(bars + kBQT, 0));
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      ok = wait_pair_warp(bars + kBSF, j & 1, abort_flag, to);
+      if (!ok) break;
+      tc_fence_after();
+      float x[kBN2];
+      {
+        uint32_t r[kBN2];
+#pragma unroll
+        for (int q = 0; q < kBN2 / 32; ++q) tmem_ld32p(lane_addr + kSCol2 + q * 32, r + q * 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < kBN2; ++c) x[c] = __uint_as_float(r[c]);
+      }
+      // S is in registers: the next Q K^T may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_cluster(bar_sr);
+      const int key0 = (j0 + j) * kBN2;
+      if (key0 < win_lo || key0 + kBN2 > row_hi) {
+#pragma unroll
+        for (int c = 0; c < kBN2; ++c) {
+          const int key = key0 + c;
+          if (key < win_lo || key >= row_hi) x[c] = -INFINITY;
+        }
+      }
+      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+      for (int c = 4; c < kBN2; c += 8) {
+        mx0 = fmax3(mx0, x[c], x[c + 1]);
+        mx1 = fmax3(mx1, x[c + 2], x[c + 3]);
+        mx2 = fmax3(mx2, x[c + 4], x[c + 5]);
+        mx3 = fmax3(mx3, x[c + 6], x[c + 7]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool move = mx > m_run + kMaxSlack;
+      const float m_new = move ? mx : m_run;
+      const float m_new_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = move ? ex2_approx(m_run - m_new_use) : 1.f;
+      uint32_t pk[kBN2 / 2];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN2; c += 2) {
+        float a, bb;
+        ffma2(a, bb, x[c], x[c + 1], sl2, sl2, -m_new_use, -m_new_use);
+        a = ex2_approx(a);
+        bb = ex2_approx(bb);
+        fadd2(sum0, sum1, sum0, sum1, a, bb);
+        pk[c >> 1] = pack_bf16x2(a, bb);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      // P V of the previous tile must be done before P is overwritten and
+      // before O is rescaled
+      if (j > 0) {
+        ok = wait_pair_warp(bars + kBPR, (j - 1) & 1, abort_flag, to);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const bool need = (j > 0) && move;
+      if (__any_sync(0xffffffffu, need)) {
+        const float a = need ? alpha : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < kDVH2 / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32p(lane_addr + kOCol2 + q * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * a);
+          tmem_st32(lane_addr + kOCol2 + q * 32, r);
+        }
+        tmem_wait_st();
+      }
+      // P row into shared memory as the K-major, 128-byte-swizzled A operand:
+      // two 64-key chunks of 128-byte rows, 16-byte pieces XOR-ed by row % 8
+#pragma unroll
+      for (int piece = 0; piece < kBN2 / 8; ++piece) {
+        const int chunk = piece >> 3, pc = piece & 7;
+        *reinterpret_cast<uint4*>(prow + chunk * kPChunk2 + ((pc ^ (row & 7)) * 16)) =
+            make_uint4(pk[4 * piece], pk[4 * piece + 1], pk[4 * piece + 2], pk[4 * piece + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_cluster(bar_pf);
+      m_run = m_new;
+      m_use = m_new_use;
+    }
+    if (ok && n_kv > 0) ok = wait_pair_warp(bars + kBOF, 0, abort_flag, to);
+    if (!ok) {
+      if (lane == 0) {
+        set_status(p.status, CPATTN_ERR_TIMEOUT);
+        *abort_flag = 1;
+        store_cluster_u32(peer_abort, 1);
+      }
+    } else {
+      tc_fence_after();
+      const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
+      const bool has = l_run > 0.f;
+      const float inv = has ? 1.f / l_run : 0.f;
+      const bool acc_mode = p.lse_acc != nullptr;
+      MergeCoef mc{0.f, inv, has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY};
+      if (acc_mode && out_row >= 0)
+        mc = merge_coef(__ldg(p.lse_acc + out_row * p.Hq + h), has, m_use, l_run);
+#pragma unroll 1
+      for (int q = 0; q < kDVH2 / 32; ++q) {
+        uint32_t r[32];
+        if (n_kv > 0) {
+          tmem_ld32p(lane_addr + kOCol2 + q * 32, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = 0u;
+        }
+        if (out_row >= 0) {
+          const long long off = (out_row * p.Hq + h) * kDV2 + half * kDVH2 + q * 32;
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]) * mc.c_new;
+          if (p.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o) + off);
+            if (acc_mode) {
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const float4 a = dst[c];
+                v[4 * c] += mc.c_old * a.x;
+                v[4 * c + 1] += mc.c_old * a.y;
+                v[4 * c + 2] += mc.c_old * a.z;
+                v[4 * c + 3] += mc.c_old * a.w;
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + off);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                  pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                  pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                  pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+          }
+        }
+      }
+      // both halves read lse_acc; only half 0 writes the LSE
+      if (out_row >= 0 && half == 0) p.lse[out_row * p.Hq + h] = mc.lse;
+    }
+  }
+
+  // ---- teardown: drain own copies after an abort, meet, free TMEM ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4 && lane == 0 && *abort_flag && n_kv > 0) {
+    // let this CTA's own TMA copies land before its shared memory is released
+    // (rank 0's copies complete on the pair barriers, rank 1's on its own)
+    if (issued[2]) mbar_wait(bars + (rank == 0 ? kBQ : kBLQ), 0, nullptr, to);
+    const int nk = issued[0], nv = issued[1];
+    for (int g = max(0, nk - kKSlots2); g < nk; ++g) {
+      const int slot = g % kKSlots2;
+      // the pair barrier of rank 0 also waits for the peer's relay; its own
+      // bytes are what matters here, so a bounded wait that may run out is fine
+      mbar_wait(bars + (rank == 0 ? kBKF : kBLK) + slot, (g / kKSlots2) & 1, nullptr, to);
+    }
+    for (int j = max(0, nv - 2); j < nv; ++j)
+      mbar_wait(bars + (rank == 0 ? kBVF : kBLV) + (j & 1), (j >> 1) & 1, nullptr, to);
+  }
+  __syncthreads();
+  cluster_sync_all();  // neither CTA frees memory the other's MMAs or arrivals still use
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+// Launch the pair kernel for the absorbed-MLA shape (Hq even).  Same contract
+// as launch_attn_mla.
+int launch_attn_mla_pair(const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
+                         int64_t k_head_stride, int num_kv_rows, int Hkv, AttnParams prm,
+                         long long tiles, cudaStream_t stream) {
+  if (prm.Hq % 2 != 0) return CPATTN_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, kD2, prm.Hq, num_q_rows, kD2, (long long)prm.Hq * kD2) ||
+      !make_map(&mk, k, kD2, Hkv, num_kv_rows, k_head_stride, k_row_stride, 64) ||
+      !make_map(&mv, k, kD2, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBN2))
+    return CPATTN_ERR_CUDA;
+  prm.q = q;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(attn_mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem2) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    configured = true;
+  }
+  // tiles x KV blocks (split mode) x head pairs x halves x 2 CTAs
+  const long long grid = tiles * (prm.Hq / 2) * 2 * 2;
+  if (grid <= 0) return CPATTN_OK;
+  if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
+  attn_mla_pair_kernel<<<(unsigned)grid, kThreads2, kSmem2, stream>>>(mq, mk, mv, prm);
+  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+}  // namespace cpattn
