@@ -130,6 +130,9 @@ def job_throughput(flops_per_rank, world, steps, max_total_ms):
 
 def kernel_label(w):
     if w.d == 576:
+        if w.Hq % 2 == 0:
+            return ("attn_mla_pair_kernel (tcgen05 cta_group::2; a pair of SMs per 128 rows x "
+                    "2 heads x one 256-column output half)")
         return "attn_mla_kernel (tcgen05; 128 rows x 1 head x one 256-column output half per CTA)"
     nq = 2 if (w.Hq // w.Hkv) % 2 == 0 else 1
     return f"attn_fwd_kernel<d={w.d}> (tcgen05; {nq} head(s) x 128 rows per CTA)"

@@ -7,6 +7,10 @@
 // cp_attn_partial: causal / windowed softmax attention per query row giving O
 // and its log-sum-exp.
 //
+// This single-SM kernel serves an odd number of query heads; with an even
+// number the pair kernel of attn_mla2.cu runs instead (MMAs issued for two
+// SMs at once over 128-key tiles).
+//
 // Tensor memory holds 512 fp32 columns per SM, exactly a 128 x 512 output,
 // so the output is split in two 256-column halves computed by sibling CTAs
 // that each recompute S = Q K^T.  One CTA: 128 query rows of one head, one
@@ -487,9 +491,17 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 }  // namespace
 
+// The pair kernel (attn_mla2.cu) for an even number of query heads.
+int launch_attn_mla_pair(const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
+                         int64_t k_head_stride, int num_kv_rows, int Hkv, AttnParams prm,
+                         long long tiles, cudaStream_t stream);
+
 int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_stride,
                     int64_t k_head_stride, int num_kv_rows, int Hkv, AttnParams prm,
                     long long tiles, cudaStream_t stream) {
+  if (prm.Hq % 2 == 0)
+    return launch_attn_mla_pair(q, num_q_rows, k, k_row_stride, k_head_stride, num_kv_rows, Hkv,
+                                prm, tiles, stream);
   CUtensorMap mq, mk;
   if (!make_map(&mq, q, kD, prm.Hq, num_q_rows, kD, (long long)prm.Hq * kD) ||
       !make_map(&mk, k, kD, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBNm))

@@ -18,154 +18,64 @@
 // Per CTA:
 //   tensor memory (512 columns): S (128 x 128 fp32, single buffer), query
 //     chunks 5..8 (A operand of their Q K^T MMAs, packed bf16) and the O half.
-//   shared memory: query chunks 0..4, a 6-slot ring of K chunks (64 keys x 64
-//     columns), two buffers of this CTA's V columns (128 keys x 128 columns)
-//     and P (128 x 128 bf16, the A operand of P V).
+//   shared memory: query chunks 0..4, a ring of three slots of three K chunks
+//     (64 keys x 64 columns each; one tile of look-ahead, one barrier per three
+//     chunks), one buffer of this CTA's V columns (128 keys x 128 columns; V_j
+//     has the whole of Q K_{j+1}^T to land) and P (128 x 128 bf16, the A
+//     operand of P V).
 //   MMA order: Q K_j^T, then P_{j-1} V_{j-1}.  The softmax loads S_j into
 //     registers and releases it at once, so Q K_{j+1}^T overlaps the rest of
 //     the softmax; P_j is written to shared memory once P_{j-1} V_{j-1} is done
 //     (which also makes the rare O rescale safe).
 // Loads: each CTA's TMA copies land in its own shared memory and complete on
-// its own barriers; the odd CTA relays completions to the even CTA's barriers
-// with cluster-scope arrivals, so an aborted CTA drains its copies locally.
+// the even CTA's barriers (the .cta_group::2 form of the copy), which the even
+// CTA's producer arms with both CTAs' bytes.
 // Every wait is bounded; a wait that runs out sets CPATTN_ERR_TIMEOUT and
-// aborts both CTAs of the pair, which drain, meet and free tensor memory.
+// aborts both CTAs of the pair, which let their copies land, meet and free
+// tensor memory.
 #include <algorithm>
 #include <cstdint>
 
 #include "attn_common.cuh"
+#include "pair.cuh"
 
 namespace cpattn {
 namespace {
+
+using namespace pair;
 
 constexpr int kD2 = 576, kDV2 = 512, kDVH2 = 256, kBN2 = 128, kCh2 = kD2 / 64;
 constexpr int kQS2 = 5;                 // query chunks 0..4 in shared memory
 constexpr int kQT2 = kCh2 - kQS2;       // chunks 5..8 in tensor memory
 constexpr int kThreads2 = 192;          // 4 softmax warps, producer warp, MMA / relay warp
-constexpr int kKSlots2 = 6;
+constexpr int kKSlots2 = 3;            // slots of kKGroup chunks
+constexpr int kKGroup = 3;
 constexpr int kQChunk2 = BM * 128;      // 16 KB: 128 rows x 64 columns
 constexpr int kKChunk2 = 64 * 128;      // 8 KB: this CTA's 64 keys x 64 columns
 constexpr int kVChunk2 = kBN2 * 128;    // 16 KB: 128 keys x 64 columns
 constexpr int kPChunk2 = BM * 128;      // 16 KB: 128 rows x 64 keys
 constexpr int kQOff2 = 0;
 constexpr int kKOff2 = kQOff2 + kQS2 * kQChunk2;
-constexpr int kVOff2 = kKOff2 + kKSlots2 * kKChunk2;
-constexpr int kPOff2 = kVOff2 + 2 * 2 * kVChunk2;
+constexpr int kVOff2 = kKOff2 + kKSlots2 * kKGroup * kKChunk2;
+constexpr int kPOff2 = kVOff2 + 2 * kVChunk2;
 constexpr int kBarOff2 = kPOff2 + 2 * kPChunk2;
-// barriers ("pair" ones live in the even CTA and count both CTAs)
+// barriers ("pair" ones are used in the even CTA and count both CTAs)
 constexpr int kBQ = 0;                    // pair: query chunks 0..4 of both CTAs
 constexpr int kBQT = 1;                   // pair: query chunks 5..8 in both CTAs' TMEM
-constexpr int kBKF = 2;                   // pair [6]: K chunk slot full in both CTAs
-constexpr int kBKE = kBKF + kKSlots2;     // local [6]: K slot free (multicast commit)
-constexpr int kBVF = kBKE + kKSlots2;     // pair [2]: V buffer full in both CTAs
-constexpr int kBVE = kBVF + 2;            // local [2]: V buffer free (multicast commit)
-constexpr int kBSF = kBVE + 2;            // local: S ready (multicast commit)
+constexpr int kBKF = 2;                   // pair [3]: K slot full in both CTAs
+constexpr int kBKE = kBKF + kKSlots2;     // local [3]: K slot free (multicast commit)
+constexpr int kBVF = kBKE + kKSlots2;     // pair: V buffer full in both CTAs
+constexpr int kBVE = kBVF + 1;            // local: V buffer free (multicast commit)
+constexpr int kBSF = kBVE + 1;            // local: S ready (multicast commit)
 constexpr int kBSR = kBSF + 1;            // pair: S read by both CTAs' softmax
 constexpr int kBPF = kBSR + 1;            // pair: P written in both CTAs
 constexpr int kBPR = kBPF + 1;            // local: P V done (P and O free), multicast
 constexpr int kBOF = kBPR + 1;            // local: last P V done, multicast
 constexpr int kBDR = kBOF + 1;            // even CTA: every MMA complete
-constexpr int kBLQ = kBDR + 1;            // odd CTA: own query loads
-constexpr int kBLK = kBLQ + 1;            // odd CTA [6]: own K chunk loads
-constexpr int kBLV = kBLK + kKSlots2;     // odd CTA [2]: own V loads
-constexpr int kNumBars2 = kBLV + 2;
+constexpr int kNumBars2 = kBDR + 1;
 constexpr int kSmem2 = kBarOff2 + kNumBars2 * 8 + 32 + 1024;
 static_assert(kSmem2 <= 232448, "MLA pair tile exceeds shared memory");
 constexpr uint32_t kSCol2 = 0, kQtCol2 = 128, kOCol2 = 256;  // TMEM column map
-
-// ------------------------------------------------------- pair primitives --
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Shared::cluster address of the same location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
-  uint32_t d;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(local)), "r"(rank));
-  return d;
-}
-__device__ __forceinline__ void arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ void store_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait with cluster-scope acquire (barriers that other CTAs or the
-// pair's MMAs arrive on).
-__device__ __forceinline__ bool wait_pair(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                          uint64_t timeout_ns) {
-  if (try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (try_wait_cluster(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) return false;
-    }
-  }
-}
-// Warp-uniform version (before warp-collective tcgen05.ld / st).
-__device__ __forceinline__ bool wait_pair_warp(uint64_t* bar, uint32_t parity,
-                                               const volatile int* abort, uint64_t timeout) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t t0 = lane == 0 ? global_timer_ns() : 0;
-  for (uint32_t i = 0;; ++i) {
-    const bool ok = try_wait_cluster(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((i & 63u) == 63u) {
-      int give_up = 0;
-      if (lane == 0) give_up = (*abort != 0) || (global_timer_ns() - t0 > timeout);
-      if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-    }
-  }
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on the barrier at this offset in both CTAs once the MMAs issued so
-// far by this thread have completed.
-__device__ __forceinline__ void commit2_both(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"((uint16_t)3)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // The MMA issuer (one thread of the even CTA).
 __device__ __noinline__ void mla2_mma_issue(const AttnParams& p, uint8_t* smem, uint32_t tmem_base,
@@ -181,41 +91,45 @@ __device__ __noinline__ void mla2_mma_issue(const AttnParams& p, uint8_t* smem, 
   const uint32_t qt = tmem_base + kQtCol2;
   auto pv = [&](int i, bool last) -> bool {
     if (!wait_pair(bars + kBPF, i & 1, abort_flag, p.timeout_ns)) return false;
-    if (!wait_pair(bars + kBVF + (i & 1), (i >> 1) & 1, abort_flag, p.timeout_ns)) return false;
+    if (!mbar_wait(bars + kBVF, i & 1, abort_flag, p.timeout_ns)) return false;
     tc_fence_after();
-    const uint64_t vd = dv0 + (uint64_t)(((i & 1) * 2 * kVChunk2) >> 4);
+    const uint64_t vd = dv0;
 #pragma unroll
     for (int kk = 0; kk < kBN2 / 16; ++kk)
       mma2_ss(o_tm, dp0 + (uint64_t)((kk >> 2) * (kPChunk2 >> 4) + (kk & 3) * 2),
               vd + (uint64_t)(kk * ((16 * 128) >> 4)), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-    commit2_both(bars + kBVE + (i & 1));
+    commit2_both(bars + kBVE);
     commit2_both(bars + (last ? kBOF : kBPR));
     return true;
   };
-  bool ok = wait_pair(bars + kBQ, 0, abort_flag, p.timeout_ns);
+  bool ok = mbar_wait(bars + kBQ, 0, abort_flag, p.timeout_ns);
   if (ok) ok = wait_pair(bars + kBQT, 0, abort_flag, p.timeout_ns);
-  int g = 0;  // K chunks consumed
+  int g = 0;  // K chunk groups consumed
   for (int j = 0; j < n_kv && ok; ++j) {
     if (j > 0) {
       ok = wait_pair(bars + kBSR, (j - 1) & 1, abort_flag, p.timeout_ns);  // S_{j-1} read
       if (!ok) break;
     }
 #pragma unroll
-    for (int c = 0; c < kCh2; ++c, ++g) {
+    for (int grp = 0; grp < kCh2 / kKGroup; ++grp, ++g) {
       const int slot = g % kKSlots2;
-      ok = wait_pair(bars + kBKF + slot, (g / kKSlots2) & 1, abort_flag, p.timeout_ns);
+      ok = mbar_wait(bars + kBKF + slot, (g / kKSlots2) & 1, abort_flag, p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t kd = dk0 + (uint64_t)((slot * kKChunk2) >> 4);
-      if (c < kQS2) {
-        const uint64_t qd = dq0 + (uint64_t)((c * kQChunk2) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma2_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (c == 0 && kk == 0) ? 0u : 1u);
-      } else {
-        const uint32_t qa = qt + (c - kQS2) * 32;
+      for (int cc = 0; cc < kKGroup; ++cc) {
+        const int c = grp * kKGroup + cc;
+        const uint64_t kd = dk0 + (uint64_t)(((slot * kKGroup + cc) * kKChunk2) >> 4);
+        if (c < kQS2) {
+          const uint64_t qd = dq0 + (uint64_t)((c * kQChunk2) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma2_ts(s_tm, qa + kk * 8, kd + kk * 2, kIdescQK, 1u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma2_ss(s_tm, qd + kk * 2, kd + kk * 2, kIdescQK, (c == 0 && kk == 0) ? 0u : 1u);
+        } else {
+          const uint32_t qa = qt + (c - kQS2) * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma2_ts(s_tm, qa + kk * 8, kd + kk * 2, kIdescQK, 1u);
+        }
       }
       commit2_both(bars + kBKE + slot);
     }
@@ -246,7 +160,6 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* issued = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [0]: K, [1]: V, [2]: Q
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const uint32_t peer = rank ^ 1u;
@@ -278,27 +191,21 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int kv_head = h / p.g;  // both heads share it (the latent head)
 
   if (threadIdx.x == 0) {
-    mbar_init(bars + kBQ, 1 + (rank == 0 ? 1 : 0));
+    mbar_init(bars + kBQ, 1);
     mbar_init(bars + kBQT, 8);
-    for (int s = 0; s < kKSlots2; ++s) {
-      mbar_init(bars + kBKF + s, 2);
-      mbar_init(bars + kBKE + s, 1);
-      mbar_init(bars + kBLK + s, 1);
+    for (int sl = 0; sl < kKSlots2; ++sl) {
+      mbar_init(bars + kBKF + sl, 1);
+      mbar_init(bars + kBKE + sl, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + kBVF + b, 2);
-      mbar_init(bars + kBVE + b, 1);
-      mbar_init(bars + kBLV + b, 1);
-    }
+    mbar_init(bars + kBVF, 1);
+    mbar_init(bars + kBVE, 1);
     mbar_init(bars + kBSF, 1);
     mbar_init(bars + kBSR, 8);
     mbar_init(bars + kBPF, 8);
     mbar_init(bars + kBPR, 1);
     mbar_init(bars + kBOF, 1);
     mbar_init(bars + kBDR, 1);
-    mbar_init(bars + kBLQ, 1);
     *abort_flag = 0;
-    issued[0] = issued[1] = issued[2] = 0;
     fence_barrier_init();
   }
   if (warp == 4) {
@@ -317,43 +224,49 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer --
+    // Every copy lands in this CTA's shared memory and completes on the even
+    // CTA's barrier, which the even CTA's producer arms with both CTAs' bytes.
+    // K chunk group g (three chunks) goes to slot g % 3 once the MMAs have
+    // released it; V_j is loaded after the K chunks of tile j+1 so that the K
+    // look-ahead never waits for P_{j-1} V_{j-1}.
     if (lane == 0 && n_kv > 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      // rank 0's loads complete on the pair barriers directly; rank 1's on its
-      // own barriers, which its relay thread forwards
-      uint64_t* fq = rank == 0 ? bars + kBQ : bars + kBLQ;
+      const bool lead = rank == 0;
       if (!p.withhold_q) {
-        mbar_arrive_expect_tx(fq, kQS2 * kQChunk2);
+        if (lead) mbar_arrive_expect_tx(bars + kBQ, 2 * kQS2 * kQChunk2);
+        const uint32_t fq = peer_addr(bars + kBQ, 0);
         for (int c = 0; c < kQS2; ++c)
-          tma_load_3d(smem + kQOff2 + c * kQChunk2, &tm_q, fq, c * 64, h, sg.q_row0 + r0);
-        issued[2] = 1;
+          tma_load_pair(smem + kQOff2 + c * kQChunk2, &tm_q, fq, c * 64, h, sg.q_row0 + r0);
       }
       bool ok = true;
-      int g = 0, nv = 0;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int kv_row = sg.kv_row0 + (j0 + j) * kBN2;
-        for (int c = 0; c < kCh2; ++c, ++g) {
-          const int slot = g % kKSlots2;
-          ok = wait_pair(bars + kBKE + slot, ((g / kKSlots2) & 1) ^ 1, abort_flag, to);
+      int g = 0;
+      for (int j = 0; j <= n_kv && ok; ++j) {
+        if (j < n_kv) {
+          const int kv_row = sg.kv_row0 + (j0 + j) * kBN2;
+          for (int grp = 0; grp < kCh2 / kKGroup; ++grp, ++g) {
+            const int slot = g % kKSlots2;
+            ok = mbar_wait(bars + kBKE + slot, ((g / kKSlots2) & 1) ^ 1, abort_flag, to);
+            if (!ok) break;
+            if (lead) mbar_arrive_expect_tx(bars + kBKF + slot, 2 * kKGroup * kKChunk2);
+            for (int cc = 0; cc < kKGroup; ++cc)
+              tma_load_pair(smem + kKOff2 + (slot * kKGroup + cc) * kKChunk2, &tm_k,
+                            peer_addr(bars + kBKF + slot, 0), (grp * kKGroup + cc) * 64, kv_head,
+                            kv_row + 64 * (int)rank);
+          }
           if (!ok) break;
-          uint64_t* fb = rank == 0 ? bars + kBKF + slot : bars + kBLK + slot;
-          mbar_arrive_expect_tx(fb, kKChunk2);
-          tma_load_3d(smem + kKOff2 + slot * kKChunk2, &tm_k, fb, c * 64, kv_head,
-                      kv_row + 64 * (int)rank);
-          issued[0] = g + 1;
         }
-        if (!ok) break;
-        const int b = j & 1;
-        ok = wait_pair(bars + kBVE + b, ((j >> 1) & 1) ^ 1, abort_flag, to);
-        if (!ok) break;
-        uint64_t* fv = rank == 0 ? bars + kBVF + b : bars + kBLV + b;
-        mbar_arrive_expect_tx(fv, 2 * kVChunk2);
-        for (int t2 = 0; t2 < 2; ++t2)
-          tma_load_3d(smem + kVOff2 + (b * 2 + t2) * kVChunk2, &tm_v, fv,
-                      (4 * half + 2 * (int)rank + t2) * 64, kv_head, kv_row);
-        issued[1] = ++nv;
+        if (j >= 1) {
+          const int jv = j - 1;  // V of tile jv, once P_{jv-1} V_{jv-1} is done
+          ok = mbar_wait(bars + kBVE, (jv & 1) ^ 1, abort_flag, to);
+          if (!ok) break;
+          if (lead) mbar_arrive_expect_tx(bars + kBVF, 2 * 2 * kVChunk2);
+          const int kv_row = sg.kv_row0 + (j0 + jv) * kBN2;
+          for (int t2 = 0; t2 < 2; ++t2)
+            tma_load_pair(smem + kVOff2 + t2 * kVChunk2, &tm_v, peer_addr(bars + kBVF, 0),
+                          (4 * half + 2 * (int)rank + t2) * 64, kv_head, kv_row);
+        }
       }
       if (!ok) {
         set_status(p.status, CPATTN_ERR_TIMEOUT);
@@ -362,40 +275,9 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
   } else if (warp == 5) {
-    if (lane == 0 && n_kv > 0) {
-      if (rank == 0) {
-        // -------------------------------------------------------- MMA issuer --
-        mla2_mma_issue(p, smem, tmem_base, n_kv, bars, abort_flag, peer_abort);
-      } else {
-        // --------------------------------------------- relay (odd CTA only) --
-        // forward the completion of this CTA's loads to the even CTA's pair
-        // barriers, in the producer's order
-        bool ok = true;
-        if (!p.withhold_q) {
-          ok = wait_pair(bars + kBLQ, 0, abort_flag, to);
-          if (ok) arrive_cluster(peer_addr(bars + kBQ, 0));
-        }
-        int g = 0;
-        for (int j = 0; j < n_kv && ok; ++j) {
-          for (int c = 0; c < kCh2; ++c, ++g) {
-            const int slot = g % kKSlots2;
-            ok = wait_pair(bars + kBLK + slot, (g / kKSlots2) & 1, abort_flag, to);
-            if (!ok) break;
-            arrive_cluster(peer_addr(bars + kBKF + slot, 0));
-          }
-          if (!ok) break;
-          const int b = j & 1;
-          ok = wait_pair(bars + kBLV + b, (j >> 1) & 1, abort_flag, to);
-          if (!ok) break;
-          arrive_cluster(peer_addr(bars + kBVF + b, 0));
-        }
-        if (!ok) {
-          set_status(p.status, CPATTN_ERR_TIMEOUT);
-          *abort_flag = 1;
-          store_cluster_u32(peer_abort, 1);
-        }
-      }
-    }
+    // ---------------------------------------------- MMA issuer (even CTA) --
+    if (lane == 0 && n_kv > 0 && rank == 0)
+      mla2_mma_issue(p, smem, tmem_base, n_kv, bars, abort_flag, peer_abort);
   } else {
     // ------------------------------------------------------------- softmax --
     const int row = warp * 32 + lane;
@@ -580,25 +462,20 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   }
 
-  // ---- teardown: drain own copies after an abort, meet, free TMEM ----
+  // ---- teardown: meet, let in-flight copies land after an abort, free ----
   tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0 && *abort_flag && n_kv > 0) {
-    // let this CTA's own TMA copies land before its shared memory is released
-    // (rank 0's copies complete on the pair barriers, rank 1's on its own)
-    if (issued[2]) mbar_wait(bars + (rank == 0 ? kBQ : kBLQ), 0, nullptr, to);
-    const int nk = issued[0], nv = issued[1];
-    for (int g = max(0, nk - kKSlots2); g < nk; ++g) {
-      const int slot = g % kKSlots2;
-      // the pair barrier of rank 0 also waits for the peer's relay; its own
-      // bytes are what matters here, so a bounded wait that may run out is fine
-      mbar_wait(bars + (rank == 0 ? kBKF : kBLK) + slot, (g / kKSlots2) & 1, nullptr, to);
+  cluster_sync_all();  // both CTAs have stopped issuing copies and MMAs
+  if (*abort_flag && n_kv > 0 && threadIdx.x == 0) {
+    // copies issued before the abort complete on barriers that may never be
+    // armed, so they cannot be waited for: give them time to land (a copy
+    // takes microseconds) before either CTA releases its shared memory
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
     }
-    for (int j = max(0, nv - 2); j < nv; ++j)
-      mbar_wait(bars + (rank == 0 ? kBVF : kBLV) + (j & 1), (j >> 1) & 1, nullptr, to);
   }
   __syncthreads();
-  cluster_sync_all();  // neither CTA frees memory the other's MMAs or arrivals still use
+  cluster_sync_all();  // neither CTA frees memory the other's MMAs or copies still use
   if (warp == 4) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512)
