@@ -372,7 +372,7 @@ def run_reference(args):
         return 0
     from context_causal_attention_cp_gb300 import workloads as W
 
-    w = W.WORKLOADS[args.workload]
+    w = W.WORKLOADS[args.workload or WORKLOAD]
     inputs = W.make_inputs(w)
     pool = OracleRows(w, inputs)
     times, flops, rows_done = [], 0.0, 0
@@ -525,7 +525,7 @@ def run_ours(args):
     launches = 0
 
     # ---- headline: the 32K workload ----
-    w = W.WORKLOADS[args.workload]
+    w = W.WORKLOADS[args.workload or WORKLOAD]
     strategy = w.strategies[0]
     inputs = W.make_inputs(w)
     main, step_ms, n, plan = bench_full_kv(w, strategy, inputs, dev, stream, pk, flush,
@@ -1098,7 +1098,7 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     status = cpa.new_status(dev)
     if args.profile_case == "partial_kv":
-        w = W.WORKLOADS[MERGE_WORKLOAD if args.workload == WORKLOAD else args.workload]
+        w = W.WORKLOADS[args.workload or MERGE_WORKLOAD]
         kv_block = w.kv_block or 8192
         inputs = W.make_inputs(w)
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", device=dev,
@@ -1156,7 +1156,7 @@ def run_profile_case(args):
         run = lambda: cpa.cp_lse_merge(po, pl, dst_rows=dst, out=out, lse_out=lse,  # noqa: E731
                                        num_out_rows=rows, status=status)
     else:
-        w = W.WORKLOADS[args.workload]
+        w = W.WORKLOADS[args.workload or WORKLOAD]
         inputs = W.make_inputs(w)
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], device=dev)
         q = cpa.cp_restore(inputs["q"].to(dev), plan.gather_idx[: w.total_new])
@@ -1192,7 +1192,9 @@ def main():
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--workload", default=None,
+                    help=f"workload of the headline line and of --profile-case attention "
+                         f"(default {WORKLOAD}; --profile-case partial_kv: {MERGE_WORKLOAD})")
     ap.add_argument("--ref-rows-per-step", type=int, default=128,
                     help="query rows (x all heads) the reference arm's oracle runs per step")
     ap.add_argument("--skip-cpu", action="store_true")

@@ -104,6 +104,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_trigger();  // a dependent merge may launch once every CTA is resident
 
   // ---- work item: (tile of 128 rows of one segment, group of NQ heads) ----
   const int hg = blockIdx.x % p.n_hgroups;
@@ -113,12 +114,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   cp_segment_t sg;
   int t, seg_id, kv_lo, kv_hi;
   long long out_row0;
-  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
-  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id) ||
+      !split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) {
+    grid_dep_wait();  // no CTA ends before the kernel this launch may overlap
+    return;
+  }
   // packed heads: BM / 2 query rows per head, two heads per tile
   const int HP = p.pack_heads ? 2 : 1;
   if (p.pack_heads && sg.q_len > BM / 2) {
     if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
+    grid_dep_wait();
     return;
   }
   const int r0 = t * BM;
@@ -300,7 +305,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
     const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
-    const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
+    // output row, computed before the KV loop (fewer live registers in the
+    // loop than at the store); split-KV mode: known only at the store
+    long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_col = s * BN, o_col = NQ * BN + s * DV;
     const float sl2 = p.scale_log2;
@@ -389,6 +396,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else {
       tc_fence_after();
+      if (p.split_block > 0) {
+        const long long w0 = split_slot_row0(p, sg, seg_id, jblk, out_row0);
+        out_row = (valid && w0 >= 0) ? w0 + r0 + row : -1;
+      }
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
       MergeCoef mc{0.f, inv, has ? (m_use + lg2_approx(l_run)) * kLn2 : -INFINITY};
@@ -480,6 +491,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 
   // ---- teardown ----
+  grid_dep_wait();  // (already returned in the epilogue unless this CTA aborted)
   tc_fence_before();
   __syncthreads();
   if (warp == C::kProducerWarp) {
@@ -515,8 +527,10 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   const long long grid = tiles * prm.n_hgroups;  // tiles x KV blocks (split mode) x head groups
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
-  kern<<<(unsigned)grid, C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, prm);
-  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return launch_kernel(kern, (unsigned)grid, C::kThreads, C::kSmemBytes, stream, prm.pdl != 0,
+                       mq, mk, mv, prm) == cudaSuccess
+             ? CPATTN_OK
+             : CPATTN_ERR_CUDA;
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 // bounded warp-uniform waits, TMEM and packed-fp32 helpers, work-item
 // resolution and tensor-map encoding.
 #pragma once
+#include <utility>
 #include <cstdint>
 #include <mutex>
 
@@ -67,6 +68,11 @@ struct AttnParams {
   // within the CTA's head group (which then spans 4 heads).  The Q tensor map
   // then has boxes of BM / 2 rows.  A longer segment sets CPATTN_ERR_RANGE.
   int pack_heads;
+  // pdl (host side): launch with programmatic stream serialization, so that
+  // the kernel's set-up and main loop overlap the kernel before it on the
+  // stream (split-KV mode, where that kernel writes only the slot table read
+  // by split_slot_row0).
+  int pdl;
 };
 
 // Number of split_block-key blocks a segment sees (key 0 is always visible).
@@ -199,7 +205,7 @@ __device__ __forceinline__ bool resolve_tile(const AttnParams& p, int tile_idx, 
 // window (or the segment's own, with seg_windows), output row = cat row -
 // out_row_base.  Split-KV mode: block j of the
 // segment's keys, output row = ws_slot[seg] + j * q_len + row-in-segment.
-// Returns false when the CTA has no block to do (or its slot is out of range).
+// Returns false when the CTA has no block to do.
 __device__ __forceinline__ bool split_window(const AttnParams& p, const cp_segment_t& sg, int seg_id,
                                              int j, int& kv_lo, int& kv_hi, long long& out_row0) {
   if (p.split_block <= 0) {
@@ -221,18 +227,31 @@ __device__ __forceinline__ bool split_window(const AttnParams& p, const cp_segme
   }
   kv_lo = j * p.split_block;
   kv_hi = kv_lo + p.split_block;
-  out_row0 = p.ws_slot[seg_id] + (long long)j * sg.q_len;
-  if (out_row0 < 0 || out_row0 + sg.q_len > p.ws_rows) {
-    if (threadIdx.x == 0) set_status(p.status, CPATTN_ERR_RANGE);
-    return false;
-  }
+  out_row0 = -1;  // the workspace slot is read by split_slot_row0 before the store
   return true;
+}
+
+// Split-KV mode: workspace row of segment row 0 of block j, read from the
+// slot table that the layout kernel before this launch writes (the launch may
+// overlap that kernel, so the read waits for it), or -1 with CPATTN_ERR_RANGE
+// when the slot is out of range.  Normal mode: out_row0 unchanged.
+__device__ __forceinline__ long long split_slot_row0(const AttnParams& p, const cp_segment_t& sg,
+                                                     int seg_id, int j, long long out_row0) {
+  if (p.split_block <= 0) return out_row0;
+  grid_dep_wait();
+  const long long r = p.ws_slot[seg_id] + (long long)j * sg.q_len;
+  if (r < 0 || r + sg.q_len > p.ws_rows) {
+    set_status(p.status, CPATTN_ERR_RANGE);
+    return -1;
+  }
+  return r;
 }
 
 // Output row of row `row` of query tile r0 of segment sg (normal mode), or -1
 // with CPATTN_ERR_RANGE when the destination index is out of range.
 __device__ __forceinline__ long long output_row(const AttnParams& p, const cp_segment_t& sg,
                                                 int r0, int row, long long out_row0) {
+  if (out_row0 < 0) return -1;  // split-KV slot out of range (status already set)
   if (!p.dst_rows) return out_row0 + r0 + row;
   const long long d = __ldg(p.dst_rows + sg.q_row0 + r0 + row);
   if (d < 0 || d >= p.dst_limit) {
@@ -302,6 +321,27 @@ inline bool make_map(CUtensorMap* m, const void* base, int cols, int heads, long
 
 
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch `kern` on `stream`, with programmatic stream serialization when pdl
+// is set (the kernel may then start before the previous kernel on the stream
+// has finished; see grid_dep_wait).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block,
+                                 size_t smem, cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Absorbed-MLA variant (d = 576, dv = 512 with V the first 512 columns of K);
 // defined in attn_mla.cu.

@@ -201,6 +201,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   volatile int* issued_n = reinterpret_cast<volatile int*>(tmem_slot + 2);  // non-V loads issued
   volatile int* issued_v = reinterpret_cast<volatile int*>(tmem_slot + 3);  // V loads issued
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_trigger();  // a dependent merge may launch once every CTA is resident
 
   // ---- work item: (128-row tile [, KV block], query head, output half) ----
   const int half = blockIdx.x & 1;
@@ -211,8 +212,11 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   cp_segment_t sg;
   int t, seg_id, kv_lo, kv_hi;
   long long out_row0;
-  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
-  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id) ||
+      !split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) {
+    grid_dep_wait();  // no CTA ends before the kernel this launch may overlap
+    return;
+  }
   const int r0 = t * BM;
   const int rows_valid = min(BM, sg.q_len - r0);
   const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
@@ -307,7 +311,6 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const bool valid = row < rows_valid;
     const int pos = valid ? sg.q_pos0 + (r0 + row) * sg.q_pos_step : -1;
     const int row_hi = valid ? (kv_hi < 0 ? pos + 1 : min(kv_hi, pos + 1)) : 0;
-    const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
     const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f, m_use = 0.f;
@@ -417,6 +420,8 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
     } else {
       tc_fence_after();
+      out_row0 = split_slot_row0(p, sg, seg_id, jblk, out_row0);
+      const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
       const bool acc_mode = p.lse_acc != nullptr;
@@ -471,6 +476,7 @@ attn_mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 
   tc_fence_before();
+  grid_dep_wait();  // (already returned in the epilogue unless this CTA aborted)
   __syncthreads();
   if (warp == 4) {
     if (lane == 0 && *abort_flag && n_kv > 0) {
@@ -517,8 +523,10 @@ int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_
   const long long grid = tiles * prm.Hq * 2;  // tiles x KV blocks (split mode) x heads x halves
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
-  attn_mla_kernel<<<(unsigned)grid, kThreadsM, kSmemM, stream>>>(mq, mk, prm);
-  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return launch_kernel(attn_mla_kernel, (unsigned)grid, kThreadsM, kSmemM, stream, prm.pdl != 0,
+                       mq, mk, prm) == cudaSuccess
+             ? CPATTN_OK
+             : CPATTN_ERR_CUDA;
 }
 
 }  // namespace cpattn

@@ -161,6 +161,7 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_trigger();  // a dependent merge may launch once every CTA is resident
   const uint32_t rank = cluster_rank();
   const uint32_t peer = rank ^ 1u;
   const uint32_t peer_abort = peer_addr((const void*)abort_flag, peer);
@@ -179,8 +180,11 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   int t, seg_id, kv_lo, kv_hi;
   long long out_row0;
   // both CTAs of a pair resolve the same tile and window, so they leave together
-  if (!resolve_tile(p, tile_idx, sg, t, seg_id)) return;
-  if (!split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) return;
+  if (!resolve_tile(p, tile_idx, sg, t, seg_id) ||
+      !split_window(p, sg, seg_id, jblk, kv_lo, kv_hi, out_row0)) {
+    grid_dep_wait();  // no CTA ends before the kernel this launch may overlap
+    return;
+  }
   const int r0 = t * BM;
   const int rows_valid = min(BM, sg.q_len - r0);
   const int pos_max = sg.q_pos0 + (r0 + rows_valid - 1) * sg.q_pos_step;
@@ -409,6 +413,7 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     } else {
       tc_fence_after();
+      out_row0 = split_slot_row0(p, sg, seg_id, jblk, out_row0);
       const long long out_row = valid ? output_row(p, sg, r0, row, out_row0) : -1;
       const bool has = l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
@@ -463,6 +468,7 @@ attn_mla_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 
   // ---- teardown: meet, let in-flight copies land after an abort, free ----
+  grid_dep_wait();  // (already returned in the epilogue unless this CTA aborted)
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // both CTAs have stopped issuing copies and MMAs
@@ -508,8 +514,10 @@ int launch_attn_mla_pair(const void* q, int num_q_rows, const void* k, int64_t k
   const long long grid = tiles * (prm.Hq / 2) * 2 * 2;
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;
-  attn_mla_pair_kernel<<<(unsigned)grid, kThreads2, kSmem2, stream>>>(mq, mk, mv, prm);
-  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return launch_kernel(attn_mla_pair_kernel, (unsigned)grid, kThreads2, kSmem2, stream,
+                       prm.pdl != 0, mq, mk, mv, prm) == cudaSuccess
+             ? CPATTN_OK
+             : CPATTN_ERR_CUDA;
 }
 
 }  // namespace cpattn

@@ -84,6 +84,7 @@ pkv_layout_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_bl
                   int max_blocks, long long cap_rows, long long* __restrict__ slot,
                   long long* __restrict__ rows_before, long long* __restrict__ total,
                   int32_t* status) {
+  grid_dep_trigger();  // the attention launch may start its loads and MMAs now
   __shared__ long long buf[33];
   long long slot_carry = 0, row_carry = 0;
   for (int c0 = 0; c0 < num_segs; c0 += kLayoutThreads) {
@@ -280,6 +281,7 @@ pkv_merge_kernel(const cp_segment_t* __restrict__ segs, int num_segs, int kv_blo
                  int Hq, int dv, int num_q_rows, const int32_t* __restrict__ dst_rows,
                  void* __restrict__ o_out, float* __restrict__ lse_out, int num_out_rows,
                  int hs, int32_t* status) {
+  grid_dep_wait();  // the attention launch before this one wrote the partials
   const int lane = threadIdx.x & 31;
   const int nslices = (Hq + hs - 1) / hs;
   const long long total_tasks = rows_before[num_segs] * nslices;
@@ -458,6 +460,9 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
   prm.ws_slot = slot;
   prm.ws_rows = L.cap_rows;
   prm.pack_heads = (max_seg_rows >= 1 && max_seg_rows <= BM / 2) ? 1 : 0;
+  // the attention overlaps the layout kernel (it reads the slot table only
+  // before its stores), and the merge's launch overlaps the attention's tail
+  prm.pdl = 1;
   int rc = attn_launch(segs_dev, num_segs, tiles_dev, num_tiles, q, num_q_rows, k, k_row_stride,
                        k_head_stride, v, v_row_stride, v_head_stride, num_kv_rows, Hq, Hkv, d, dv,
                        scale, prm, stream);
@@ -475,13 +480,14 @@ extern "C" int cp_attn_partial_kv(const cp_segment_t* segs_dev, int num_segs,
   const int grid = (int)std::max<long long>(
       1, std::min<long long>((long long)num_sms() * 2 * 8,
                              (tasks + kMergeThreadsP / 32 - 1) / (kMergeThreadsP / 32)));
-  if (o_is_fp32)
-    pkv_merge_kernel<true><<<grid, kMergeThreadsP, 0, stream>>>(
-        segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
-        o_out, lse_out, num_out_rows, hs, status_dev);
-  else
-    pkv_merge_kernel<false><<<grid, kMergeThreadsP, 0, stream>>>(
-        segs_dev, num_segs, kv_block, slot, rows_before, ws_o, ws_l, L.cap_rows, Hq, dv, num_q_rows, dst_rows,
-        o_out, lse_out, num_out_rows, hs, status_dev);
-  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  const long long* slot_c = slot;
+  const long long* rows_c = rows_before;
+  const float* ws_o_c = ws_o;
+  const float* ws_l_c = ws_l;
+  const cudaError_t e =
+      launch_kernel(o_is_fp32 ? pkv_merge_kernel<true> : pkv_merge_kernel<false>, (unsigned)grid,
+                    kMergeThreadsP, 0, stream, true, segs_dev, num_segs, kv_block, slot_c, rows_c,
+                    ws_o_c, ws_l_c, L.cap_rows, Hq, dv, num_q_rows, dst_rows, o_out, lse_out,
+                    num_out_rows, hs, status_dev);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }

@@ -203,6 +203,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ------------------------------------------ programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it on the stream is still running.  grid_dep_wait() blocks
+// until that kernel has completed and its memory writes are visible (it
+// returns at once when the launch was an ordinary one); every read of that
+// kernel's results must come after it.  grid_dep_trigger() lets such a
+// dependent kernel be scheduled once every CTA of this grid has issued it or
+// exited, so that its launch overlaps this grid's tail.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }

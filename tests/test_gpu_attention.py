@@ -340,8 +340,8 @@ def test_merge_sweep_interleaved_kv_shards():
 
 # ------------------------------------------------- bounded pipeline waits ----
 
-@pytest.mark.parametrize("shape", [(2, 1, 128, 128), (1, 1, 64, 64), (1, 1, 576, 512),
-                                   (2, 1, 576, 512)])
+@pytest.mark.parametrize("shape", [(2, 1, 128, 128), (4, 1, 128, 128), (1, 1, 64, 64),
+                                   (1, 1, 576, 512), (2, 1, 576, 512)])
 def test_wait_limit_reports_timeout_and_context_survives(shape):
     """With the query load withheld, the MMA thread's wait runs out: the kernel
     reports CPATTN_ERR_TIMEOUT, drains its own copies, frees TMEM and returns.
