@@ -285,6 +285,19 @@ def test_mla_small_all_rows(seed):
         assert_attn_close(o, lse, O_ref, L_ref, f"mla/{strategy}")
 
 
+def test_mla_small_odd_head_count_all_rows():
+    """An odd number of query heads runs on the single-SM MLA kernel (the pair
+    kernel needs head pairs)."""
+    w = mla_case([190, 61], [0, 17], 3, 4, 905)
+    inputs = W.make_inputs(w)
+    k64 = np64(inputs["k"])
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), k64, k64[:, :, :512],
+                                               w.new_lens, w.prefix_lens, w.scale)
+    for strategy in w.strategies:
+        o, lse = run_full_kv(w, strategy, inputs)
+        assert_attn_close(o, lse, O_ref, L_ref, f"mla-odd/{strategy}")
+
+
 def test_mla_16k_sampled():
     w = W.WORKLOADS["mla_16k"]
     inputs = W.make_inputs(w)
