@@ -110,9 +110,6 @@ __device__ __forceinline__ void tma_load_pair(void* smem_dst, const void* tmap, 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 }  // namespace pair
 }  // namespace cpattn
