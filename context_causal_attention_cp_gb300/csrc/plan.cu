@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "../../include/cpattn.h"
+#include "attn_common.cuh"
 #include "ptx.cuh"
 #include "trace.h"
 
@@ -54,17 +55,59 @@ __device__ int block_excl_scan(int v, int* scratch /* >= 33 ints */, int* total)
   return res;
 }
 
-struct ReqInfo {
-  int n, p, flat0, kv0;
-};
+// Block-wide exclusive scan of four ints per thread at once (any multiple of
+// 32 threads up to 1024): one pass of warp shuffles and two barriers for all
+// four.  v[] is replaced by its exclusive prefixes, total[] by the block sums.
+__device__ void block_excl_scan4(int (&v)[4], int4* scratch /* >= 33 */, int (&total)[4]) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+  }
+  if (lane == 31) scratch[wid] = make_int4(x[0], x[1], x[2], x[3]);
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = (int)(blockDim.x >> 5);
+    const int4 w4 = lane < nw ? scratch[lane] : make_int4(0, 0, 0, 0);
+    int w[4] = {w4.x, w4.y, w4.z, w4.w}, sacc[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int y = __shfl_up_sync(0xffffffffu, sacc[k], o);
+        if (lane >= o) sacc[k] += y;
+      }
+    }
+    scratch[lane] = make_int4(sacc[0] - w[0], sacc[1] - w[1], sacc[2] - w[2], sacc[3] - w[3]);
+    if (lane == 31) scratch[32] = make_int4(sacc[0], sacc[1], sacc[2], sacc[3]);
+  }
+  __syncthreads();
+  const int4 off = scratch[wid], tot = scratch[32];
+  v[0] = off.x + x[0] - v[0];
+  v[1] = off.y + x[1] - v[1];
+  v[2] = off.z + x[2] - v[2];
+  v[3] = off.w + x[3] - v[3];
+  total[0] = tot.x;
+  total[1] = tot.y;
+  total[2] = tot.z;
+  total[3] = tot.w;
+  __syncthreads();
+}
 
-// Kernel 1: one CTA writes every segment plus the rank offsets.
+// Kernel 1: one CTA (a multiple of 32 threads, up to 1024, sized to the
+// request count) writes every segment plus the rank offsets.
 __global__ void __launch_bounds__(kPlanThreads)
 plan_segments_kernel(const int32_t* __restrict__ new_lens, const int32_t* __restrict__ prefix_lens,
                      int num_reqs, int C, int strategy, int total_rows, int total_segs,
                      cp_segment_t* __restrict__ segs, int32_t* __restrict__ seg_offsets,
                      int32_t* __restrict__ row_offsets, int32_t* status) {
-  __shared__ int scan_buf[33];
+  grid_dep_trigger();  // the row and tile kernels may launch and wait for this one
+  __shared__ int4 scan_buf[33];
   int row_base = 0, seg_base = 0;  // identical in every thread
   for (int r = 0; r < C; ++r) {
     if (threadIdx.x == 0) {
@@ -72,7 +115,7 @@ plan_segments_kernel(const int32_t* __restrict__ new_lens, const int32_t* __rest
       seg_offsets[r] = seg_base;
     }
     int flat_carry = 0, kv_carry = 0, row_carry = 0, seg_carry = 0;
-    for (int c0 = 0; c0 < num_reqs; c0 += kPlanThreads) {
+    for (int c0 = 0; c0 < num_reqs; c0 += (int)blockDim.x) {
       const int b = c0 + threadIdx.x;
       const bool valid = b < num_reqs;
       int n = valid ? new_lens[b] : 0;
@@ -82,11 +125,24 @@ plan_segments_kernel(const int32_t* __restrict__ new_lens, const int32_t* __rest
         n = 0;
         p = 0;
       }
-      int tot;
-      const int flat0 = flat_carry + block_excl_scan(n, scan_buf, &tot);
-      flat_carry += tot;
-      const int kv0 = kv_carry + block_excl_scan(n + p, scan_buf, &tot);
-      kv_carry += tot;
+      // the request's flat start, KV start, and (below) its rows and segments
+      // on rank r, as prefix sums over the batch; the flat start decides the
+      // interleave counts, so it is scanned first
+      int sc[4] = {n, n + p, 0, 0}, tot[4];
+      if (strategy == CP_INTERLEAVE) {
+        block_excl_scan4(sc, scan_buf, tot);
+      } else {
+        // zigzag counts do not depend on the flat start: one scan for all four
+        const int nb = 2 * C, base = n / nb, rem = n % nb, kl = nb - 1 - r;
+        const int e0 = base + (r < rem ? 1 : 0), l0 = base + (kl < rem ? 1 : 0);
+        sc[2] = e0 + l0;
+        sc[3] = (e0 > 0) + (l0 > 0);
+        block_excl_scan4(sc, scan_buf, tot);
+      }
+      const int flat0 = flat_carry + sc[0];
+      flat_carry += tot[0];
+      const int kv0 = kv_carry + sc[1];
+      kv_carry += tot[1];
       int rows_b = 0, segs_b = 0;
       int e = 0, l = 0, st_e = 0, st_l = 0, i0 = 0;
       if (strategy == CP_ZIGZAG) {
@@ -105,10 +161,20 @@ plan_segments_kernel(const int32_t* __restrict__ new_lens, const int32_t* __rest
         segs_b = cnt > 0;
         e = cnt;
       }
-      const int row_in_rank = row_carry + block_excl_scan(rows_b, scan_buf, &tot);
-      row_carry += tot;
-      const int seg_in_rank = seg_carry + block_excl_scan(segs_b, scan_buf, &tot);
-      seg_carry += tot;
+      int row_in_rank, seg_in_rank;
+      if (strategy == CP_INTERLEAVE) {
+        int sc2[4] = {rows_b, segs_b, 0, 0}, tot2[4];
+        block_excl_scan4(sc2, scan_buf, tot2);
+        row_in_rank = row_carry + sc2[0];
+        row_carry += tot2[0];
+        seg_in_rank = seg_carry + sc2[1];
+        seg_carry += tot2[1];
+      } else {
+        row_in_rank = row_carry + sc[2];
+        row_carry += tot[2];
+        seg_in_rank = seg_carry + sc[3];
+        seg_carry += tot[3];
+      }
       if (valid) {
         int si = seg_base + seg_in_rank;
         if (si + segs_b > total_segs) {
@@ -144,6 +210,8 @@ __global__ void plan_rows_kernel(const cp_segment_t* __restrict__ segs, int tota
                                  int total_rows, int32_t* __restrict__ gather_idx,
                                  int32_t* __restrict__ positions, int32_t* __restrict__ restore_idx,
                                  int32_t* status) {
+  grid_dep_wait();  // the segment kernel before this launch wrote segs
+  grid_dep_trigger();
   for (int row = blockIdx.x * blockDim.x + threadIdx.x; row < total_rows;
        row += gridDim.x * blockDim.x) {
     int lo = 0, hi = total_segs;  // last segment with q_row0 <= row
@@ -170,6 +238,7 @@ constexpr int kTileBins = 4096;
 __global__ void __launch_bounds__(kPlanThreads)
 plan_tiles_kernel(const cp_segment_t* __restrict__ segs, int total_segs, int total_tiles,
                   int32_t* __restrict__ tiles, int32_t* status) {
+  grid_dep_wait();  // the kernels before this launch wrote segs
   __shared__ int hist[kTileBins];
   __shared__ int scan_buf[33];
   for (int i = threadIdx.x; i < kTileBins; i += blockDim.x) hist[i] = 0;
@@ -294,20 +363,29 @@ extern "C" int cp_shard_plan(const int32_t* new_lens_dev, const int32_t* prefix_
       misaligned(positions_dev) || misaligned(restore_idx_dev) || misaligned(tiles_dev) ||
       misaligned(seg_offsets_dev) || misaligned(row_offsets_dev) || misaligned(status_dev))
     return CPATTN_ERR_ALIGNMENT;
-  plan_segments_kernel<<<1, kPlanThreads, 0, stream>>>(new_lens_dev, prefix_lens_dev, num_reqs,
-                                                       cp_size, strategy, total_rows, total_segs,
-                                                       segs_dev, seg_offsets_dev, row_offsets_dev,
-                                                       status_dev);
+  // one warp per 32 requests (at least one, at most the 1024-thread block)
+  const int seg_threads = std::min(kPlanThreads, std::max(32, (num_reqs + 31) / 32 * 32));
+  plan_segments_kernel<<<1, seg_threads, 0, stream>>>(new_lens_dev, prefix_lens_dev, num_reqs,
+                                                      cp_size, strategy, total_rows, total_segs,
+                                                      segs_dev, seg_offsets_dev, row_offsets_dev,
+                                                      status_dev);
+  if (cudaGetLastError() != cudaSuccess) return CPATTN_ERR_CUDA;
+  // the row and tile kernels are launched to overlap the kernel before them
+  // and wait for it before their first read (programmatic dependent launch)
   if (total_rows > 0 && total_segs > 0) {
     const int threads = 256;
     const int blocks = (int)std::min<long long>(((long long)total_rows + threads - 1) / threads, 4096);
-    plan_rows_kernel<<<blocks, threads, 0, stream>>>(segs_dev, total_segs, total_rows,
-                                                     gather_idx_dev, positions_dev,
-                                                     restore_idx_dev, status_dev);
+    const cp_segment_t* segs_c = segs_dev;
+    if (launch_kernel(plan_rows_kernel, (unsigned)blocks, threads, 0, stream, true, segs_c,
+                      total_segs, total_rows, gather_idx_dev, positions_dev, restore_idx_dev,
+                      status_dev) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
   }
   if (tiles_dev && total_tiles > 0) {
-    plan_tiles_kernel<<<1, kPlanThreads, 0, stream>>>(segs_dev, total_segs, total_tiles, tiles_dev,
-                                                      status_dev);
+    const cp_segment_t* segs_c = segs_dev;
+    if (launch_kernel(plan_tiles_kernel, 1u, kPlanThreads, 0, stream, true, segs_c, total_segs,
+                      total_tiles, tiles_dev, status_dev) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return CPATTN_OK;
 }
