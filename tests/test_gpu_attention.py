@@ -298,6 +298,74 @@ def test_mla_small_odd_head_count_all_rows():
         assert_attn_close(o, lse, O_ref, L_ref, f"mla-odd/{strategy}")
 
 
+# ------------------------------------------------- running max that moves ----
+
+def _growing_keys(w, inputs, grow_from=0):
+    """Scale every KV row of a request by 1 + pos/48 (pos = its position in
+    the request), columns [grow_from:] only, re-rounded to bf16: later keys
+    score higher, so the running row max keeps rising by more than the
+    lazy-max slack and every kernel's O-rescale path runs."""
+    k = inputs["k"].float()
+    kv0 = 0
+    for n, p in zip(w.new_lens, w.prefix_lens):
+        f = 1.0 + torch.arange(n + p, dtype=torch.float32) / 48.0
+        k[kv0: kv0 + n + p, :, grow_from:] *= f[:, None, None]
+        kv0 += n + p
+    out = dict(inputs)
+    out["k"] = k.to(torch.bfloat16)
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 2, 128), (3, 3, 128), (4, 2, 64), (2, 1, 576),
+                                      (1, 1, 576)])
+def test_running_max_moves_all_rows(Hq, Hkv, d):
+    """Keys whose scores grow along the sequence make the row max move by more
+    than the lazy-max slack many times; O is rescaled in tensor memory each
+    time (in the MLA pair kernel by both halves of every row).  All rows
+    against the oracle, both strategies: the two-head and one-head d = 128
+    kernels, d = 64, the MLA pair kernel (even head count) and the single-SM
+    MLA kernel (odd)."""
+    mla = d == 576
+    w = W.Workload(name=f"grow{Hq}x{d}", new_lens=[700, 130], prefix_lens=[100, 0], Hq=Hq,
+                   Hkv=Hkv, d=d, dv=512 if mla else d,
+                   scale=1 / math.sqrt(192 if mla else d), std=1.0, cp_size=2,
+                   strategies=["zigzag", "interleave"], seed=7300 + d + Hq,
+                   v_is_k_prefix=mla)
+    # MLA: grow only the rope columns, so that V (the latent) keeps its scale
+    inputs = _growing_keys(w, W.make_inputs(w), grow_from=512 if mla else 0)
+    k64 = np64(inputs["k"])
+    v64 = k64[:, :, :512] if mla else np64(inputs["v"])
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), k64, v64, w.new_lens,
+                                               w.prefix_lens, w.scale)
+    for strategy in w.strategies:
+        o, lse = run_full_kv(w, strategy, inputs)
+        assert_attn_close(o, lse, O_ref, L_ref, f"{w.name}/{strategy}")
+
+
+def test_running_max_moves_split_kv_and_packed_heads():
+    """The same growing keys through the split-KV call (blocks of 256 keys:
+    per-block partials, the fused merge) with and without two query heads
+    packed per tile (segments of at most 64 rows)."""
+    w = W.Workload(name="grow_split", new_lens=[500, 60], prefix_lens=[300, 0], Hq=8, Hkv=2,
+                   d=128, dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=8,
+                   strategies=["zigzag"], seed=7400)
+    inputs = _growing_keys(w, W.make_inputs(w))
+    O_ref, L_ref = oatt.dense_causal_attention(np64(inputs["q"]), np64(inputs["k"]),
+                                               np64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    status = cpa.new_status()
+    plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, "zigzag", status=status)
+    q, k, v = inputs["q"].cuda(), inputs["k"].cuda(), inputs["v"].cuda()
+    q_cat = cpa.cp_restore(q, plan.gather_idx[: w.total_new], status=status)
+    for packed in (False, True):
+        # zigzag blocks here have at most 32 rows: packing is allowed, 0 turns it off
+        o, lse, _ = cpa.cp_attn_partial_kv(plan, q_cat, k, v, w.scale, 256, status=status,
+                                           max_seg_rows=None if packed else 0)
+        torch.cuda.synchronize()
+        cpa.check_status(status, w.name)
+        assert_attn_close(o, lse, O_ref, L_ref, f"{w.name}/packed={packed}")
+
+
 def test_mla_16k_sampled():
     w = W.WORKLOADS["mla_16k"]
     inputs = W.make_inputs(w)
