@@ -138,20 +138,32 @@ def test_partialkv_128k_sampled():
 
 # --------------------------------------------------------------- partials ----
 
-def test_windowed_partials_and_empty_windows():
-    """cp_attn_partial in partial mode: fp32 O, windows, empty rows -> (0, -inf)."""
-    w = random_case(3, 4, 2, 128, max_new=500, max_prefix=50)
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 2, 128), (8, 8, 64), (2, 1, 576), (1, 1, 576)])
+def test_windowed_partials_and_empty_windows(Hq, Hkv, d):
+    """cp_attn_partial in partial mode: fp32 O, windows, empty rows -> (0, -inf);
+    every kernel family (MLA: the pair kernel for two heads, the single-SM
+    kernel for one)."""
+    mla = d == 576
+    if mla:
+        new, pre = W.random_batch(3, max_reqs=4, max_new=500, max_prefix=50)
+        w = W.Workload(name="win_mla", new_lens=new, prefix_lens=pre, Hq=Hq, Hkv=Hkv, d=576,
+                       dv=512, scale=1 / math.sqrt(192), std=0.5, cp_size=2,
+                       strategies=["zigzag"], seed=5103, v_is_k_prefix=True)
+    else:
+        w = random_case(3, Hq, Hkv, d, max_new=500, max_prefix=50)
     inputs = W.make_inputs(w)
     status = cpa.new_status()
     plan = cpa.make_plan(w.new_lens, w.prefix_lens, 2, "zigzag", status=status)
     N = w.total_new
     q_cat = cpa.cp_restore(inputs["q"].cuda(), plan.gather_idx[:N], status=status)
-    k, v = inputs["k"].cuda(), inputs["v"].cuda()
+    k = inputs["k"].cuda()
+    v = k[:, :, :512] if mla else inputs["v"].cuda()
     op = oplan.make_plan(w.new_lens, w.prefix_lens, 2, "zigzag")
     pos = np.asarray(op.positions)
     kv0 = np.asarray([oatt.token_tables(w.new_lens, w.prefix_lens)[1][i] for i in op.gather_idx])
     q64 = np64(inputs["q"])[np.asarray(op.gather_idx)]
-    k64, v64 = np64(inputs["k"]), np64(inputs["v"])
+    k64 = np64(inputs["k"])
+    v64 = k64[:, :, :512] if mla else np64(inputs["v"])
     for lo, hi in [(0, 100), (37, 300), (256, 384), (400, 10 ** 6), (10 ** 6, -1)]:
         o, lse = cpa.cp_attn_partial(plan.segs, q_cat, k, v, w.scale,
                                      num_segs=plan.total_segs, kv_lo=lo, kv_hi=hi,
