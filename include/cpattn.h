@@ -327,7 +327,10 @@ int cp_select_pass_cost(int64_t new_tokens, int64_t cached_tokens, int Hq, int H
  *     cp_partial_kv_workspace_size for the plan's lengths; its contents are
  *     overwritten.  Too small: CPATTN_ERR_INVALID_ARG in *status_dev and the
  *     partials that do not fit are skipped.
- * Three launches on the stream (layout, attention, merge). */
+ * Three launches on the stream (layout, attention, merge); the attention and
+ * the merge use programmatic dependent launch, so each may start while the
+ * launch before it in the call is still running (the layout kernel itself
+ * waits for earlier work on the stream like any launch). */
 /* Sizing (host only).  bytes: the workspace for the segments cp_shard_plan
  * makes from these lengths; max_blocks (nullable): the largest block count of
  * any segment, the value to pass to cp_attn_partial_kv; max_seg_rows
