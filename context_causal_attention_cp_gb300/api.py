@@ -11,7 +11,7 @@ Layouts (see include/cpattn.h):
 """
 
 from dataclasses import dataclass
-from typing import List, Optional, Sequence
+from typing import List, Sequence
 
 import ctypes
 import math

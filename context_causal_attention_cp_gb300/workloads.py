@@ -16,7 +16,7 @@ partial-KV (ring-style) decomposition plus a decode-style merge sweep.
 """
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import List, Optional
 
 import torch
