@@ -109,8 +109,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // ---- work item: (tile of 128 rows of one segment, group of NQ heads) ----
   const int hg = blockIdx.x % p.n_hgroups;
   const int rest = blockIdx.x / p.n_hgroups;
-  const int jblk = p.split_block > 0 ? rest % p.max_blocks : 0;
-  const int tile_idx = p.split_block > 0 ? rest / p.max_blocks : rest;
+  // split-KV mode: block-major (the grid is query-tile units x KV blocks x
+  // head groups), so that the CTAs running together read the same KV block:
+  // one block of every head fits L2, all blocks do not
+  const int tile_units = p.split_block > 0 ? (int)(gridDim.x / p.n_hgroups) / p.max_blocks : 1;
+  const int jblk = p.split_block > 0 ? rest / tile_units : 0;
+  const int tile_idx = p.split_block > 0 ? rest % tile_units : rest;
   cp_segment_t sg;
   int t, seg_id, kv_lo, kv_hi;
   long long out_row0;
