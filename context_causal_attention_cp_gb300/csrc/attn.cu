@@ -513,7 +513,9 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const AttnParams& prm, long long tiles, cudaStream_t stream) {
   using C = Cfg<D, DV, NQ, KST, VST>;
   auto kern = attn_fwd_kernel<D, DV, NQ, KST, VST>;
-  static int configured = 0;  // 1 ok, -1 refused
+  static PerDeviceState launch_state;
+  int scratch;
+  int& configured = launch_state.get(scratch);  // 1 ok, -1 refused
   if (configured == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)

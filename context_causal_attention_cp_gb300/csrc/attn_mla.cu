@@ -513,12 +513,14 @@ int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_
       !make_map(&mk, k, kD, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBNm))
     return CPATTN_ERR_CUDA;
   prm.q = q;
-  static bool configured = false;
+  static PerDeviceState launch_state;
+  int scratch;
+  int& configured = launch_state.get(scratch);
   if (!configured) {
     if (cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemM) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    configured = true;
+    configured = 1;
   }
   const long long grid = tiles * prm.Hq * 2;  // tiles x KV blocks (split mode) x heads x halves
   if (grid <= 0) return CPATTN_OK;
