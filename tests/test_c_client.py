@@ -1,8 +1,9 @@
-"""The boundary from plain C: a C99 program that includes include/cpattn.h,
-links libcpattn.so and calls its host-only entry points (no GPU needed).
-Checks that the header is valid C, the symbols link without Python, and the
+"""The boundary from plain C: C99 programs that include include/cpattn.h and
+link libcpattn.so.  The first calls the host-only entry points (no GPU
+needed): the header is valid C, the symbols link without Python, and the
 results agree with the oracle (SGLang docs, "Prefill Context Parallelism",
-§Zigzag strategy: 16 tokens over CP = 4 give 4 rows per rank)."""
+§Zigzag strategy: 16 tokens over CP = 4 give 4 rows per rank).  The second
+(GPU) runs the whole host-to-host step through cp_prefill_host."""
 
 import os
 import shutil
@@ -100,3 +101,128 @@ def test_c_program_links_and_calls_the_library(tmp_path):
     # decode over a long cache: pass-Q exposes less
     assert out[5] == f"cost {L.PASS_Q} 1"
     assert out[6].startswith("prefill_ws 0 ") and int(out[6].split()[2]) > 2 * 16 * 8 * 64 * 2
+
+
+C_PREFILL = r"""
+#include <stdio.h>
+#include <stdlib.h>
+#include <cuda_runtime_api.h>
+#include "cpattn.h"
+
+static int rd(const char* dir, const char* name, void* dst, size_t n) {
+  char path[4096];
+  snprintf(path, sizeof path, "%s/%s", dir, name);
+  FILE* f = fopen(path, "rb");
+  if (!f) return -1;
+  size_t got = fread(dst, 1, n, f);
+  fclose(f);
+  return got == n ? 0 : -1;
+}
+static int wr(const char* dir, const char* name, const void* src, size_t n) {
+  char path[4096];
+  snprintf(path, sizeof path, "%s/%s", dir, name);
+  FILE* f = fopen(path, "wb");
+  if (!f) return -1;
+  size_t put = fwrite(src, 1, n, f);
+  fclose(f);
+  return put == n ? 0 : -1;
+}
+
+int main(int argc, char** argv) {
+  if (argc < 2) return 10;
+  const char* dir = argv[1];
+  int32_t new_lens[2] = {300, 77}, prefix_lens[2] = {0, 40};
+  const int Hq = 8, Hkv = 2, d = 128, dv = 128, C = 2, N = 377, KV = 417;
+  const float scale = 0.08838834764831845f;
+  const size_t qb = (size_t)N * Hq * d * 2, kb = (size_t)KV * Hkv * d * 2;
+  const size_t vb = (size_t)KV * Hkv * dv * 2, ob = (size_t)N * Hq * dv * 2;
+  const size_t lb = (size_t)N * Hq * 4;
+  void *q, *k, *v, *o0, *o1;
+  float *l0, *l1;
+  if (cudaMallocHost(&q, qb) || cudaMallocHost(&k, kb) || cudaMallocHost(&v, vb) ||
+      cudaMallocHost(&o0, ob) || cudaMallocHost(&o1, ob) || cudaMallocHost((void**)&l0, lb) ||
+      cudaMallocHost((void**)&l1, lb))
+    return 11;
+  if (rd(dir, "q.bin", q, qb) || rd(dir, "k.bin", k, kb) || rd(dir, "v.bin", v, vb)) return 12;
+  int64_t ws_bytes = 0;
+  int rc = cp_prefill_host_workspace_size(new_lens, prefix_lens, 2, C, CP_ZIGZAG, Hq, Hkv, d,
+                                          dv, 0, &ws_bytes);
+  if (rc != CPATTN_OK) return 13;
+  void* ws = NULL;
+  int32_t* st = NULL;
+  if (cudaMalloc(&ws, (size_t)ws_bytes) || cudaMalloc((void**)&st, 4) || cudaMemset(st, 0, 4))
+    return 14;
+  cudaStream_t s[3];
+  for (int i = 0; i < 3; ++i)
+    if (cudaStreamCreate(&s[i])) return 15;
+  /* two batches with the same inputs: both buffer sets, overlapped streams */
+  const void* qs[2] = {q, q};
+  const void* ks[2] = {k, k};
+  const void* vs[2] = {v, v};
+  void* os[2] = {o0, o1};
+  float* ls[2] = {l0, l1};
+  rc = cp_prefill_host(new_lens, prefix_lens, 2, C, CP_ZIGZAG, Hq, Hkv, d, dv, scale, 0, 2, qs,
+                       ks, vs, os, ls, ws, ws_bytes, st, s[0], s[1], s[2]);
+  if (cudaDeviceSynchronize()) return 16;
+  int32_t status = -1;
+  if (cudaMemcpy(&status, st, 4, cudaMemcpyDeviceToHost)) return 17;
+  if (wr(dir, "o0.bin", o0, ob) || wr(dir, "o1.bin", o1, ob) || wr(dir, "l0.bin", l0, lb) ||
+      wr(dir, "l1.bin", l1, lb))
+    return 18;
+  printf("prefill %d %d\n", rc, status);
+  return 0;
+}
+"""
+
+
+@pytest.mark.gpu
+def test_c_program_runs_the_host_to_host_prefill(tmp_path):
+    """The whole step from a plain C program: pinned host q / k / v in,
+    cp_prefill_host (plan, attention, copies on three streams, two batches),
+    host O / LSE out; no Python on the path.  Both batches against the
+    oracle on every row."""
+    import math
+
+    import numpy as np
+    import torch
+
+    from context_causal_attention_cp_gb300 import workloads as W
+    from oracle import attention as oatt
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    L.load()
+    lib_dir = os.path.dirname(L.LIB_PATH)
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    w = W.Workload(name="c_prefill", new_lens=[300, 77], prefix_lens=[0, 40], Hq=8, Hkv=2,
+                   d=128, dv=128, scale=1 / math.sqrt(128), std=1.0, cp_size=2,
+                   strategies=["zigzag"], seed=4244)
+    inputs = W.make_inputs(w)
+    for name in ("q", "k", "v"):
+        inputs[name].contiguous().view(torch.int16).numpy().tofile(str(tmp_path / f"{name}.bin"))
+    src = tmp_path / "prefill.c"
+    src.write_text(C_PREFILL)
+    exe = tmp_path / "prefill"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda_home, "include"), str(src), "-o", str(exe), "-L",
+                    lib_dir, "-lcpattn", "-L", os.path.join(cuda_home, "lib64"), "-lcudart",
+                    "-Wl,-rpath," + lib_dir, "-Wl,-rpath," + os.path.join(cuda_home, "lib64")],
+                   check=True)
+    out = subprocess.run([str(exe), str(tmp_path)], check=True, capture_output=True,
+                         text=True).stdout.split()
+    assert out == ["prefill", str(L.OK), "0"]
+
+    def f64(t):
+        return t.float().numpy().astype(np.float64)
+
+    O_ref, L_ref = oatt.dense_causal_attention(f64(inputs["q"]), f64(inputs["k"]),
+                                               f64(inputs["v"]), w.new_lens, w.prefix_lens,
+                                               w.scale)
+    N, Hq, dv = w.total_new, w.Hq, w.dv
+    for b in (0, 1):
+        o = torch.from_numpy(np.fromfile(str(tmp_path / f"o{b}.bin"), dtype=np.int16))
+        o = f64(o.view(torch.bfloat16).reshape(N, Hq, dv))
+        lse = np.fromfile(str(tmp_path / f"l{b}.bin"), dtype=np.float32).reshape(N, Hq)
+        assert np.abs(o - O_ref).max() <= 2e-2
+        assert (np.abs(lse - L_ref) / np.maximum(1.0, np.abs(L_ref))).max() <= 1e-5
