@@ -723,7 +723,11 @@ def bench_128k(args, dev, stream, pk, status, clk):
                     "bytes_written": written, "parts": slot_rows // (N // 16),
                     "roofline": {"kernel": "lse_merge_kernel / lse_merge_batched_kernel",
                                  "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"],
-                                 "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None},
+                                 "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                                 "traffic": profiled_traffic("lse_merge_partialkv_128k.md"),
+                                 "traffic_unit": "bytes per average launch (ncu dram read + "
+                                                 "write, scaled by partials read)",
+                                 "algorithmic_bytes": (read + written) // len(slots)},
                     "note": "partials exceed L2 (18 GB), so every read comes from HBM"}
     del parts_o, parts_l
     torch.cuda.empty_cache()
@@ -973,7 +977,10 @@ def bench_merge_sweep(args, dev, stream, pk, clk):
             "roofline": {"kernel": "decode step (split-KV attention + merge)", "bound": "hbm",
                          "achieved": kv_bytes / (best_us * 1e-6) / 1e9, "peak": pk["hbm_gbs"],
                          "unit": "GB/s", "frac": kv_bytes / (best_us * 1e-6) / 1e9 / pk["hbm_gbs"],
-                         "traffic": None,
+                         "traffic": profiled_traffic("decode_step_one_merge_merge_sweep.md"),
+                         "traffic_unit": "bytes per call (ncu dram read + write of its three "
+                                         "launches, cold cache)",
+                         "algorithmic_bytes": kv_bytes,
                          "note": "K and V of all 65536 keys (268 MB) over the whole step"},
             "launches": launches,
             "path": "decode step: one cp_attn_split_kv over the 8 ranks' KV caches as one "
