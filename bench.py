@@ -50,7 +50,8 @@ MERGE_WORKLOAD = "partialkv_128k"
 DECODE_KV_BLOCK = 4096  # keys per CTA in the decode step (2 blocks per rank)
 ORACLE_SAMPLE_ROWS = 512  # rows x all heads when the oracle runs a sample of a workload
 # ncu summary under profiles/ holding the attention kernel's DRAM bytes per launch
-PROFILE_MD = {"llama8b_32k": "attn_fwd_llama8b_32k.md", "mla_16k": "attn_mla_mla_16k.md"}
+PROFILE_MD = {"llama8b_32k": "attn_fwd_llama8b_32k.md", "mla_16k": "attn_mla_mla_16k.md",
+              "d64_32k": "attn_fwd_d64_32k.md"}
 L2_NOTE = "flushed between steps (256 MiB write outside the step's events)"
 
 
@@ -525,7 +526,7 @@ def run_ours(args):
     launches = 0
 
     # ---- headline: the 32K workload ----
-    w = W.WORKLOADS[args.workload or WORKLOAD]
+    w = profile_workload(W, args.workload or WORKLOAD)
     strategy = w.strategies[0]
     inputs = W.make_inputs(w)
     main, step_ms, n, plan = bench_full_kv(w, strategy, inputs, dev, stream, pk, flush,
@@ -1078,11 +1079,24 @@ def bench_e2e(args, w, inputs, dev, world, clk):
                     "uploads and downloads overlap neighbouring steps' attention"}
 
 
+def profile_workload(W, name):
+    """A bench workload, or d64_32k: the 32K workload at d = dv = 64 (scale 1/8),
+    where a tile carries half the MMA work of d = 128 for the same number of
+    exponentials, so the exp unit rather than the tensor pipe may bind."""
+    if name == "d64_32k":
+        import dataclasses
+        return dataclasses.replace(
+            W.WORKLOADS["llama8b_32k"], name="d64_32k", d=64, dv=64, scale=0.125,
+            description="1 request, 32768 tokens, GQA 32/8, d=64, CP=8 zigzag (16 x 2048)")
+    return W.WORKLOADS[name]
+
+
 def run_profile_case(args):
     """One kernel, small case, for ncu: 3 warm-up launches then one launch.
 
     attention: the workload's attention launch as in the bench step (zigzag:
-               queries and outputs by token index; else restore store).
+               queries and outputs by token index; else restore store);
+               --workload d64_32k runs the 32K workload at d = 64.
     merge:     the heaviest query block of the 128K partial-KV workload
                (16 fp32 partials of 8192 rows x 32 heads x 128, 2.2 GB read).
     merge4:    query block 3 of that workload (4 partials, 0.54 GB read; the
@@ -1163,7 +1177,7 @@ def run_profile_case(args):
         run = lambda: cpa.cp_lse_merge(po, pl, dst_rows=dst, out=out, lse_out=lse,  # noqa: E731
                                        num_out_rows=rows, status=status)
     else:
-        w = W.WORKLOADS[args.workload or WORKLOAD]
+        w = profile_workload(W, args.workload or WORKLOAD)
         inputs = W.make_inputs(w)
         plan = cpa.make_plan(w.new_lens, w.prefix_lens, w.cp_size, w.strategies[0], device=dev)
         q = cpa.cp_restore(inputs["q"].to(dev), plan.gather_idx[: w.total_new])
@@ -1201,7 +1215,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None,
                     help=f"workload of the headline line and of --profile-case attention "
-                         f"(default {WORKLOAD}; --profile-case partial_kv: {MERGE_WORKLOAD})")
+                         f"(default {WORKLOAD}; --profile-case partial_kv: {MERGE_WORKLOAD}; "
+                         f"also d64_32k, the 32K workload at d = 64)")
     ap.add_argument("--ref-rows-per-step", type=int, default=128,
                     help="query rows (x all heads) the reference arm's oracle runs per step")
     ap.add_argument("--skip-cpu", action="store_true")
