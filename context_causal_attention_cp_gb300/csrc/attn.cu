@@ -513,23 +513,21 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const AttnParams& prm, long long tiles, cudaStream_t stream) {
   using C = Cfg<D, DV, NQ, KST, VST>;
   auto kern = attn_fwd_kernel<D, DV, NQ, KST, VST>;
-  static PerDeviceState launch_state;
-  int scratch;
-  int& configured = launch_state.get(scratch);  // 1 ok, -1 refused
-  if (configured == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
-      return CPATTN_ERR_CUDA;
+  if (!allow_smem(kern, C::kSmemBytes)) return CPATTN_ERR_CUDA;
+  // setmaxnreg.inc waits until the block's launch allocation can cover the
+  // split; refuse a build whose register count could not.  The count is a
+  // property of this binary, the same in every context: 0 not checked yet,
+  // 1 ok, -1 refused.
+  static int regs_ok = 0;
+  if (regs_ok == 0) {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return CPATTN_ERR_CUDA;
-    // setmaxnreg.inc waits until the block's launch allocation can cover the
-    // split; refuse a build whose register count could not.
-    configured = (!C::kSplitRegs || fa.numRegs * C::kThreads >=
-                                        C::kRegsOther * 128 + C::kRegsSoftmax * 256)
-                     ? 1
-                     : -1;
+    regs_ok = (!C::kSplitRegs ||
+               fa.numRegs * C::kThreads >= C::kRegsOther * 128 + C::kRegsSoftmax * 256)
+                  ? 1
+                  : -1;
   }
-  if (configured < 0) return CPATTN_ERR_UNSUPPORTED;
+  if (regs_ok < 0) return CPATTN_ERR_UNSUPPORTED;
   const long long grid = tiles * prm.n_hgroups;  // tiles x KV blocks (split mode) x head groups
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;

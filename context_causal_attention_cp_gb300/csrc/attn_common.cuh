@@ -322,19 +322,16 @@ inline bool make_map(CUtensorMap* m, const void* base, int cols, int heads, long
 
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launch configuration state of one kernel, per device (a kernel's dynamic
-// shared-memory attribute is set on each device separately): 0 not done yet,
-// 1 done, -1 refused.  Devices beyond the table get a fresh state every call.
-struct PerDeviceState {
-  static constexpr int kMaxDev = 64;
-  int state[kMaxDev] = {};
-  int& get(int& scratch) {
-    int dev = 0;
-    scratch = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return scratch;
-    return state[dev];
-  }
-};
+// Opt `kern` in to `smem` bytes of dynamic shared memory.  The attribute
+// belongs to the CUDA context that is current, so it is set on every launch
+// (a host-side call of about a microsecond): a new context on the device
+// (after cudaDeviceReset, or a caller's own context) never sees a launch
+// without it.
+template <typename... Params>
+inline bool allow_smem(void (*kern)(Params...), int smem) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+         cudaSuccess;
+}
 
 // Launch `kern` on `stream`, with programmatic stream serialization when pdl
 // is set (the kernel may then start before the previous kernel on the stream

@@ -513,15 +513,7 @@ int launch_attn_mla(const void* q, int num_q_rows, const void* k, int64_t k_row_
       !make_map(&mk, k, kD, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBNm))
     return CPATTN_ERR_CUDA;
   prm.q = q;
-  static PerDeviceState launch_state;
-  int scratch;
-  int& configured = launch_state.get(scratch);
-  if (!configured) {
-    if (cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemM) != cudaSuccess)
-      return CPATTN_ERR_CUDA;
-    configured = 1;
-  }
+  if (!allow_smem(attn_mla_kernel, kSmemM)) return CPATTN_ERR_CUDA;
   const long long grid = tiles * prm.Hq * 2;  // tiles x KV blocks (split mode) x heads x halves
   if (grid <= 0) return CPATTN_OK;
   if (grid > 0x7fffffffLL) return CPATTN_ERR_INVALID_ARG;

@@ -498,15 +498,7 @@ int launch_attn_mla_pair(const void* q, int num_q_rows, const void* k, int64_t k
       !make_map(&mk, k, kD2, Hkv, num_kv_rows, k_head_stride, k_row_stride, 64) ||
       !make_map(&mv, k, kD2, Hkv, num_kv_rows, k_head_stride, k_row_stride, kBN2))
     return CPATTN_ERR_CUDA;
-  static PerDeviceState launch_state;
-  int scratch;
-  int& configured = launch_state.get(scratch);
-  if (!configured) {
-    if (cudaFuncSetAttribute(attn_mla_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem2) != cudaSuccess)
-      return CPATTN_ERR_CUDA;
-    configured = 1;
-  }
+  if (!allow_smem(attn_mla_pair_kernel, kSmem2)) return CPATTN_ERR_CUDA;
   // tiles x KV blocks (split mode) x head pairs x halves x 2 CTAs
   const long long grid = tiles * (prm.Hq / 2) * 2 * 2;
   if (grid <= 0) return CPATTN_OK;
