@@ -373,7 +373,7 @@ def run_reference(args):
         return 0
     from context_causal_attention_cp_gb300 import workloads as W
 
-    w = W.WORKLOADS[args.workload or WORKLOAD]
+    w = profile_workload(W, args.workload or WORKLOAD)
     inputs = W.make_inputs(w)
     pool = OracleRows(w, inputs)
     times, flops, rows_done = [], 0.0, 0
