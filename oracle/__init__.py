@@ -25,7 +25,8 @@ Modules:
     merge      -- the log-sum-exp merge of partial results
     pipeline   -- plan -> per-shard partial -> [merge] -> restore, end to end;
                   the pass-Q ring (hop-by-hop merge into a carried accumulator)
-    select     -- the pass-KV / pass-Q choice (message sizes; fitted heuristic)
+    select     -- the pass-KV / pass-Q choice (message sizes; fitted heuristic;
+                  the roofline cost rule)
 
 Readings where the pages are silent:
     R1 remainder tokens of a zigzag split go one each to blocks 0..rem-1;
@@ -37,7 +38,14 @@ Readings where the pages are silent:
     R6 an empty partial has O = 0 and L = -inf, the identity of the merge;
     R7 pass-Q keeps each request's KV resident in 2C blocks split like the
        zigzag query blocks, rank r holding blocks r and 2C-1-r;
-    R8 the fitted switch heuristic uses natural logarithms of token counts.
+    R8 the fitted switch heuristic uses natural logarithms of token counts;
+    R9 the miss-rate threshold 2 Nkv / Nh compares one ring hop's messages
+       (T Hq query rows against K and V of T+P tokens), ties to pass-Q;
+    R10 the roofline rule prices, for one rank of a ring of C, the part of
+       each hop's message (and of pass-Q's All2All of partials) that does
+       not hide behind one C-th of the attention, pass-KV on a tie;
+    R11 pass-Q carries an accumulator round the ring (section 3.3.2); the
+       cost rule prices the All2All variant of section 3.5.
 The remainder placement (R1) and rank-local order (R2) are fixed by these
 readings only: "parity unpinned" by the pages beyond their even-split
 examples.  The fitted heuristic (R8) is "parity unpinned": the page's stated
